@@ -1,0 +1,121 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) online-softmax attention library.
+ *
+ * Two operations, both from the pages on online softmax and FlashAttention:
+ *
+ *  - fa_fwd / fa_fwd_dt: exact dense attention forward O = softmax(scale * Q K^T) V,
+ *    computed tile by tile with the online-softmax state (row max m, denominator l,
+ *    alpha = exp(m - m_new) rescaling both l and the O accumulator), so that the
+ *    N x N score matrix never reaches device memory.
+ *    ("Softmax 数值稳定性与 IO-Aware Attention：从在线归一化到 FlashAttention", §七,
+ *    the per-Q-tile loop; the 1/sqrt(d) factor as in "为什么 Flash Attention 算出来的
+ *    结果和标准注意力有微小差异？有损但值得", section "罪魁祸首是 online softmax 里那步
+ *    rescale".)
+ *
+ *  - online_softmax_rows: the per-row softmax state (m, l), m = max_t x_t,
+ *    l = sum_t exp(x_t - m), reduced thread -> warp shuffle -> shared memory -> first
+ *    warp with the merge rule m = max(m_a, m_b), l = l_a e^(m_a - m) + l_b e^(m_b - m).
+ *    (Same page, §四, §4.1 and §4.2.)
+ *
+ * Conventions common to every call:
+ *  - Every pointer passed to a compute call is a DEVICE pointer owned by the caller.
+ *    The library allocates no device memory: it keeps one status word per device in
+ *    static device memory.
+ *  - Calls are asynchronous on `stream` (0 = the legacy default stream). The return
+ *    value reports argument errors (checked on the host, nothing is launched) and
+ *    launch errors only. Errors the kernels detect while running (a bounded wait that
+ *    ran out) are reported by fa_last_device_error().
+ *  - Concurrent calls on different streams are allowed; the library keeps no
+ *    per-call host state.
+ */
+#ifndef ONLINE_SOFTMAX_07_GB300_FA_H
+#define ONLINE_SOFTMAX_07_GB300_FA_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = 1,      /* a null pointer, a negative size, len == 0 with rows > 0,
+                              a non-finite or non-positive scale, causal not 0/1     */
+  FA_ERR_UNSUPPORTED = 2,  /* head dimension or dtype outside what is built          */
+  FA_ERR_ALIGN = 3,        /* a pointer without the alignment the call needs         */
+  FA_ERR_CUDA = 4,         /* the CUDA runtime or driver returned an error           */
+  FA_ERR_TIMEOUT = 5       /* a kernel gave up a bounded wait (fa_last_device_error) */
+} fa_status;
+
+typedef enum {
+  FA_BF16 = 0,             /* q, k, v, o bf16; fp32 scores, softmax state and O accumulator */
+  FA_F32 = 1               /* q, k, v, o fp32; fp32 arithmetic on CUDA cores                */
+} fa_dtype;
+
+/*
+ * Attention forward, bf16.
+ *
+ * q, k, v: device, contiguous [B, H, N, d] bf16 (row-major; one N x d matrix per
+ *          head; K and V have the same N as Q). 16-byte aligned.
+ * o:       device, contiguous [B, H, N, d] bf16, written. 16-byte aligned.
+ * lse:     device fp32 [B, H, N], written with LSE_i = m_i + ln l_i = ln sum_j
+ *          exp(scale q_i.k_j) over the visible keys j; NULL = not written. 4-byte aligned.
+ * B, H, N: >= 0; any of them 0 is an empty problem (FA_OK, nothing launched).
+ * d:       64 or 128 (else FA_ERR_UNSUPPORTED).
+ * scale:   finite, > 0; multiplies the scores before the softmax (1/sqrt(d) usually).
+ * causal:  0 = no mask; 1 = key j visible to query i iff j <= i.
+ * Accuracy: scores, m, l and the O accumulator in fp32; P rounded to bf16 (round to
+ * nearest even) for the P.V product; O rounded to bf16 at the end.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal,
+                 cudaStream_t stream);
+
+/*
+ * Attention forward with an explicit element type. fa_fwd(...) is
+ * fa_fwd_dt(..., FA_BF16, stream). With FA_F32, q, k, v and o are fp32 [B, H, N, d]
+ * (4-byte aligned), d may be any value in 1..128, and all arithmetic is fp32 on CUDA
+ * cores (the same online-softmax tile loop, 32 keys per tile).
+ */
+fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int N, int d, float scale, int causal,
+                    fa_dtype dtype, cudaStream_t stream);
+
+/*
+ * Row online-softmax state.
+ *
+ * x:      device fp32 [rows, len], contiguous row-major; any 4-byte alignment (a row
+ *         may start at any float offset).
+ * m_out:  device fp32 [rows], written with m_r = max_t x[r, t].
+ * l_out:  device fp32 [rows], written with l_r = sum_t exp(x[r, t] - m_r).
+ * rows:   >= 0 (0 = nothing to do, FA_OK). len: >= 1 when rows > 0.
+ */
+fa_status online_softmax_rows(const float* x, float* m_out, float* l_out,
+                              int rows, int len, cudaStream_t stream);
+
+/* Static, never-NULL description of a status code. */
+const char* fa_status_str(fa_status status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word.
+ * Returns FA_ERR_TIMEOUT if a kernel launched since the last call gave up a bounded
+ * wait (it then skipped the rest of its work, so its outputs are not valid),
+ * FA_ERR_CUDA if the synchronisation failed, else FA_OK.
+ */
+fa_status fa_last_device_error(cudaStream_t stream);
+
+/*
+ * Self-test of the bounded-wait path: launches one block that waits on a
+ * shared-memory barrier nothing ever completes, with a time limit of `limit_ns`
+ * nanoseconds (1..2e9). The wait runs out, the kernel records the timeout in the
+ * status word and returns, leaving the context usable; fa_last_device_error() then
+ * returns FA_ERR_TIMEOUT. Not part of the method; it exists so that tests can check
+ * the timeout path without faulting or hanging the GPU.
+ */
+fa_status fa_selftest_wait_timeout(long long limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ONLINE_SOFTMAX_07_GB300_FA_H */

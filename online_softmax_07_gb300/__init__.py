@@ -1,0 +1,83 @@
+"""GB300 (sm_103a) online-softmax attention forward and row softmax state.
+
+The compute lives in ``lib/libosfa.so`` (hand-written CUDA, C ABI in include/fa.h);
+this package only binds it.  ``abi`` exposes the C calls by their C names; the two
+helpers below allocate outputs with torch and call them.  CPU tensors are copied
+to the GPU and the results copied back (the end-to-end path); the computation itself
+always runs in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import math
+
+from . import abi
+from .abi import FAError, fa_fwd, fa_fwd_dt, online_softmax_rows, fa_last_device_error
+
+__all__ = ["attention_forward", "row_state", "abi", "FAError", "fa_fwd", "fa_fwd_dt",
+           "online_softmax_rows", "fa_last_device_error"]
+
+
+def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=True):
+    """O = softmax(scale * Q K^T) V and LSE for [B, H, N, d] tensors (bf16 or fp32).
+
+    Returns (O, LSE) with O of q's dtype and LSE fp32 [B, H, N], on q's device.  For
+    CPU inputs the copies to and from the current CUDA device are part of the call
+    (pinned staging).  Everything is ordered on ``stream`` (a torch.cuda.Stream;
+    default: torch's current stream)."""
+    import torch
+
+    if stream is not None:
+        with torch.cuda.stream(stream):
+            return attention_forward(q, k, v, scale, causal, None, with_lse)
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must be [B, H, N, d] of one shape")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must all be bf16 or all fp32")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    host = not q.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        q, k, v = (t.contiguous().pin_memory().to(dev, non_blocking=True) for t in (q, k, v))
+    else:
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if with_lse else None
+    dtype = abi.FA_BF16 if q.dtype == torch.bfloat16 else abi.FA_F32
+    fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), dtype)
+    if host:
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        o_h.copy_(o, non_blocking=True)
+        lse_h = None
+        if lse is not None:
+            lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+            lse_h.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return o_h, lse_h
+    return o, lse
+
+
+def row_state(x, stream=None):
+    """Per-row (m, l) of an fp32 [rows, len] tensor: m = max, l = sum exp(x - m)."""
+    import torch
+
+    if stream is not None:
+        with torch.cuda.stream(stream):
+            return row_state(x, None)
+    if x.dim() != 2 or x.dtype != torch.float32:
+        raise ValueError("x must be an fp32 [rows, len] tensor")
+    host = not x.is_cuda
+    if host:
+        x = x.contiguous().pin_memory().to(torch.device("cuda", torch.cuda.current_device()),
+                                           non_blocking=True)
+    else:
+        x = x.contiguous()
+    rows, length = x.shape
+    m = torch.empty(rows, dtype=torch.float32, device=x.device)
+    l = torch.empty(rows, dtype=torch.float32, device=x.device)
+    online_softmax_rows(x, m, l, rows, length)
+    if host:
+        return m.cpu(), l.cpu()
+    return m, l

@@ -1,0 +1,119 @@
+"""ctypes binding of the C ABI in include/fa.h (argument marshalling only).
+
+The functions here carry the C names and signatures: ``fa_fwd``, ``fa_fwd_dt``,
+``online_softmax_rows``, ``fa_status_str``, ``fa_last_device_error`` and
+``fa_selftest_wait_timeout``.  Pointer arguments accept a CUDA ``torch.Tensor``
+(its data pointer is passed), an ``int`` address, or ``None`` (NULL).  A non-OK
+status raises :class:`FAError`.  Every computation runs in the library's CUDA
+kernels; there is no other implementation to fall back to, and loading fails
+loudly when the library has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
+FA_BF16, FA_F32 = 0, 1
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libosfa.so")
+
+# Every exported symbol of include/fa.h with its ctypes signature.
+_SIGNATURES = {
+    "fa_fwd": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 4
+               + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
+    "fa_fwd_dt": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 4
+                  + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "online_softmax_rows": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2
+                            + [ctypes.c_void_p]),
+    "fa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "fa_last_device_error": (ctypes.c_int, [ctypes.c_void_p]),
+    "fa_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_longlong, ctypes.c_void_p]),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call}: {status_str(status)} (status {status})")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libosfa.so (once).  Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it first (python -m online_softmax_07_gb300.build); "
+                "the attention and row-state operations exist only as CUDA kernels")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if not x.is_cuda:
+            raise ValueError("device pointer expected: pass a CUDA tensor")
+        if not x.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return x.data_ptr()
+    raise TypeError(f"cannot pass {type(x).__name__} as a pointer")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, call: str) -> None:
+    if status != FA_OK:
+        raise FAError(status, call)
+
+
+def status_str(status: int) -> str:
+    return load().fa_status_str(status).decode()
+
+
+fa_status_str = status_str
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream=None) -> None:
+    _check(load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                         float(scale), int(causal), _stream(stream)), "fa_fwd")
+
+
+def fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream=None) -> None:
+    _check(load().fa_fwd_dt(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                            float(scale), int(causal), int(dtype), _stream(stream)), "fa_fwd_dt")
+
+
+def online_softmax_rows(x, m_out, l_out, rows, length, stream=None) -> None:
+    _check(load().online_softmax_rows(_ptr(x), _ptr(m_out), _ptr(l_out), rows, length,
+                                      _stream(stream)), "online_softmax_rows")
+
+
+def fa_last_device_error(stream=None) -> int:
+    """Returns the status code (does not raise)."""
+    return load().fa_last_device_error(_stream(stream))
+
+
+def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(load().fa_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "fa_selftest_wait_timeout")

@@ -1,0 +1,208 @@
+// api.cu -- the C ABI declared in include/fa.h: argument checks, TMA descriptor set-up
+// and dispatch to the kernels.  No device memory is allocated here: the status word
+// the kernels report bounded-wait time-outs in is a static device variable.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_tc.cuh"
+#include "fa.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace osfa {
+namespace {
+
+__device__ unsigned g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned* g_status_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Address of this device's status word (looked up once per device).
+cudaError_t status_word(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorSymbolNotFound;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = g_encode;
+  return cudaSuccess;
+}
+
+// A [BH, N, d] bf16 tensor seen by TMA as 3-D (d innermost), boxes of 128 rows x 64
+// columns (128 bytes) with the 128-byte swizzle.  Rows past N read as zero and are
+// not written by stores.
+bool encode_bhnd(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base,
+                 int BH, int N, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxCols), static_cast<cuuint32_t>(kBlockM),
+                             1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+__global__ void wait_timeout_selftest_kernel(unsigned* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);  // expects one arrival that never comes
+    abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned long long limit_ns,
+                                         cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace osfa
+
+using namespace osfa;
+
+extern "C" {
+
+const char* fa_status_str(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension or dtype";
+    case FA_ERR_ALIGN: return "misaligned pointer";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+  }
+  return "unknown status";
+}
+
+fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                    cudaStream_t stream) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID;
+  if (dtype != FA_BF16 && dtype != FA_F32) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_F32 && (d < 1 || d > 128)) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > INT_MAX) return FA_ERR_INVALID;
+  if (BH == 0 || N == 0) return FA_OK;  // empty problem
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID;
+  if (lse != nullptr && !aligned(lse, 4)) return FA_ERR_ALIGN;
+
+  unsigned* status = nullptr;
+  if (dtype == FA_F32) {
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(o, 4)) return FA_ERR_ALIGN;
+    if ((static_cast<long long>(N) + 15) / 16 * BH > INT_MAX) return FA_ERR_INVALID;
+    return from_cuda(launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                     static_cast<const float*>(v), static_cast<float*>(o), lse,
+                                     static_cast<int>(BH), N, d, scale, causal, stream));
+  }
+
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return FA_ERR_ALIGN;
+  const long long nqb = (static_cast<long long>(N) + 2 * kBlockM - 1) / (2 * kBlockM);
+  if (nqb * BH > INT_MAX) return FA_ERR_INVALID;
+  cudaError_t e = status_word(&status);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if ((e = encode_fn(&enc)) != cudaSuccess) return FA_ERR_CUDA;
+  CUtensorMap tq, tk, tv, to;
+  const int bh = static_cast<int>(BH);
+  if (!encode_bhnd(enc, &tq, q, bh, N, d) || !encode_bhnd(enc, &tk, k, bh, N, d) ||
+      !encode_bhnd(enc, &tv, v, bh, N, d) || !encode_bhnd(enc, &to, o, bh, N, d))
+    return FA_ERR_CUDA;
+  AttnTcParams p;
+  p.lse = lse;
+  p.status = status;
+  p.N = N;
+  p.BH = bh;
+  p.nqb = static_cast<int>(nqb);
+  p.causal = causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  e = (d == 64) ? launch_attn_tc<64>(tq, tk, tv, to, p, stream)
+                : launch_attn_tc<128>(tq, tk, tv, to, p, stream);
+  return from_cuda(e);
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, cudaStream_t stream) {
+  return fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, FA_BF16, stream);
+}
+
+fa_status online_softmax_rows(const float* x, float* m_out, float* l_out, int rows, int len,
+                              cudaStream_t stream) {
+  if (rows < 0 || len < 0) return FA_ERR_INVALID;
+  if (rows == 0) return FA_OK;
+  if (len == 0) return FA_ERR_INVALID;
+  if (x == nullptr || m_out == nullptr || l_out == nullptr) return FA_ERR_INVALID;
+  if (!aligned(x, 4) || !aligned(m_out, 4) || !aligned(l_out, 4)) return FA_ERR_ALIGN;
+  return from_cuda(launch_row_state(x, m_out, l_out, rows, len, stream));
+}
+
+fa_status fa_last_device_error(cudaStream_t stream) {
+  unsigned* status = nullptr;
+  if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned value = 0;
+  if (cudaMemcpy(&value, status, sizeof(value), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (value != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  return (value & kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+fa_status fa_selftest_wait_timeout(long long limit_ns, cudaStream_t stream) {
+  if (limit_ns < 1 || limit_ns > 2000000000LL) return FA_ERR_INVALID;
+  unsigned* status = nullptr;
+  if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
+  return from_cuda(
+      launch_wait_timeout_selftest(status, static_cast<unsigned long long>(limit_ns), stream));
+}
+
+}  // extern "C"

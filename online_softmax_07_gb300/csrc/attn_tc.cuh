@@ -1,0 +1,75 @@
+// attn_tc.cuh -- bf16 attention forward on the 5th-generation tensor cores (sm_103a).
+//
+// Computes, for every (batch, head) and query row i,
+//   O_i = sum_j softmax_j(scale * q_i . k_j) v_j  and  LSE_i = ln sum_j exp(scale q_i.k_j)
+// with the online-softmax tile loop of "Softmax 数值稳定性与 IO-Aware Attention：从在线
+// 归一化到 FlashAttention", §七: per Q tile, m = -inf, l = 0, O = 0; for each K/V tile
+// S = Q K^T, m_new = max(m, rowmax S), P = exp(S - m_new), alpha = exp(m - m_new),
+// l = alpha l + rowsum P, O = alpha O + P V; finally O = O / l.  Alpha rescales both l
+// and O.  The §八 work split is kept: Q is the outer loop (each O row is written once),
+// and K/V tiles entirely above the causal diagonal are skipped, never loaded.
+//
+// GB300 mapping (not the pages' A100-era tiling):
+//  * one CTA per SM holds TWO 128-row Q tiles that share one stream of K/V tiles;
+//    the tensor pipe alternates between them, so the softmax of one tile overlaps
+//    the two MMAs of the other ("ping-pong");
+//  * S = Q K^T and O += P V are tcgen05.mma kind::f16 (bf16 in, fp32 accumulate), one
+//    thread issues them; S, P and O live in tensor memory (TMEM), never in HBM;
+//  * Q, K, V tiles arrive by TMA into 128-byte-swizzled shared memory through a ring of
+//    slots guarded by mbarriers; O leaves through shared memory and a TMA store;
+//  * each softmax thread owns one query row of its tile (TMEM lane = row), so row max
+//    and row sum need no shuffles;
+//  * the rescale reference m is moved only when a row's maximum grows by more than
+//    2^8 (kRescaleLog2); between moves alpha = 1 and the O rescale is skipped.  The
+//    identity behind the merge rule holds for any common reference, so O and LSE are
+//    the same in exact arithmetic; P then lies in [0, 2^8] instead of [0, 1], which
+//    bf16 and fp32 represent with the same relative precision.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx.cuh"
+
+namespace osfa {
+
+constexpr int kBlockM = 128;        // query rows per tile = TMEM lanes
+constexpr int kBlockN = 128;        // keys per K/V tile
+constexpr int kBoxCols = 64;        // bf16 per 128-byte swizzled row
+constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 128 bytes
+constexpr int kAttnThreads = 320;   // warps 0-3 softmax tile 0, 4-7 tile 1, 8 MMA, 9 TMA
+constexpr int kWarpMma = 8;
+constexpr int kWarpLoad = 9;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct AttnTcCfg {
+  static_assert(D == 64 || D == 128, "head dimension");
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D bf16
+  static constexpr int kSlots = (D == 128) ? 5 : 8;       // K/V ring depth
+  static constexpr int kSmemQ0 = 0;
+  static constexpr int kSmemQ1 = kTileBytes;
+  static constexpr int kSmemSlots = 2 * kTileBytes;
+  static constexpr int kSmemBars = kSmemSlots + kSlots * kTileBytes;
+  static constexpr int kSmemBytes = kSmemBars + 512 + 1024;  // + barriers + alignment slack
+  // TMEM columns: S/P of tile 0 and 1, then O of tile 0 and 1.
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+struct AttnTcParams {
+  float* lse;          // [BH, N] or nullptr
+  unsigned* status;    // device status word
+  int N;
+  int BH;
+  int nqb;             // number of 256-row query blocks per head
+  int causal;
+  float scale_log2;    // scale * log2(e)
+};
+
+template <int D>
+cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& to, const AttnTcParams& p, cudaStream_t stream);
+
+}  // namespace osfa

@@ -1,0 +1,351 @@
+// attn_tc_impl.cuh -- kernel body of the tcgen05 attention forward (see attn_tc.cuh).
+// Included by one translation unit per head dimension.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "attn_tc.cuh"
+
+namespace osfa {
+
+struct AttnTcBarriers {
+  uint64_t q_full;
+  uint64_t s_full[2];    // MMA -> softmax t: S_t of the current K/V tile is in TMEM
+  uint64_t p_ready[2];   // softmax t -> MMA: P_t stored in TMEM and O_t rescaled
+  uint64_t o_final[2];   // MMA -> softmax t: last P_t V product done
+  uint64_t mma_drain;    // MMA thread: all of its MMAs finished (before TMEM is freed)
+  uint64_t slot_full[8];
+  uint64_t slot_empty[8];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand (tcgen05 "matrix
+// descriptor"): start address, leading and stride byte offsets (all >> 4), the
+// descriptor version 1 at bit 46 and the swizzle mode (2 = 128 B) at bits 61-63.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
+// B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_o, const AttnTcParams p) {
+  using Cfg = AttnTcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  AttnTcBarriers* bars = reinterpret_cast<AttnTcBarriers*>(smem + Cfg::kSmemBars);
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work item: heavy (late) query blocks first so that causal tails overlap.
+  const int L = blockIdx.x;
+  const int qb = p.nqb - 1 - L / p.BH;
+  const int bh = L % p.BH;
+  const int nblk = (p.N + kBlockN - 1) / kBlockN;
+  // K/V tiles each Q tile needs: all of them, or up to its diagonal tile (causal).
+  const int nb0 = p.causal ? min(nblk, (qb * 2 * kBlockM + kBlockM - 1) / kBlockN + 1) : nblk;
+  const int nb1 = p.causal ? min(nblk, (qb * 2 * kBlockM + 2 * kBlockM - 1) / kBlockN + 1) : nblk;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->q_full), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bars->s_full[t]), 1);
+      mbar_init(smem_u32(&bars->p_ready[t]), 128);
+      mbar_init(smem_u32(&bars->o_final[t]), 1);
+    }
+    mbar_init(smem_u32(&bars->mma_drain), 1);
+    for (int s = 0; s < Cfg::kSlots; ++s) {
+      mbar_init(smem_u32(&bars->slot_full[s]), 1);
+      mbar_init(smem_u32(&bars->slot_empty[s]), 1);
+    }
+    bars->abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(&bars->tmem_base), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+
+  if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_o);
+      const uint32_t qbar = smem_u32(&bars->q_full);
+      mbar_arrive_expect_tx(qbar, 2 * Cfg::kTileBytes);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int b = 0; b < Cfg::kBoxes; ++b)
+          tma_load_3d(sbase + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0) + b * kBoxBytes, &tm_q, qbar,
+                      b * kBoxCols, qb * 2 * kBlockM + t * kBlockM, bh);
+      int issued = 0;
+      const int nload = 2 * nb1;  // K_j, V_j for j < nb1 (tile 1 needs the most)
+      for (int it = 0; it < nload; ++it) {
+        const int slot = it % Cfg::kSlots;
+        const int phase = (it / Cfg::kSlots) & 1;
+        if (!mbar_wait(smem_u32(&bars->slot_empty[slot]), phase ^ 1, abort, p.status)) break;
+        const uint32_t full = smem_u32(&bars->slot_full[slot]);
+        mbar_arrive_expect_tx(full, Cfg::kTileBytes);
+        const CUtensorMap* tm = (it & 1) ? &tm_v : &tm_k;
+        const uint32_t dst = sbase + Cfg::kSmemSlots + slot * Cfg::kTileBytes;
+#pragma unroll
+        for (int b = 0; b < Cfg::kBoxes; ++b)
+          tma_load_3d(dst + b * kBoxBytes, tm, full, b * kBoxCols, (it >> 1) * kBlockN, bh);
+        issued = it + 1;
+      }
+      // Every issued copy must land before the block's shared memory goes away: wait
+      // for the last load issued into each slot.
+      int no_abort = 0;
+      mbar_wait(qbar, 0, &no_abort, p.status);
+      for (int it = max(0, issued - Cfg::kSlots); it < issued; ++it)
+        mbar_wait(smem_u32(&bars->slot_full[it % Cfg::kSlots]), (it / Cfg::kSlots) & 1, &no_abort,
+                  p.status);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, true);
+      auto tS = [&](int t) { return tbase + (t ? Cfg::kColS1 : Cfg::kColS0); };
+      auto tO = [&](int t) { return tbase + (t ? Cfg::kColO1 : Cfg::kColO0); };
+      auto sQ = [&](int t) { return sbase + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0); };
+      auto slot_addr = [&](int it) {
+        return sbase + Cfg::kSmemSlots + (it % Cfg::kSlots) * Cfg::kTileBytes;
+      };
+      auto wait_full = [&](int it) {
+        return mbar_wait(smem_u32(&bars->slot_full[it % Cfg::kSlots]), (it / Cfg::kSlots) & 1,
+                         abort, p.status);
+      };
+      // S_t = Q_t K^T: K-major A and B, 16 columns (32 bytes) of d per instruction.
+      auto issue_s = [&](int t, uint32_t k_addr) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_bf16_ss(tS(t), desc_sw128(sQ(t) + off, 16, 1024), desc_sw128(k_addr + off, 16, 1024),
+                      kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V: P from TMEM (bf16 packed two per column), V MN-major in shared
+      // memory; 16 keys (2 KB of the V tile) per instruction.
+      auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_bf16_ts(tO(t), tS(t) + kk * 8, desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024),
+                      kIdescPV, (acc || kk > 0) ? 1u : 0u);
+      };
+
+      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort, p.status) && wait_full(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, slot_addr(0));
+        mma_commit(smem_u32(&bars->s_full[0]));
+        issue_s(1, slot_addr(0));
+        mma_commit(smem_u32(&bars->s_full[1]));
+        mma_commit(smem_u32(&bars->slot_empty[0]));
+      }
+      for (int j = 0; ok && j < nb1; ++j) {
+        const int itV = 2 * j + 1, itK = 2 * j + 2;
+        if (!(ok = wait_full(itV))) break;
+        if (j < nb0) {
+          if (!(ok = mbar_wait(smem_u32(&bars->p_ready[0]), j & 1, abort, p.status))) break;
+          tc_fence_after();
+          issue_pv(0, slot_addr(itV), j > 0);
+          if (j + 1 < nb0) {
+            if (!(ok = wait_full(itK))) break;
+            tc_fence_after();
+            issue_s(0, slot_addr(itK));
+            mma_commit(smem_u32(&bars->s_full[0]));
+          } else {
+            mma_commit(smem_u32(&bars->o_final[0]));
+          }
+        }
+        if (!(ok = mbar_wait(smem_u32(&bars->p_ready[1]), j & 1, abort, p.status))) break;
+        tc_fence_after();
+        issue_pv(1, slot_addr(itV), j > 0);
+        mma_commit(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
+        if (j + 1 < nb1) {
+          if (!(ok = wait_full(itK))) break;
+          tc_fence_after();
+          issue_s(1, slot_addr(itK));
+          mma_commit(smem_u32(&bars->s_full[1]));
+          mma_commit(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
+        } else {
+          mma_commit(smem_u32(&bars->o_final[1]));
+        }
+      }
+      // Drain: nothing may still read shared memory or TMEM when the block exits.
+      mma_commit(smem_u32(&bars->mma_drain));
+      int no_abort = 0;
+      mbar_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax tile t
+    const int t = warp >> 2;       // warps 0-3 -> tile 0, 4-7 -> tile 1
+    const int wq = warp & 3;       // TMEM lane quarter this warp may access
+    const int rr = wq * 32 + lane; // row within the tile
+    const int r0 = qb * 2 * kBlockM + t * kBlockM;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off + (t ? Cfg::kColS1 : Cfg::kColS0);
+    const uint32_t tO = tbase + lane_off + (t ? Cfg::kColO1 : Cfg::kColO0);
+    const float sl2 = p.scale_log2;
+    float m2 = -INFINITY;  // rescale reference, log2 units of the scaled score
+    float l = 0.f;
+    bool ok = true;
+
+    const int nbt = t ? nb1 : nb0;
+    for (int j = 0; j < nbt; ++j) {
+      ok = mbar_wait(smem_u32(&bars->s_full[t]), j & 1, abort, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld128_wait(tS, sr);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+
+      // Mask: keys >= N (ragged last tile) and, on the diagonal tile, keys > row.
+      const int key0 = j * kBlockN;
+      const bool diag = p.causal && (key0 + kBlockN - 1 > r0);
+      if (diag || key0 + kBlockN > p.N) {
+        int lim = p.N - 1 - key0;
+        if (p.causal) lim = min(lim, r0 + rr - key0);
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+      }
+
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float rowmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m2_new = fmaxf(m2, rowmax * sl2);
+      const float m2_use = (m2_new > m2 + kRescaleLog2) ? m2_new : m2;
+      const float alpha = ex2_approx(m2 - m2_use);  // 1 if unchanged, 0 on the first tile
+
+      // Rescale O_t by alpha.  S_t(j) complete implies P_t(j-1) V done (one issuing
+      // thread, completion tracked in order), so O_t is stable here.
+      if (j > 0 && __any_sync(0xffffffffu, m2_use != m2)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32_wait(tO + 32 * c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + 32 * c, o);
+        }
+      }
+      m2 = m2_use;
+
+      // P = exp2(s * scale * log2 e - m2), row sum in fp32, P packed to bf16 pairs
+      // and stored over the first 64 columns of S_t.
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(fmaf(s[64 * h + 2 * i], sl2, -m2));
+          const float p1 = ex2_approx(fmaf(s[64 * h + 2 * i + 1], sl2, -m2));
+          sum[i & 3] += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + 32 * h, pk);
+      }
+      l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->p_ready[t]));
+    }
+
+    if (ok) {
+      ok = mbar_wait(smem_u32(&bars->o_final[t]), 0, abort, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    // Epilogue: O / l -> bf16 -> swizzled staging in the (now unused) Q_t buffer ->
+    // TMA store; LSE = m + ln l in natural-log units of the scaled score.
+    uint8_t* stage = smem + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0);
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(tO + 32 * c, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        // columns 32c .. 32c+31 = box (32c / 64), 16-byte chunks (32c % 64) / 8 .. +3
+        uint8_t* rowp = stage + (c >> 1) * kBoxBytes + rr * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = ((c & 1) * 4 + q) ^ (rr & 7);
+          *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      if (p.lse != nullptr && r0 + rr < p.N)
+        p.lse[static_cast<int64_t>(bh) * p.N + r0 + rr] = m2 * 0.69314718055994531f + logf(l);
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(1 + t, 128);
+    if (rr == 0 && ok && !*abort && r0 < p.N) {
+#pragma unroll
+      for (int b = 0; b < Cfg::kBoxes; ++b)
+        tma_store_3d(&tm_o, smem_u32(stage + b * kBoxBytes), b * kBoxCols, r0, bh);
+      bulk_commit_group();
+      bulk_wait_group_0();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tbase, Cfg::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& to, const AttnTcParams& p, cudaStream_t stream) {
+  using Cfg = AttnTcCfg<D>;
+  static_assert(sizeof(AttnTcBarriers) <= 512, "barrier block");
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(p.nqb) * p.BH;
+  attn_fwd_tc_kernel<D><<<static_cast<unsigned>(grid), kAttnThreads, Cfg::kSmemBytes, stream>>>(
+      tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
+}  // namespace osfa

@@ -1,0 +1,111 @@
+"""The C-ABI library on the host (no GPU): it builds, loads, exports every symbol
+include/fa.h declares, and rejects bad arguments before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from online_softmax_07_gb300 import abi
+from online_softmax_07_gb300.build import build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return abi.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert set(names) == set(abi._SIGNATURES), names
+    for name in names:
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert abi.status_str(code)
+    assert abi.status_str(99) == "unknown status"
+
+
+FAKE = 0x10000  # an aligned address that is never dereferenced (checks fail first)
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(d=96), abi.FA_ERR_UNSUPPORTED),
+    (dict(d=32), abi.FA_ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), abi.FA_ERR_INVALID),
+    (dict(scale=float("inf")), abi.FA_ERR_INVALID),
+    (dict(scale=0.0), abi.FA_ERR_INVALID),
+    (dict(scale=-0.125), abi.FA_ERR_INVALID),
+    (dict(causal=2), abi.FA_ERR_INVALID),
+    (dict(N=-1), abi.FA_ERR_INVALID),
+    (dict(B=-2), abi.FA_ERR_INVALID),
+    (dict(q=None), abi.FA_ERR_INVALID),
+    (dict(o=None), abi.FA_ERR_INVALID),
+    (dict(q=FAKE + 8), abi.FA_ERR_ALIGN),
+    (dict(v=FAKE + 2), abi.FA_ERR_ALIGN),
+    (dict(lse=FAKE + 2), abi.FA_ERR_ALIGN),
+    (dict(B=0), abi.FA_OK),          # empty problems launch nothing
+    (dict(H=0), abi.FA_OK),
+    (dict(N=0), abi.FA_OK),
+    (dict(B=65536, H=65536), abi.FA_ERR_INVALID),
+])
+def test_fa_fwd_argument_checks(lib, args, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64, scale=0.125,
+             causal=0)
+    a.update(args)
+    st = lib.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                    a["scale"], a["causal"], None)
+    assert st == expect, abi.status_str(st)
+
+
+@pytest.mark.parametrize("d,align,dtype,expect", [
+    (200, 4, abi.FA_F32, abi.FA_ERR_UNSUPPORTED),
+    (0, 4, abi.FA_F32, abi.FA_ERR_UNSUPPORTED),
+    (17, 2, abi.FA_F32, abi.FA_ERR_ALIGN),
+    (64, 16, 7, abi.FA_ERR_UNSUPPORTED),
+])
+def test_fa_fwd_dt_argument_checks(lib, d, align, dtype, expect):
+    p = FAKE + (align if align < 4 else 0)
+    st = lib.fa_fwd_dt(p, p, p, p, None, 1, 1, 16, d, 0.5, 0, dtype, None)
+    assert st == expect
+
+
+@pytest.mark.parametrize("x,m,l,rows,length,expect", [
+    (FAKE, FAKE, FAKE, 0, 0, abi.FA_OK),          # nothing to do
+    (None, None, None, 0, 5, abi.FA_OK),
+    (FAKE, FAKE, FAKE, 3, 0, abi.FA_ERR_INVALID),  # the max of an empty row is undefined
+    (FAKE, FAKE, FAKE, -1, 5, abi.FA_ERR_INVALID),
+    (None, FAKE, FAKE, 3, 5, abi.FA_ERR_INVALID),
+    (FAKE, None, FAKE, 3, 5, abi.FA_ERR_INVALID),
+    (FAKE + 1, FAKE, FAKE, 3, 5, abi.FA_ERR_ALIGN),
+    (FAKE, FAKE, FAKE + 2, 3, 5, abi.FA_ERR_ALIGN),
+])
+def test_row_state_argument_checks(lib, x, m, l, rows, length, expect):
+    assert lib.online_softmax_rows(x, m, l, rows, length, None) == expect
+
+
+def test_selftest_limit_checked(lib):
+    assert lib.fa_selftest_wait_timeout(0, None) == abi.FA_ERR_INVALID
+    assert lib.fa_selftest_wait_timeout(3_000_000_000, None) == abi.FA_ERR_INVALID
+
+
+def test_binding_has_no_fallback(tmp_path):
+    saved = abi._lib
+    try:
+        abi._lib = None
+        with pytest.raises(RuntimeError, match="missing"):
+            abi.load(str(tmp_path / "libosfa.so"))
+    finally:
+        abi._lib = saved
