@@ -1,0 +1,507 @@
+"""Benchmark of the online-softmax hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. attention forward, bf16, B=2 H=16 N=8192 d=128, causal, scale 1/sqrt(128)
+     (fa_fwd, the tcgen05 kernel), and
+  2. the row online-softmax state of a 4096 x 32768 fp32 array N(0, 9) with the
+     special rows (online_softmax_rows).
+Inputs are resident in HBM before the timed region; every step re-reads inputs far
+larger than the 129 MB L2 (Q, K, V: 201 MB; x: 537 MB), so no L2 flush is needed.
+
+Printed JSON (one line, rank 0):
+  value      attention TFLOP/s = 4*B*H*N^2*d/2 / mean attention kernel time (CUDA events
+             on the launching stream, max over ranks);
+  row_softmax  the row kernel's GB/s = (rows*len*4 + rows*8) / mean kernel time;
+  e2e        the same attention metric through the public Python API with pinned host
+             buffers: host->device copy of Q, K, V, the kernel and device->host read of
+             O and LSE inside the timed region;
+  roofline   the attention kernel against the measured dense bf16 peak; the row kernel
+             (inside row_softmax) against the measured HBM copy bandwidth;
+  cpu_baseline  the fp64 oracle timed on a bounded sample of the same workload on the
+             host cores (rank 0, one GPU only).
+``--impl reference`` times the oracle alone (see ``reference_arm``).
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+ATTN = dict(name="attn_bf16_b2h16n8192d128_causal", B=2, H=16, N=8192, d=128, causal=True)
+ROWS = dict(name="rows_4096x32768", rows=4096, length=32768)
+METRIC = "attn fwd TFLOP/s and % of GB300 bf16 dense peak (1 GPU); row-softmax HBM GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def attn_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def row_bytes(rows, length):
+    return rows * length * 4.0 + rows * 8.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", 0) or 0),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "online_softmax_07_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(kernel)
+    if not ent or ent.get("sources") != kernel_sources_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.index = index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period_ms}", f"--id={self.index}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle sample (CPU)
+_SHARED = {}
+
+
+def _attach(spec):
+    """Pool initialiser: map the parent's input arrays (shared memory, read only)."""
+    from multiprocessing import shared_memory
+    for key, (name, shape, dtype) in spec.items():
+        shm = shared_memory.SharedMemory(name=name)
+        _SHARED[key] = (shm, np.ndarray(shape, dtype=dtype, buffer=shm.buf))
+    import oracle  # noqa: F401  (import cost outside the timing)
+
+
+def _arr(key):
+    return _SHARED[key][1]
+
+
+def _oracle_attention_task(args):
+    """Query rows `rows` of head (b, h) through the fp64 oracle; returns the
+    algorithmic FLOPs of those rows (4 d per visible key) and the seconds taken."""
+    import oracle
+    b, h, rows, scale, causal = args
+    q, k, v = _arr("q")[b, h], _arr("k")[b, h], _arr("v")[b, h]
+    t0 = time.perf_counter()
+    oracle.attention_forward(q[None, None], k[None, None], v[None, None], scale, causal,
+                             rows=rows)
+    dt = time.perf_counter() - t0
+    n, d = q.shape
+    keys = (rows + 1) if causal else np.full(rows.shape, n)
+    return 4.0 * d * float(np.sum(keys)), dt
+
+
+def _oracle_rows_task(args):
+    import oracle
+    r0, r1 = args
+    x = _arr("x")[r0:r1]
+    t0 = time.perf_counter()
+    oracle.row_state(x)
+    return row_bytes(*x.shape), time.perf_counter() - t0
+
+
+def _noop(_):
+    return 0
+
+
+class OraclePool:
+    """A spawn pool over the host cores.  Each worker uses one BLAS thread (so that
+    `cores` is the number of workers) and maps the inputs from shared memory."""
+
+    def __init__(self, arrays: dict, workers: int):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        self.workers = workers
+        self.shms = []
+        spec = {}
+        for key, a in arrays.items():
+            a = np.ascontiguousarray(a)
+            shm = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
+            np.ndarray(a.shape, dtype=a.dtype, buffer=shm.buf)[...] = a
+            self.shms.append(shm)
+            spec[key] = (shm.name, a.shape, a.dtype.str)
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                                "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(workers, initializer=_attach,
+                                                     initargs=(spec,))
+        finally:
+            for k, val in saved.items():
+                if val is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = val
+        self.pool.map(_noop, range(workers))   # start-up outside any timing
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+        for shm in self.shms:
+            shm.close()
+            shm.unlink()
+
+
+def attention_sample_tasks(shape, rows_per_task, n_tasks, seed):
+    """Tasks of a bounded oracle sample: heads (b, h) in turn, each task with
+    `rows_per_task` query rows drawn uniformly (seeded) over the whole sequence."""
+    B, H, N, d = shape
+    g = np.random.Generator(np.random.PCG64(seed))
+    tasks = []
+    for i in range(n_tasks):
+        b, h = (i // H) % B, i % H
+        rows = np.sort(g.choice(N, size=rows_per_task, replace=False))
+        tasks.append((b, h, rows, 1.0 / math.sqrt(d), ATTN["causal"]))
+    return tasks
+
+
+def cpu_baseline(q, k, v, x, budget_s=15.0):
+    """The oracle as it stands on a bounded sample of the same workload: batches of
+    tasks (64 attention query rows of one head each, rows drawn uniformly) for about
+    2/3 of the budget, then batches of row states (4 whole rows per task) of the row
+    workload for the rest."""
+    workers = os.cpu_count() or 1
+    op = OraclePool({"q": q, "k": k, "v": v, "x": x}, workers)
+    try:
+        flops, done, s, t0 = 0.0, 0, 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s * 2 / 3:
+            tasks = attention_sample_tasks(q.shape, 64, 2 * workers, seed=4242 + s)
+            flops += sum(f for f, _ in op.pool.map(_oracle_attention_task, tasks))
+            done += len(tasks)
+            s += 1
+        att_s = time.perf_counter() - t0
+        nrows = x.shape[0]
+        nbytes, rdone, i, t0 = 0.0, 0, 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s / 3:
+            chunks = [((4 * (i + w)) % nrows, (4 * (i + w)) % nrows + 4) for w in range(workers)]
+            nbytes += sum(b for b, _ in op.pool.map(_oracle_rows_task, chunks))
+            rdone += 4 * workers
+            i += workers
+        row_s = time.perf_counter() - t0
+    finally:
+        op.close()
+    return {
+        "value": flops / att_s / 1e12, "unit": "TFLOP/s", "cores": workers, "kind": "oracle",
+        "sample": (f"{done} tasks x 64 query rows of {ATTN['name']} (rows uniform over the "
+                   f"sequence, heads in turn), fp64, {workers} spawn workers x 1 BLAS thread, "
+                   f"{att_s:.1f} s wall"),
+        "row_softmax": {"value": nbytes / row_s / 1e9, "unit": "GB/s",
+                        "sample": f"{rdone} rows of {ROWS['name']}, {row_s:.1f} s wall"},
+    }
+
+
+# ------------------------------------------------------------------ reference arm
+def reference_arm(args, rank, world):
+    """The oracle, as it stands, on the host cores: each step is a bounded sample of
+    the workload (one task of 32 attention query rows per worker, plus 2 rows of the
+    row-state array per worker), timed with the wall clock."""
+    if rank != 0:
+        return None
+    from online_softmax_07_gb300 import synth
+    q, k, v = synth.workload_attention_inputs(ATTN["name"])
+    x = synth.row_inputs(64, ROWS["length"], seed=2000)
+    workers = os.cpu_count() or 1
+    op = OraclePool({"q": q, "k": k, "v": v, "x": x}, workers)
+    try:
+        flops = secs = 0.0
+        for s in range(args.warmup + args.steps):
+            tasks = attention_sample_tasks(q.shape, 32, workers, seed=900 + s)
+            t0 = time.perf_counter()
+            res = op.pool.map(_oracle_attention_task, tasks)
+            op.pool.map(_oracle_rows_task, [((2 * i) % 64, (2 * i) % 64 + 2)
+                                            for i in range(workers)])
+            dt = time.perf_counter() - t0
+            if s >= args.warmup:
+                flops += sum(r[0] for r in res)
+                secs += dt
+    finally:
+        op.close()
+    value = flops / secs / 1e12
+    sample = (f"per step {workers} tasks x 32 query rows of {ATTN['name']} plus "
+              f"{2 * workers} rows of {ROWS['name']}; fp64 oracle, {workers} spawn workers "
+              f"x 1 BLAS thread")
+    return {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": ATTN["name"] + " + " + ROWS["name"], "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": workers, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ our arm
+def our_arm(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from online_softmax_07_gb300 import abi, attention_forward, synth
+    from online_softmax_07_gb300.build import build_library
+
+    build_library()
+    abi.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    B, H, N, d, causal = ATTN["B"], ATTN["H"], ATTN["N"], ATTN["d"], ATTN["causal"]
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = synth.workload_attention_inputs(ATTN["name"])
+    x = synth.workload_row_inputs()[0]
+    dq, dk, dv = (torch.from_numpy(t).to(dev, torch.bfloat16) for t in (q, k, v))
+    do = torch.empty_like(dq)
+    dlse = torch.empty((B, H, N), device=dev)
+    dx = torch.from_numpy(x).to(dev)
+    rows, length = x.shape
+    dm = torch.empty(rows, device=dev)
+    dl = torch.empty(rows, device=dev)
+
+    for _ in range(args.warmup):
+        abi.fa_fwd(dq, dk, dv, do, dlse, B, H, N, d, scale, int(causal), stream)
+        abi.online_softmax_rows(dx, dm, dl, rows, length, stream)
+    torch.cuda.synchronize()
+    if abi.fa_last_device_error() != abi.FA_OK:
+        raise RuntimeError("device-side error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)   # let the sampler come up before the timed region
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        abi.fa_fwd(dq, dk, dv, do, dlse, B, H, N, d, scale, int(causal), stream)
+        ev[i][1].record(stream)
+        abi.online_softmax_rows(dx, dm, dl, rows, length, stream)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    if abi.fa_last_device_error() != abi.FA_OK:
+        raise RuntimeError("device-side error in the timed region")
+
+    attn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    rows_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    step_ms = t_start.elapsed_time(t_end) / args.steps
+    if world > 1:
+        t = torch.tensor([attn_ms, rows_ms, step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        attn_ms, rows_ms, step_ms = (float(z) for z in t.tolist())
+
+    flops = attn_flops(B, H, N, d, causal)
+    rbytes = row_bytes(rows, length)
+    value = flops * world / (attn_ms * 1e-3) / 1e12
+    row_gbs = rbytes * world / (rows_ms * 1e-3) / 1e9
+    peaks = load_peaks()
+    per_gpu_tflops = flops / (attn_ms * 1e-3) / 1e12
+    per_gpu_gbs = rbytes / (rows_ms * 1e-3) / 1e9
+
+    # End to end through the public API with pinned host buffers.
+    qh, kh, vh = (torch.from_numpy(t).to(torch.bfloat16).pin_memory() for t in (q, k, v))
+    oh = torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=True)
+    lh = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 30))
+    for _ in range(3):
+        attention_forward(qh, kh, vh, scale, causal, out=oh, lse_out=lh)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        attention_forward(qh, kh, vh, scale, causal, out=oh, lse_out=lh)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = 3 * qh.numel() * 2
+    d2h = oh.numel() * 2 + lh.numel() * 4
+
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{ATTN['name']} + {ROWS['name']}",
+            "attention": {"B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": scale,
+                          "inputs": "Q, K, V i.i.d. N(0,1) rounded to bf16"},
+            "rows": {"rows": rows, "len": length,
+                     "inputs": "N(0,9) fp32 with all-equal, +1000 and -1e4 special rows"},
+            "l2": "inputs larger than L2 (201 MB attention, 537 MB rows); no flush",
+            "parallelism": f"replicas x{world} (each GPU runs the full workload)",
+        },
+        "pct_of_peak": per_gpu_tflops / peaks["bf16_tflops"] * 100.0,
+        "ms_attention": attn_ms,
+        "ms_rows": rows_ms,
+        "row_softmax": {
+            "value": row_gbs, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": per_gpu_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": per_gpu_gbs / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("row_state_block_kernel"),
+                         "peak_source": peaks["source"]},
+        },
+        "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": per_gpu_tflops / peaks["bf16_tflops"],
+                     "traffic": recorded_traffic("attn_fwd_tc_kernel"),
+                     "peak_source": peaks["source"] + " bf16 burst"},
+        "clocks": clocks,
+        "e2e": {"value": flops * world / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "online_softmax_07_gb300.attention_forward(pinned host tensors)"},
+        "gpu_launches": 2 * args.steps,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(q, k, v, x, budget_s=args.cpu_seconds)
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    if args.impl == "reference":
+        out = reference_arm(args, rank, world)
+    else:
+        out = our_arm(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -18,18 +18,22 @@ __all__ = ["attention_forward", "row_state", "abi", "FAError", "fa_fwd", "fa_fwd
            "online_softmax_rows", "fa_last_device_error"]
 
 
-def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=True):
+def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=True,
+                      out=None, lse_out=None):
     """O = softmax(scale * Q K^T) V and LSE for [B, H, N, d] tensors (bf16 or fp32).
 
-    Returns (O, LSE) with O of q's dtype and LSE fp32 [B, H, N], on q's device.  For
-    CPU inputs the copies to and from the current CUDA device are part of the call
-    (pinned staging).  Everything is ordered on ``stream`` (a torch.cuda.Stream;
-    default: torch's current stream)."""
+    Returns (O, LSE) with O of q's dtype and LSE fp32 [B, H, N] (None without
+    ``with_lse``), on q's device.  For CPU inputs the copies to and from the current
+    CUDA device are part of the call: pinned inputs are copied asynchronously (others
+    are pinned first), and the results land in ``out`` / ``lse_out`` when given
+    (pinned host tensors of the right shape), else in new pinned tensors.  Everything
+    is ordered on ``stream`` (a torch.cuda.Stream; default: torch's current stream).
+    """
     import torch
 
     if stream is not None:
         with torch.cuda.stream(stream):
-            return attention_forward(q, k, v, scale, causal, None, with_lse)
+            return attention_forward(q, k, v, scale, causal, None, with_lse, out, lse_out)
     if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must be [B, H, N, d] of one shape")
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
@@ -40,23 +44,31 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
     host = not q.is_cuda
     if host:
         dev = torch.device("cuda", torch.cuda.current_device())
-        q, k, v = (t.contiguous().pin_memory().to(dev, non_blocking=True) for t in (q, k, v))
+
+        def up(t):
+            t = t.contiguous()
+            if not t.is_pinned():
+                t = t.pin_memory()
+            return t.to(dev, non_blocking=True)
+
+        q, k, v = up(q), up(k), up(v)
     else:
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if with_lse else None
     dtype = abi.FA_BF16 if q.dtype == torch.bfloat16 else abi.FA_F32
     fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), dtype)
-    if host:
-        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        o_h.copy_(o, non_blocking=True)
-        lse_h = None
-        if lse is not None:
-            lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-            lse_h.copy_(lse, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return o_h, lse_h
-    return o, lse
+    if not host:
+        return o, lse
+    o_h = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    o_h.copy_(o, non_blocking=True)
+    lse_h = None
+    if lse is not None:
+        lse_h = lse_out if lse_out is not None else torch.empty(lse.shape, dtype=torch.float32,
+                                                                pin_memory=True)
+        lse_h.copy_(lse, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return o_h, lse_h
 
 
 def row_state(x, stream=None):
@@ -70,8 +82,10 @@ def row_state(x, stream=None):
         raise ValueError("x must be an fp32 [rows, len] tensor")
     host = not x.is_cuda
     if host:
-        x = x.contiguous().pin_memory().to(torch.device("cuda", torch.cuda.current_device()),
-                                           non_blocking=True)
+        x = x.contiguous()
+        if not x.is_pinned():
+            x = x.pin_memory()
+        x = x.to(torch.device("cuda", torch.cuda.current_device()), non_blocking=True)
     else:
         x = x.contiguous()
     rows, length = x.shape
