@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -160,6 +161,10 @@ fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float*
   p.N = N;
   p.BH = bh;
   p.nqb = static_cast<int>(nqb);
+  // Heads scheduled together: as many as keep their K and V within about 64 MB of L2.
+  const long long kv_head_bytes = 2LL * N * d * 2;
+  p.head_group = static_cast<int>(
+      std::max(1LL, std::min(BH, (64LL << 20) / std::max(1LL, kv_head_bytes))));
   p.causal = causal;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   e = (d == 64) ? launch_attn_tc<64>(tq, tk, tv, to, p, stream)

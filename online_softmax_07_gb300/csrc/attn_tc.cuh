@@ -37,7 +37,12 @@ constexpr int kBlockM = 128;        // query rows per tile = TMEM lanes
 constexpr int kBlockN = 128;        // keys per K/V tile
 constexpr int kBoxCols = 64;        // bf16 per 128-byte swizzled row
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 128 bytes
-constexpr int kAttnThreads = 320;   // warps 0-3 softmax tile 0, 4-7 tile 1, 8 MMA, 9 TMA
+// Warps 0-3: softmax of tile 0; 4-7: softmax of tile 1; 8: MMA issue; 9: TMA loads;
+// 10-11 idle (they complete the third warpgroup so that it can hand its registers to
+// the softmax warpgroups).
+constexpr int kAttnThreads = 384;
+constexpr int kRegsSoftmax = 216;  // per thread, softmax warpgroups
+constexpr int kRegsIssue = 72;     // per thread, MMA / TMA warpgroup (384 x 168 = 256 x 216 + 128 x 72)
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr float kRescaleLog2 = 8.0f;
@@ -64,6 +69,7 @@ struct AttnTcParams {
   int N;
   int BH;
   int nqb;             // number of 256-row query blocks per head
+  int head_group;      // heads scheduled together (1 <= head_group <= BH)
   int causal;
   float scale_log2;    // scale * log2(e)
 };

@@ -52,10 +52,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: heavy (late) query blocks first so that causal tails overlap.
-  const int L = blockIdx.x;
-  const int qb = p.nqb - 1 - L / p.BH;
-  const int bh = L % p.BH;
+  // Work item.  Heads are taken in groups of p.head_group (sized on the host so that
+  // the group's K and V fit in L2); inside a group, the heavy (late) query blocks of
+  // all its heads come first, so that causal tails overlap lighter work.
+  int bh, qb;
+  {
+    const int L = blockIdx.x;
+    const int per_group = p.head_group * p.nqb;
+    const int full = p.BH / p.head_group;
+    const int g = L / per_group;
+    if (g < full) {
+      const int r = L - g * per_group;
+      qb = p.nqb - 1 - r / p.head_group;
+      bh = g * p.head_group + r % p.head_group;
+    } else {
+      const int rem = p.BH - full * p.head_group;
+      const int r = L - full * per_group;
+      qb = p.nqb - 1 - r / rem;
+      bh = full * p.head_group + r % rem;
+    }
+  }
   const int nblk = (p.N + kBlockN - 1) / kBlockN;
   // K/V tiles each Q tile needs: all of them, or up to its diagonal tile (causal).
   const int nb0 = p.causal ? min(nblk, (qb * 2 * kBlockM + kBlockM - 1) / kBlockN + 1) : nblk;
@@ -65,7 +81,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(smem_u32(&bars->q_full), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bars->s_full[t]), 1);
-      mbar_init(smem_u32(&bars->p_ready[t]), 128);
+      mbar_init(smem_u32(&bars->p_ready[t]), 4);  // one arrival per softmax warp
       mbar_init(smem_u32(&bars->o_final[t]), 1);
     }
     mbar_init(smem_u32(&bars->mma_drain), 1);
@@ -86,7 +102,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tbase = bars->tmem_base;
   volatile int* abort = &bars->abort;
 
-  if (warp == kWarpLoad) {
+  if (warp >= 8) {
+    // One setmaxnreg for the whole issue warpgroup (warps 8-11).
+    regs_decrease<kRegsIssue>();
+  }
+  if (warp >= 10) {
+    // idle warps of the issue warpgroup
+  } else if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -126,84 +148,97 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, true);
-      auto tS = [&](int t) { return tbase + (t ? Cfg::kColS1 : Cfg::kColS0); };
-      auto tO = [&](int t) { return tbase + (t ? Cfg::kColO1 : Cfg::kColO0); };
-      auto sQ = [&](int t) { return sbase + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0); };
-      auto slot_addr = [&](int it) {
-        return sbase + Cfg::kSmemSlots + (it % Cfg::kSlots) * Cfg::kTileBytes;
-      };
-      auto wait_full = [&](int it) {
-        return mbar_wait(smem_u32(&bars->slot_full[it % Cfg::kSlots]), (it / Cfg::kSlots) & 1,
-                         abort, p.status);
-      };
-      // S_t = Q_t K^T: K-major A and B, 16 columns (32 bytes) of d per instruction.
-      auto issue_s = [&](int t, uint32_t k_addr) {
+    // The whole warp runs this loop with warp-uniform values; elect.sync inside the
+    // MMA and commit wrappers lets one lane issue each instruction.
+    constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false);
+    constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, true);
+    // Descriptors of the tile bases; an operand at byte offset `off` inside a tile is
+    // base + (off >> 4) (the start-address field never overflows: shared memory is
+    // below 256 KB).
+    const uint64_t dQ0 = desc_sw128(sbase + Cfg::kSmemQ0, 16, 1024);
+    const uint64_t dQ1 = desc_sw128(sbase + Cfg::kSmemQ1, 16, 1024);
+    const uint64_t dSlot0K = desc_sw128(sbase + Cfg::kSmemSlots, 16, 1024);
+    const uint64_t dSlot0V = desc_sw128(sbase + Cfg::kSmemSlots, kBoxBytes, 1024);
+    const uint32_t tS0 = tbase + Cfg::kColS0, tS1 = tbase + Cfg::kColS1;
+    const uint32_t tO0 = tbase + Cfg::kColO0, tO1 = tbase + Cfg::kColO1;
+    auto slot_off16 = [](int it) {
+      return static_cast<uint64_t>(((it % Cfg::kSlots) * Cfg::kTileBytes) >> 4);
+    };
+    auto wait_full = [&](int it) {
+      return mbar_wait(smem_u32(&bars->slot_full[it % Cfg::kSlots]), (it / Cfg::kSlots) & 1,
+                       abort, p.status);
+    };
+    // S_t = Q_t K^T: K-major A and B, 16 columns (32 bytes) of d per instruction.
+    auto issue_s = [&](uint32_t tS, uint64_t dQ, int itK) {
+      const uint64_t dK = dSlot0K + slot_off16(itK);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_bf16_ss(tS(t), desc_sw128(sQ(t) + off, 16, 1024), desc_sw128(k_addr + off, 16, 1024),
-                      kIdescS, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_t += P_t V: P from TMEM (bf16 packed two per column), V MN-major in shared
-      // memory; 16 keys (2 KB of the V tile) per instruction.
-      auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_elect(tS, dQ + off16, dK + off16, kIdescS, kk > 0 ? 1u : 0u);
+      }
+    };
+    // O_t += P_t V: P from TMEM (bf16 packed two per column), V MN-major in shared
+    // memory; 16 keys (2 KB of the V tile) per instruction.
+    auto issue_pv = [&](uint32_t tO, uint32_t tP, int itV, bool acc) {
+      const uint64_t dV = dSlot0V + slot_off16(itV);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_bf16_ts(tO(t), tS(t) + kk * 8, desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024),
-                      kIdescPV, (acc || kk > 0) ? 1u : 0u);
-      };
+      for (int kk = 0; kk < kBlockN / 16; ++kk)
+        mma_bf16_ts_elect(tO, tP + kk * 8, dV + ((kk * 2048) >> 4), kIdescPV,
+                          (acc || kk > 0) ? 1u : 0u);
+    };
 
-      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort, p.status) && wait_full(0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, slot_addr(0));
-        mma_commit(smem_u32(&bars->s_full[0]));
-        issue_s(1, slot_addr(0));
-        mma_commit(smem_u32(&bars->s_full[1]));
-        mma_commit(smem_u32(&bars->slot_empty[0]));
-      }
-      for (int j = 0; ok && j < nb1; ++j) {
-        const int itV = 2 * j + 1, itK = 2 * j + 2;
-        if (!(ok = wait_full(itV))) break;
-        if (j < nb0) {
-          if (!(ok = mbar_wait(smem_u32(&bars->p_ready[0]), j & 1, abort, p.status))) break;
-          tc_fence_after();
-          issue_pv(0, slot_addr(itV), j > 0);
-          if (j + 1 < nb0) {
-            if (!(ok = wait_full(itK))) break;
-            tc_fence_after();
-            issue_s(0, slot_addr(itK));
-            mma_commit(smem_u32(&bars->s_full[0]));
-          } else {
-            mma_commit(smem_u32(&bars->o_final[0]));
-          }
-        }
-        if (!(ok = mbar_wait(smem_u32(&bars->p_ready[1]), j & 1, abort, p.status))) break;
-        tc_fence_after();
-        issue_pv(1, slot_addr(itV), j > 0);
-        mma_commit(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
-        if (j + 1 < nb1) {
-          if (!(ok = wait_full(itK))) break;
-          tc_fence_after();
-          issue_s(1, slot_addr(itK));
-          mma_commit(smem_u32(&bars->s_full[1]));
-          mma_commit(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
-        } else {
-          mma_commit(smem_u32(&bars->o_final[1]));
-        }
-      }
-      // Drain: nothing may still read shared memory or TMEM when the block exits.
-      mma_commit(smem_u32(&bars->mma_drain));
-      int no_abort = 0;
-      mbar_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
+    bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort, p.status) && wait_full(0);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      issue_s(tS0, dQ0, 0);
+      mma_commit_elect(smem_u32(&bars->s_full[0]));
+      issue_s(tS1, dQ1, 0);
+      mma_commit_elect(smem_u32(&bars->s_full[1]));
+      mma_commit_elect(smem_u32(&bars->slot_empty[0]));
     }
+    for (int j = 0; ok && j < nb1; ++j) {
+      const int itV = 2 * j + 1, itK = 2 * j + 2;
+      if (!(ok = __all_sync(0xffffffffu, wait_full(itV)))) break;
+      if (j < nb0) {
+        if (!(ok = __all_sync(0xffffffffu,
+                              mbar_wait(smem_u32(&bars->p_ready[0]), j & 1, abort, p.status))))
+          break;
+        tc_fence_after();
+        issue_pv(tO0, tS0, itV, j > 0);
+        if (j + 1 < nb0) {
+          if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
+          tc_fence_after();
+          issue_s(tS0, dQ0, itK);
+          mma_commit_elect(smem_u32(&bars->s_full[0]));
+        } else {
+          mma_commit_elect(smem_u32(&bars->o_final[0]));
+        }
+      }
+      if (!(ok = __all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(&bars->p_ready[1]), j & 1, abort, p.status))))
+        break;
+      tc_fence_after();
+      issue_pv(tO1, tS1, itV, j > 0);
+      mma_commit_elect(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
+      if (j + 1 < nb1) {
+        if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
+        tc_fence_after();
+        issue_s(tS1, dQ1, itK);
+        mma_commit_elect(smem_u32(&bars->s_full[1]));
+        mma_commit_elect(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
+      } else {
+        mma_commit_elect(smem_u32(&bars->o_final[1]));
+      }
+    }
+    // Drain: nothing may still read shared memory or TMEM when the block exits.
+    mma_commit_elect(smem_u32(&bars->mma_drain));
+    int no_abort = 0;
+    mbar_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax tile t
+    regs_increase<kRegsSoftmax>();
     const int t = warp >> 2;       // warps 0-3 -> tile 0, 4-7 -> tile 1
     const int wq = warp & 3;       // TMEM lane quarter this warp may access
     const int rr = wq * 32 + lane; // row within the tile
@@ -224,9 +259,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld128_wait(tS, sr);
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+      float* s = reinterpret_cast<float*>(sr);
 
       // Mask: keys >= N (ragged last tile) and, on the diagonal tile, keys > row.
       const int key0 = j * kBlockN;
@@ -238,13 +271,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
       }
 
-      float mx[8];
+      // Row max: four independent chains of three-input max.
+      float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float rowmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 4; c < 128; c += 2) mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], s[c], s[c + 1]);
+      const float rowmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       const float m2_new = fmaxf(m2, rowmax * sl2);
       const float m2_use = (m2_new > m2 + kRescaleLog2) ? m2_new : m2;
       const float alpha = ex2_approx(m2 - m2_use);  // 1 if unchanged, 0 on the first tile
@@ -263,25 +294,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       m2 = m2_use;
 
-      // P = exp2(s * scale * log2 e - m2), row sum in fp32, P packed to bf16 pairs
-      // and stored over the first 64 columns of S_t.
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = exp2(s * scale * log2 e - m2) on pairs (packed fp32 FMA, two MUFU ex2),
+      // row sum in packed fp32, P packed to bf16 pairs and stored over the first 64
+      // columns of S_t in four pieces.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t negm2 = f2_pack(-m2, -m2);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
+      for (int h = 0; h < 4; ++h) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(fmaf(s[64 * h + 2 * i], sl2, -m2));
-          const float p1 = ex2_approx(fmaf(s[64 * h + 2 * i + 1], sl2, -m2));
-          sum[i & 3] += p0 + p1;
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * h + 2 * i;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tS + 32 * h, pk);
+        tmem_st16(tS + 16 * h, pk);
       }
-      l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      float a0, a1, a2, a3, a4, a5, a6, a7;
+      f2_unpack(acc[0], a0, a1);
+      f2_unpack(acc[1], a2, a3);
+      f2_unpack(acc[2], a4, a5);
+      f2_unpack(acc[3], a6, a7);
+      l = l * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars->p_ready[t]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready[t]));
     }
 
     if (ok) {
