@@ -94,6 +94,25 @@ def recorded_traffic(kernel):
     return ent.get("dram_bytes_per_launch")
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(values, device):
+    """Element-wise max of a list of floats over all ranks (a no-op on one rank): the
+    timing rule is the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def rank_env():
+    """(world, rank, local_rank) from the launcher's environment (1, 0, 0 if absent)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -389,10 +408,7 @@ def our_arm(args, rank, world, local_rank):
     attn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     rows_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     step_ms = t_start.elapsed_time(t_end) / args.steps
-    if world > 1:
-        t = torch.tensor([attn_ms, rows_ms, step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        attn_ms, rows_ms, step_ms = (float(z) for z in t.tolist())
+    attn_ms, rows_ms, step_ms = max_over_ranks([attn_ms, rows_ms, step_ms], dev)
 
     flops = attn_flops(B, H, N, d, causal)
     rbytes = row_bytes(rows, length)
@@ -417,10 +433,7 @@ def our_arm(args, rank, world, local_rank):
         attention_forward(qh, kh, vh, scale, causal, out=oh, lse_out=lh)
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks([e2e_s], dev)[0]
     h2d = 3 * qh.numel() * 2
     d2h = oh.numel() * 2 + lh.numel() * 4
 
@@ -483,9 +496,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local_rank = rank_env()
     if world > 1 and args.impl == "ours":
         import torch
         import torch.distributed as dist
