@@ -49,7 +49,8 @@ typedef enum {
 
 typedef enum {
   FA_BF16 = 0,             /* q, k, v, o bf16; fp32 scores, softmax state and O accumulator */
-  FA_F32 = 1               /* q, k, v, o fp32; fp32 arithmetic on CUDA cores                */
+  FA_F32 = 1,              /* q, k, v, o fp32; fp32 arithmetic on CUDA cores                */
+  FA_F16 = 2               /* q, k, v, o fp16; as FA_BF16 with P and O rounded to fp16      */
 } fa_dtype;
 
 /*
@@ -73,9 +74,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 /*
  * Attention forward with an explicit element type. fa_fwd(...) is
- * fa_fwd_dt(..., FA_BF16, stream). With FA_F32, q, k, v and o are fp32 [B, H, N, d]
- * (4-byte aligned), d may be any value in 1..128, and all arithmetic is fp32 on CUDA
- * cores (the same online-softmax tile loop, 32 keys per tile).
+ * fa_fwd_dt(..., FA_BF16, stream). With FA_F16, q, k, v and o are fp16 with the same
+ * layout, alignment and d as for bf16 (the tensor-core path; P is rounded to fp16, whose
+ * range holds it: P <= 2^8). With FA_F32, q, k, v and o are fp32 [B, H, N, d] (4-byte
+ * aligned), d may be any value in 1..128, and all arithmetic is fp32 on CUDA cores (the
+ * same online-softmax tile loop, 32 keys per tile).
  */
 fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float* lse,
                     int B, int H, int N, int d, float scale, int causal,
@@ -92,6 +95,20 @@ fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float*
  */
 fa_status online_softmax_rows(const float* x, float* m_out, float* l_out,
                               int rows, int len, cudaStream_t stream);
+
+/*
+ * Row softmax: y[r, t] = exp(x[r, t] - m_r) / l_r with m_r, l_r as in
+ * online_softmax_rows ("Softmax 数值稳定性与 IO-Aware Attention", §三: the third pass,
+ * here fused with the (m, l) reduction).  Rows of up to 32768 floats are read from
+ * device memory once; longer rows twice.
+ *
+ * x:     device fp32 [rows, len], contiguous; any 4-byte alignment.
+ * y:     device fp32 [rows, len], written; may alias x (in place); any 4-byte alignment.
+ * m_out, l_out: device fp32 [rows], written with the row state, or NULL.
+ * rows:  >= 0 (0 = nothing to do).  len: >= 1 when rows > 0.
+ */
+fa_status online_softmax_forward(const float* x, float* y, float* m_out, float* l_out,
+                                 int rows, int len, cudaStream_t stream);
 
 /* Static, never-NULL description of a status code. */
 const char* fa_status_str(fa_status status);

@@ -12,15 +12,16 @@ from __future__ import annotations
 import math
 
 from . import abi
-from .abi import FAError, fa_fwd, fa_fwd_dt, online_softmax_rows, fa_last_device_error
+from .abi import (FAError, fa_fwd, fa_fwd_dt, online_softmax_rows, online_softmax_forward,
+                  fa_last_device_error)
 
-__all__ = ["attention_forward", "row_state", "abi", "FAError", "fa_fwd", "fa_fwd_dt",
-           "online_softmax_rows", "fa_last_device_error"]
+__all__ = ["attention_forward", "row_state", "softmax", "abi", "FAError", "fa_fwd", "fa_fwd_dt",
+           "online_softmax_rows", "online_softmax_forward", "fa_last_device_error"]
 
 
 def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=True,
                       out=None, lse_out=None):
-    """O = softmax(scale * Q K^T) V and LSE for [B, H, N, d] tensors (bf16 or fp32).
+    """O = softmax(scale * Q K^T) V and LSE for [B, H, N, d] tensors (bf16, fp16 or fp32).
 
     Returns (O, LSE) with O of q's dtype and LSE fp32 [B, H, N] (None without
     ``with_lse``), on q's device.  For CPU inputs the copies to and from the current
@@ -36,8 +37,9 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
             return attention_forward(q, k, v, scale, causal, None, with_lse, out, lse_out)
     if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must be [B, H, N, d] of one shape")
-    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("q, k, v must all be bf16 or all fp32")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float16,
+                                                               torch.float32):
+        raise ValueError("q, k, v must all be bf16, all fp16 or all fp32")
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -56,7 +58,8 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if with_lse else None
-    dtype = abi.FA_BF16 if q.dtype == torch.bfloat16 else abi.FA_F32
+    dtype = {torch.bfloat16: abi.FA_BF16, torch.float16: abi.FA_F16,
+             torch.float32: abi.FA_F32}[q.dtype]
     fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), dtype)
     if not host:
         return o, lse
@@ -95,3 +98,21 @@ def row_state(x, stream=None):
     if host:
         return m.cpu(), l.cpu()
     return m, l
+
+
+def softmax(x, stream=None):
+    """Row softmax of an fp32 [rows, len] CUDA tensor; returns (y, m, l)."""
+    import torch
+
+    if stream is not None:
+        with torch.cuda.stream(stream):
+            return softmax(x, None)
+    if x.dim() != 2 or x.dtype != torch.float32 or not x.is_cuda:
+        raise ValueError("x must be an fp32 [rows, len] CUDA tensor")
+    x = x.contiguous()
+    rows, length = x.shape
+    y = torch.empty_like(x)
+    m = torch.empty(rows, dtype=torch.float32, device=x.device)
+    l = torch.empty(rows, dtype=torch.float32, device=x.device)
+    online_softmax_forward(x, y, m, l, rows, length)
+    return y, m, l

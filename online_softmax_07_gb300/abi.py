@@ -1,8 +1,8 @@
 """ctypes binding of the C ABI in include/fa.h (argument marshalling only).
 
 The functions here carry the C names and signatures: ``fa_fwd``, ``fa_fwd_dt``,
-``online_softmax_rows``, ``fa_status_str``, ``fa_last_device_error`` and
-``fa_selftest_wait_timeout``.  Pointer arguments accept a CUDA ``torch.Tensor``
+``online_softmax_rows``, ``online_softmax_forward``, ``fa_status_str``,
+``fa_last_device_error`` and ``fa_selftest_wait_timeout``.  Pointer arguments accept a CUDA ``torch.Tensor``
 (its data pointer is passed), an ``int`` address, or ``None`` (NULL).  A non-OK
 status raises :class:`FAError`.  Every computation runs in the library's CUDA
 kernels; there is no other implementation to fall back to, and loading fails
@@ -15,7 +15,7 @@ import ctypes
 import os
 
 FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
-FA_BF16, FA_F32 = 0, 1
+FA_BF16, FA_F32, FA_F16 = 0, 1, 2
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libosfa.so")
 
@@ -27,6 +27,8 @@ _SIGNATURES = {
                   + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "online_softmax_rows": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2
                             + [ctypes.c_void_p]),
+    "online_softmax_forward": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 2
+                               + [ctypes.c_void_p]),
     "fa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_last_device_error": (ctypes.c_int, [ctypes.c_void_p]),
     "fa_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_longlong, ctypes.c_void_p]),
@@ -107,6 +109,11 @@ def fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream=None) ->
 def online_softmax_rows(x, m_out, l_out, rows, length, stream=None) -> None:
     _check(load().online_softmax_rows(_ptr(x), _ptr(m_out), _ptr(l_out), rows, length,
                                       _stream(stream)), "online_softmax_rows")
+
+
+def online_softmax_forward(x, y, m_out, l_out, rows, length, stream=None) -> None:
+    _check(load().online_softmax_forward(_ptr(x), _ptr(y), _ptr(m_out), _ptr(l_out), rows, length,
+                                         _stream(stream)), "online_softmax_forward")
 
 
 def fa_last_device_error(stream=None) -> int:

@@ -58,11 +58,11 @@ cudaError_t encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return cudaSuccess;
 }
 
-// A [BH, N, d] bf16 tensor seen by TMA as 3-D (d innermost), boxes of 128 rows x 64
+// A [BH, N, d] bf16 or fp16 tensor seen by TMA as 3-D (d innermost), boxes of 128 rows x 64
 // columns (128 bytes) with the 128-byte swizzle.  Rows past N read as zero and are
 // not written by stores.
 bool encode_bhnd(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base,
-                 int BH, int N, int d) {
+                 int BH, int N, int d, bool f16) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
@@ -70,7 +70,8 @@ bool encode_bhnd(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const vo
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxCols), static_cast<cuuint32_t>(kBlockM),
                              1};
   const cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides,
                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -125,8 +126,8 @@ fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float*
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID;
-  if (dtype != FA_BF16 && dtype != FA_F32) return FA_ERR_UNSUPPORTED;
-  if (dtype == FA_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_BF16 && dtype != FA_F32 && dtype != FA_F16) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_F32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_F32 && (d < 1 || d > 128)) return FA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > INT_MAX) return FA_ERR_INVALID;
@@ -152,8 +153,9 @@ fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float*
   if ((e = encode_fn(&enc)) != cudaSuccess) return FA_ERR_CUDA;
   CUtensorMap tq, tk, tv, to;
   const int bh = static_cast<int>(BH);
-  if (!encode_bhnd(enc, &tq, q, bh, N, d) || !encode_bhnd(enc, &tk, k, bh, N, d) ||
-      !encode_bhnd(enc, &tv, v, bh, N, d) || !encode_bhnd(enc, &to, o, bh, N, d))
+  const bool f16 = dtype == FA_F16;
+  if (!encode_bhnd(enc, &tq, q, bh, N, d, f16) || !encode_bhnd(enc, &tk, k, bh, N, d, f16) ||
+      !encode_bhnd(enc, &tv, v, bh, N, d, f16) || !encode_bhnd(enc, &to, o, bh, N, d, f16))
     return FA_ERR_CUDA;
   AttnTcParams p;
   p.lse = lse;
@@ -167,8 +169,12 @@ fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float*
       std::max(1LL, std::min(BH, (64LL << 20) / std::max(1LL, kv_head_bytes))));
   p.causal = causal;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  e = (d == 64) ? launch_attn_tc<64>(tq, tk, tv, to, p, stream)
-                : launch_attn_tc<128>(tq, tk, tv, to, p, stream);
+  if (d == 64)
+    e = f16 ? launch_attn_tc<64, true>(tq, tk, tv, to, p, stream)
+            : launch_attn_tc<64, false>(tq, tk, tv, to, p, stream);
+  else
+    e = f16 ? launch_attn_tc<128, true>(tq, tk, tv, to, p, stream)
+            : launch_attn_tc<128, false>(tq, tk, tv, to, p, stream);
   return from_cuda(e);
 }
 
@@ -185,6 +191,18 @@ fa_status online_softmax_rows(const float* x, float* m_out, float* l_out, int ro
   if (x == nullptr || m_out == nullptr || l_out == nullptr) return FA_ERR_INVALID;
   if (!aligned(x, 4) || !aligned(m_out, 4) || !aligned(l_out, 4)) return FA_ERR_ALIGN;
   return from_cuda(launch_row_state(x, m_out, l_out, rows, len, stream));
+}
+
+fa_status online_softmax_forward(const float* x, float* y, float* m_out, float* l_out, int rows,
+                                 int len, cudaStream_t stream) {
+  if (rows < 0 || len < 0) return FA_ERR_INVALID;
+  if (rows == 0) return FA_OK;
+  if (len == 0) return FA_ERR_INVALID;
+  if (x == nullptr || y == nullptr) return FA_ERR_INVALID;
+  if (!aligned(x, 4) || !aligned(y, 4) || (m_out != nullptr && !aligned(m_out, 4)) ||
+      (l_out != nullptr && !aligned(l_out, 4)))
+    return FA_ERR_ALIGN;
+  return from_cuda(launch_softmax_rows(x, y, m_out, l_out, rows, len, stream));
 }
 
 fa_status fa_last_device_error(cudaStream_t stream) {

@@ -74,7 +74,8 @@ struct AttnTcParams {
   float scale_log2;    // scale * log2(e)
 };
 
-template <int D>
+// F16 = false: bf16 Q, K, V, O (and P); F16 = true: fp16.
+template <int D, bool F16>
 cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, const AttnTcParams& p, cudaStream_t stream);
 

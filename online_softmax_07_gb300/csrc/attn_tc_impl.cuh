@@ -29,14 +29,28 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
-// B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16 (format 1) or
+// both fp16 (format 0), A K-major, B K-major or MN-major, N >> 3 at bit 17, M >> 4 at
+// bit 24.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool b_mn_major, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-template <int D>
+// Two fp32 to the kernel's 16-bit element type (round to nearest even), `lo` in bits 0..15.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_elem2(float lo, float hi) {
+  if constexpr (F16) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  } else {
+    return pack_bf16x2(lo, hi);
+  }
+}
+
+template <int D, bool F16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -150,8 +164,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop with warp-uniform values; elect.sync inside the
     // MMA and commit wrappers lets one lane issue each instruction.
-    constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false);
-    constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, true);
+    constexpr uint32_t kIdescS = idesc_f16kind(kBlockM, kBlockN, false, F16);
+    constexpr uint32_t kIdescPV = idesc_f16kind(kBlockM, D, true, F16);
     // Descriptors of the tile bases; an operand at byte offset `off` inside a tile is
     // base + (off >> 4) (the start-address field never overflows: shared memory is
     // below 256 KB).
@@ -311,7 +325,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
           acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+          pk[i] = pack_elem2<F16>(p0, p1);
         }
         tmem_st16(tS + 16 * h, pk);
       }
@@ -344,7 +358,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          pk[i] = pack_elem2<F16>(__uint_as_float(o[2 * i]) * inv_l,
+                                  __uint_as_float(o[2 * i + 1]) * inv_l);
         // columns 32c .. 32c+31 = box (32c / 64), 16-byte chunks (32c % 64) / 8 .. +3
         uint8_t* rowp = stage + (c >> 1) * kBoxBytes + rr * 128;
 #pragma unroll
@@ -376,17 +391,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, const AttnTcParams& p, cudaStream_t stream) {
   using Cfg = AttnTcCfg<D>;
   static_assert(sizeof(AttnTcBarriers) <= 512, "barrier block");
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, F16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.nqb) * p.BH;
-  attn_fwd_tc_kernel<D><<<static_cast<unsigned>(grid), kAttnThreads, Cfg::kSmemBytes, stream>>>(
+  attn_fwd_tc_kernel<D, F16><<<static_cast<unsigned>(grid), kAttnThreads, Cfg::kSmemBytes, stream>>>(
       tq, tk, tv, to, p);
   return cudaGetLastError();
 }

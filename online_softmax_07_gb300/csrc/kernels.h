@@ -12,6 +12,9 @@ cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, floa
 cudaError_t launch_row_state(const float* x, float* m_out, float* l_out, int rows, int len,
                              cudaStream_t stream);
 
+cudaError_t launch_softmax_rows(const float* x, float* y, float* m_out, float* l_out, int rows,
+                                int len, cudaStream_t stream);
+
 cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned long long limit_ns,
                                          cudaStream_t stream);
 

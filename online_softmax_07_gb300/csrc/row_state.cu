@@ -164,6 +164,157 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Normalised row softmax y = exp(x - m) / l ("Softmax 数值稳定性与 IO-Aware Attention", §三,
+// pass three), with the state (m, l) from the same reduction as above.  A row of up to
+// kCacheVec * 4 * kBlockThreads floats stays in registers between the state and the
+// output, so x is read once and y written once; longer rows are streamed twice.
+
+constexpr int kCacheVec = 16;  // float4 per thread kept in registers (32768 floats per row)
+
+__device__ __forceinline__ State block_merge(State st, State* warp_states) {
+  st = warp_merge(st);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // warp_states may still be read from a previous merge
+  if (lane == 0) warp_states[warp] = st;
+  __syncthreads();
+  st = (lane < kBlockThreads / 32) ? warp_states[lane] : State{-INFINITY, 0.f};
+  return warp_merge(st);  // every warp computes the block result
+}
+
+__global__ void __launch_bounds__(kBlockThreads)
+    softmax_rows_block_kernel(const float* x, float* y,  // y may alias x
+                              float* __restrict__ m_out, float* __restrict__ l_out, int len) {
+  __shared__ State warp_states[kBlockThreads / 32];
+  const int64_t row = blockIdx.x;
+  const float* xr = x + row * static_cast<int64_t>(len);
+  float* yr = y + row * static_cast<int64_t>(len);
+  const int tid = threadIdx.x;
+  const int head =
+      min(len, static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(xr) & 15)) & 15) >> 2));
+  const int nvec = (len - head) >> 2;
+  const int tail0 = head + 4 * nvec;
+  const int extra = head + (len - tail0);
+  const float4* xv = reinterpret_cast<const float4*>(xr + head);
+  // y can take 16-byte stores only where it has x's alignment
+  const bool y_vec = ((reinterpret_cast<uintptr_t>(yr) ^ reinterpret_cast<uintptr_t>(xr)) & 15) == 0;
+  const bool cached = nvec <= kCacheVec * kBlockThreads;
+
+  State st = {-INFINITY, 0.f};
+  float e0 = 0.f;
+  if (tid < extra) {
+    e0 = xr[tid < head ? tid : tail0 + (tid - head)];
+    float e[1] = {e0};
+    fold<1>(st, e, 1);
+  }
+  float4 c[kCacheVec];
+  if (cached) {
+#pragma unroll
+    for (int u = 0; u < kCacheVec; ++u) {
+      const int i = u * kBlockThreads + tid;
+      c[u] = (i < nvec) ? __ldcs(xv + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u0 = 0; u0 < kCacheVec; u0 += 8) {
+      float v[32];
+      int cnt = 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        v[4 * u] = c[u0 + u].x;
+        v[4 * u + 1] = c[u0 + u].y;
+        v[4 * u + 2] = c[u0 + u].z;
+        v[4 * u + 3] = c[u0 + u].w;
+        if ((u0 + u) * kBlockThreads + tid < nvec) cnt = 4 * (u + 1);
+      }
+      fold<32>(st, v, cnt);
+    }
+  } else {
+    for (int base = 0; base < nvec; base += kUnroll * kBlockThreads) {
+      float v[4 * kUnroll];
+      int cnt = 0;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i = base + u * kBlockThreads + tid;
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < nvec) {
+          f = xv[i];
+          cnt = 4 * (u + 1);
+        }
+        v[4 * u] = f.x;
+        v[4 * u + 1] = f.y;
+        v[4 * u + 2] = f.z;
+        v[4 * u + 3] = f.w;
+      }
+      fold<4 * kUnroll>(st, v, cnt);
+    }
+  }
+  st = block_merge(st, warp_states);
+  if (tid == 0) {
+    if (m_out != nullptr) m_out[row] = st.m;
+    if (l_out != nullptr) l_out[row] = st.l;
+  }
+  const float m = st.m, inv_l = 1.0f / st.l;
+  auto out = [&](float xv_) { return exp_diff(xv_, m) * inv_l; };
+  if (tid < extra) yr[tid < head ? tid : tail0 + (tid - head)] = out(e0);
+  float* yv = yr + head;
+  auto store4 = [&](int i, float4 f) {
+    const float4 r = make_float4(out(f.x), out(f.y), out(f.z), out(f.w));
+    if (y_vec) {
+      __stcs(reinterpret_cast<float4*>(yv) + i, r);
+    } else {
+      yv[4 * i] = r.x;
+      yv[4 * i + 1] = r.y;
+      yv[4 * i + 2] = r.z;
+      yv[4 * i + 3] = r.w;
+    }
+  };
+  if (cached) {
+#pragma unroll
+    for (int u = 0; u < kCacheVec; ++u) {
+      const int i = u * kBlockThreads + tid;
+      if (i < nvec) store4(i, c[u]);
+    }
+  } else {
+    for (int i = tid; i < nvec; i += kBlockThreads) store4(i, __ldcs(xv + i));
+  }
+}
+
+// One warp per row, for short rows: the row stays in registers (up to 32 per lane).
+__global__ void __launch_bounds__(256)
+    softmax_rows_warp_kernel(const float* x, float* y,  // y may alias x
+                             float* __restrict__ m_out, float* __restrict__ l_out, int rows,
+                             int len) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float* xr = x + row * static_cast<int64_t>(len);
+  float* yr = y + row * static_cast<int64_t>(len);
+  float v[32];
+  int cnt = 0;
+#pragma unroll
+  for (int u = 0; u < 32; ++u) {
+    const int i = u * 32 + lane;
+    v[u] = 0.f;
+    if (i < len) {
+      v[u] = __ldcs(xr + i);
+      cnt = u + 1;
+    }
+  }
+  State st = {-INFINITY, 0.f};
+  fold<32>(st, v, cnt);
+  st = warp_merge(st);
+  if (lane == 0) {
+    if (m_out != nullptr) m_out[row] = st.m;
+    if (l_out != nullptr) l_out[row] = st.l;
+  }
+  const float inv_l = 1.0f / st.l;
+#pragma unroll
+  for (int u = 0; u < 32; ++u) {
+    const int i = u * 32 + lane;
+    if (i < len) __stcs(yr + i, exp_diff(v[u], st.m) * inv_l);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_row_state(const float* x, float* m_out, float* l_out, int rows, int len,
@@ -174,6 +325,18 @@ cudaError_t launch_row_state(const float* x, float* m_out, float* l_out, int row
   } else {
     row_state_block_kernel<<<static_cast<unsigned>(rows), kBlockThreads, 0, stream>>>(x, m_out,
                                                                                      l_out, len);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_rows(const float* x, float* y, float* m_out, float* l_out, int rows,
+                                int len, cudaStream_t stream) {
+  if (len <= 1024) {
+    const unsigned grid = static_cast<unsigned>((static_cast<long long>(rows) + 7) / 8);
+    softmax_rows_warp_kernel<<<grid, 256, 0, stream>>>(x, y, m_out, l_out, rows, len);
+  } else {
+    softmax_rows_block_kernel<<<static_cast<unsigned>(rows), kBlockThreads, 0, stream>>>(
+        x, y, m_out, l_out, len);
   }
   return cudaGetLastError();
 }

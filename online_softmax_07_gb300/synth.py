@@ -46,14 +46,21 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
         torch.bfloat16).to(torch.float32).numpy()
 
 
+def round_to_f16(x: np.ndarray) -> np.ndarray:
+    """fp32 -> nearest fp16 (ties to even), returned as fp32 holding fp16 values."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
 def attention_inputs(B, H, N, d, seed, dtype="bf16", q_std=1.0, kv_std=1.0):
-    """q, k, v as fp32 numpy [B, H, N, d], i.i.d. normal; bf16-representable when
-    dtype == 'bf16' (the values the GPU path receives, exactly)."""
+    """q, k, v as fp32 numpy [B, H, N, d], i.i.d. normal; bf16- (or fp16-) representable
+    when dtype == 'bf16' ('f16'): the values the GPU path receives, exactly."""
     q = _normal(seed + 0, (B, H, N, d), q_std)
     k = _normal(seed + 1, (B, H, N, d), kv_std)
     v = _normal(seed + 2, (B, H, N, d), kv_std)
     if dtype == "bf16":
         q, k, v = round_to_bf16(q), round_to_bf16(k), round_to_bf16(v)
+    elif dtype == "f16":
+        q, k, v = round_to_f16(q), round_to_f16(k), round_to_f16(v)
     elif dtype != "f32":
         raise ValueError(dtype)
     return q, k, v

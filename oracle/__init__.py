@@ -12,6 +12,7 @@ blocking, fusion or reordering beyond what the definition states:
 * ``row_state``          -- per-row (m, l) of the safe softmax
                             ("Softmax 数值稳定性与 IO-Aware Attention：从在线归一化到
                             FlashAttention", §二 2.1 and §三).
+* ``softmax_rows``       -- the normalised row softmax, pass three of §三.
 * ``attention_forward``  -- standard attention S = scale*Q K^T, P = softmax(S),
                             O = P V, plus LSE = m + ln l (same page, §七; the
                             scale follows "为什么 Flash Attention 算出来的结果和标准
@@ -23,7 +24,7 @@ only to cross-check the three-pass forms above.  Parity status of every function
 is pinned by ``tests/test_oracle_pins.py``; no function here is unpinned.
 """
 
-from .reference import attention_forward, row_state, visible_mask
+from .reference import attention_forward, row_state, softmax_rows, visible_mask
 from .online import (
     online_weighted_sum,
     online_state,
@@ -34,6 +35,7 @@ from .online import (
 __all__ = [
     "attention_forward",
     "row_state",
+    "softmax_rows",
     "visible_mask",
     "online_weighted_sum",
     "online_state",

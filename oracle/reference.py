@@ -50,6 +50,17 @@ def row_state(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return m, l
 
 
+def softmax_rows(x: np.ndarray) -> np.ndarray:
+    """Row-wise softmax of a [rows, len] array, in float64.
+
+    "Softmax 数值稳定性与 IO-Aware Attention：从在线归一化到 FlashAttention", §三: pass one
+    m = max_t x_t, pass two l = sum_t exp(x_t - m), pass three y_t = exp(x_t - m) / l.
+    """
+    m, l = row_state(x)
+    x = np.asarray(x, dtype=np.float64)
+    return np.exp(x - m[:, None]) / l[:, None]          # pass 3
+
+
 def attention_forward(q, k, v, scale: float, causal: bool, rows=None):
     """Standard attention in float64; returns (O, LSE).
 

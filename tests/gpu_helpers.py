@@ -28,12 +28,12 @@ def to_device(x, dtype):
 def run_attention(q, k, v, scale, causal, dtype="bf16", with_lse=True):
     """Calls fa_fwd_dt through the C ABI; returns O (fp32 numpy) and LSE."""
     import torch
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
     B, H, N, d = q.shape
     dq, dk, dv = to_device(q, tdt), to_device(k, tdt), to_device(v, tdt)
     o = torch.full_like(dq, float("nan"))
     lse = torch.full((B, H, N), float("nan"), device="cuda") if with_lse else None
-    code = abi.FA_BF16 if dtype == "bf16" else abi.FA_F32
+    code = {"bf16": abi.FA_BF16, "f16": abi.FA_F16, "f32": abi.FA_F32}[dtype]
     abi.fa_fwd_dt(dq, dk, dv, o, lse, B, H, N, d, scale, int(causal), code)
     assert abi.fa_last_device_error() == abi.FA_OK
     o_h = o.float().cpu().numpy()
@@ -55,7 +55,7 @@ def run_rows(x):
 def check_attention(o, lse, o_ref, lse_ref, dtype="bf16"):
     err = np.abs(o.astype(np.float64) - o_ref)
     assert np.all(np.isfinite(o)), "non-finite output"
-    if dtype == "bf16":
+    if dtype in ("bf16", "f16"):
         assert err.max() <= BF16_O_MAX_ABS, f"O max abs err {err.max():.3e}"
         assert err.mean() <= BF16_O_MEAN_ABS, f"O mean abs err {err.mean():.3e}"
         lse_tol = LSE_ABS

@@ -164,3 +164,22 @@ def test_workload_b2h16n8191d128_causal_sampled():
 
 def test_workload_b1h8n32768d128_causal_qstd4_sampled():
     _full_size("attn_bf16_b1h8n32768d128_causal_qstd4", 256)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 129, 300, 640])
+def test_f16_small_all_rows(N, d, causal):
+    """fp16 inputs through the same tensor-core kernel (operand format F16)."""
+    q, k, v = synth.attention_inputs(2, 2, N, d, seed=77000 + N + d + int(causal), dtype="f16")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_attention(q, k, v, scale, causal, dtype="f16")
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, scale, causal)
+    check_attention(o, lse, o_ref, lse_ref, dtype="f16")
+
+
+def test_f16_large_logits():
+    q, k, v = synth.attention_inputs(1, 4, 1000, 128, seed=78000, dtype="f16", q_std=4.0)
+    o, lse = run_attention(q, k, v, 1 / math.sqrt(128), True, dtype="f16")
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, 1 / math.sqrt(128), True)
+    check_attention(o, lse, o_ref, lse_ref, dtype="f16")

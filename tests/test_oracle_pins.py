@@ -385,3 +385,35 @@ def test_unmutated_copy_passes_and_alpha_mutant_caught():
     with np.errstate(all="ignore"):
         assert not _fails_some_pin(_mutant("none"))
         assert _fails_some_pin(_tiled_mutant_alpha_on_l_only)
+
+
+# ----------------------------------------------------------------------------
+# Tests of the row softmax output (pass three)
+# ----------------------------------------------------------------------------
+
+def test_softmax_rows_worked_example_weights():
+    """The weights behind the worked example: e^s / (1 + e + e^2) for s = 0, 1, 2, and
+    their weighted sum of the values reproduces the printed 25.752104."""
+    g = _golden()
+    y = oracle.softmax_rows(np.array([g["scores"]]))[0]
+    z = 1 + math.e + math.e ** 2
+    assert np.allclose(y, [1 / z, math.e / z, math.e ** 2 / z], rtol=1e-15, atol=0)
+    assert round(float(y @ np.array(g["values"])), 6) == g["result_6dp"][0]
+
+
+def test_softmax_rows_properties():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((6, 41)) * 3
+    y = oracle.softmax_rows(x)
+    assert np.allclose(y.sum(axis=1), 1.0, atol=1e-14)          # rows sum to one
+    assert np.all(y > 0)
+    assert np.all(np.argsort(y, axis=1) == np.argsort(x, axis=1))  # monotone in x
+    y2 = oracle.softmax_rows(x + 1000.0)                           # shift invariance
+    assert np.allclose(y2, y, rtol=1e-11, atol=0)
+    # naive softmax where it does not overflow
+    xs = rng.uniform(-5, 5, (3, 9))
+    naive = np.exp(xs) / np.exp(xs).sum(axis=1, keepdims=True)
+    assert np.allclose(oracle.softmax_rows(xs), naive, rtol=1e-14)
+    # all-equal rows are uniform, length-1 rows are 1
+    assert np.all(oracle.softmax_rows(np.full((2, 8), -7.0)) == 0.125)
+    assert np.all(oracle.softmax_rows(np.array([[1e4], [-3.0]])) == 1.0)
