@@ -31,6 +31,8 @@
 #ifndef ONLINE_SOFTMAX_07_GB300_FA_H
 #define ONLINE_SOFTMAX_07_GB300_FA_H
 
+#include <stddef.h>
+
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -83,6 +85,36 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float* lse,
                     int B, int H, int N, int d, float scale, int causal,
                     fa_dtype dtype, cudaStream_t stream);
+
+/*
+ * Split-KV attention forward.  Same operation, arguments and results as fa_fwd_dt (bf16
+ * or fp16, d in {64, 128}); each query block's K/V tiles are divided into num_splits
+ * contiguous chunks processed by separate thread blocks, which raises the parallelism
+ * when B * H * ceil(N / 256) is small next to the number of SMs.  Each chunk's result
+ * (O normalised by its own denominator, and its LSE) goes to `workspace`; a second
+ * kernel merges them by bringing them to a common maximum, as the lihaoran.work
+ * FlashAttention note ("为什么不能平均各块的softmax") and the merge rule of "Softmax
+ * 数值稳定性与 IO-Aware Attention" §4.1 prescribe (partial results are not averaged).
+ *
+ * num_splits: 1..64 (1 = fa_fwd_dt; the workspace is then unused).
+ * workspace:  device memory of at least fa_fwd_splitkv_workspace_bytes(...) bytes,
+ *             16-byte aligned, owned by the caller; its contents need no initialisation
+ *             and are overwritten.  Calls that share a workspace must not overlap.
+ * Errors: as fa_fwd_dt, plus FA_ERR_INVALID for num_splits out of range, a NULL or too
+ * small workspace (num_splits > 1), FA_ERR_ALIGN for a misaligned workspace.
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal, int num_splits,
+                         void* workspace, size_t workspace_bytes, fa_dtype dtype,
+                         cudaStream_t stream);
+
+/* Workspace bytes fa_fwd_splitkv needs: num_splits * B * H * ceil(N/256)*256 * (d + 1) * 4
+ * (0 for invalid arguments).  Host-only, no CUDA call. */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
+
+/* A split count for fa_fwd_splitkv on the current device: enough thread blocks for two
+ * waves of its SMs, at least two K/V tiles per split, at most 64 (1 when no split pays). */
+int fa_fwd_splitkv_default_splits(int B, int H, int N);
 
 /*
  * Row online-softmax state.

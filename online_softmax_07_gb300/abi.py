@@ -1,6 +1,7 @@
 """ctypes binding of the C ABI in include/fa.h (argument marshalling only).
 
 The functions here carry the C names and signatures: ``fa_fwd``, ``fa_fwd_dt``,
+``fa_fwd_splitkv``, ``fa_fwd_splitkv_workspace_bytes``, ``fa_fwd_splitkv_default_splits``,
 ``online_softmax_rows``, ``online_softmax_forward``, ``fa_status_str``,
 ``fa_last_device_error`` and ``fa_selftest_wait_timeout``.  Pointer arguments accept a CUDA ``torch.Tensor``
 (its data pointer is passed), an ``int`` address, or ``None`` (NULL).  A non-OK
@@ -25,6 +26,11 @@ _SIGNATURES = {
                + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_dt": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 4
                   + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "fa_fwd_splitkv": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 4
+                       + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                          ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
+    "fa_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 5),
+    "fa_fwd_splitkv_default_splits": (ctypes.c_int, [ctypes.c_int] * 3),
     "online_softmax_rows": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2
                             + [ctypes.c_void_p]),
     "online_softmax_forward": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 2
@@ -104,6 +110,22 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream=None) -> None:
 def fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream=None) -> None:
     _check(load().fa_fwd_dt(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
                             float(scale), int(causal), int(dtype), _stream(stream)), "fa_fwd_dt")
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,
+                   workspace_bytes, dtype, stream=None) -> None:
+    _check(load().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                 float(scale), int(causal), int(num_splits), _ptr(workspace),
+                                 int(workspace_bytes), int(dtype), _stream(stream)),
+           "fa_fwd_splitkv")
+
+
+def fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits) -> int:
+    return int(load().fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits))
+
+
+def fa_fwd_splitkv_default_splits(B, H, N) -> int:
+    return int(load().fa_fwd_splitkv_default_splits(B, H, N))
 
 
 def online_softmax_rows(x, m_out, l_out, rows, length, stream=None) -> None:

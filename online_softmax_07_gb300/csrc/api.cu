@@ -22,6 +22,7 @@ namespace {
 __device__ unsigned g_device_status;
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 64;
 std::mutex g_mutex;
 unsigned* g_status_ptr[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -120,33 +121,39 @@ const char* fa_status_str(fa_status s) {
   return "unknown status";
 }
 
-fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                    int H, int N, int d, float scale, int causal, fa_dtype dtype,
-                    cudaStream_t stream) {
+}  // extern "C"
+
+namespace osfa {
+namespace {
+
+// Checks shared by the tensor-core entry points (bf16/fp16, d in {64, 128}).
+fa_status check_tc_args(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, int B, int H, int N, int d, float scale, int causal,
+                        fa_dtype dtype) {
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID;
-  if (dtype != FA_BF16 && dtype != FA_F32 && dtype != FA_F16) return FA_ERR_UNSUPPORTED;
-  if (dtype != FA_F32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (dtype == FA_F32 && (d < 1 || d > 128)) return FA_ERR_UNSUPPORTED;
-  const long long BH = static_cast<long long>(B) * H;
-  if (BH > INT_MAX) return FA_ERR_INVALID;
-  if (BH == 0 || N == 0) return FA_OK;  // empty problem
+  if (dtype != FA_BF16 && dtype != FA_F16) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > INT_MAX) return FA_ERR_INVALID;
+  if (static_cast<long long>(B) * H == 0 || N == 0) return FA_OK;
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID;
   if (lse != nullptr && !aligned(lse, 4)) return FA_ERR_ALIGN;
-
-  unsigned* status = nullptr;
-  if (dtype == FA_F32) {
-    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(o, 4)) return FA_ERR_ALIGN;
-    if ((static_cast<long long>(N) + 15) / 16 * BH > INT_MAX) return FA_ERR_INVALID;
-    return from_cuda(launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                     static_cast<const float*>(v), static_cast<float*>(o), lse,
-                                     static_cast<int>(BH), N, d, scale, causal, stream));
-  }
-
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return FA_ERR_ALIGN;
-  const long long nqb = (static_cast<long long>(N) + 2 * kBlockM - 1) / (2 * kBlockM);
-  if (nqb * BH > INT_MAX) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+long long nqb_of(int N) { return (static_cast<long long>(N) + 2 * kBlockM - 1) / (2 * kBlockM); }
+
+// Launches the tensor-core kernel; with splits > 1 it writes partials to ws_o / ws_lse
+// (caller-sized) and the combine kernel then writes o and lse.
+fa_status run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, fa_dtype dtype, int splits, float* ws_o,
+                 float* ws_lse, cudaStream_t stream) {
+  const long long BH = static_cast<long long>(B) * H;
+  const long long nqb = nqb_of(N);
+  if (nqb * BH * splits > INT_MAX) return FA_ERR_INVALID;
+  unsigned* status = nullptr;
   cudaError_t e = status_word(&status);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
@@ -169,13 +176,93 @@ fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float*
       std::max(1LL, std::min(BH, (64LL << 20) / std::max(1LL, kv_head_bytes))));
   p.causal = causal;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.splits = splits;
+  p.n_pad = static_cast<int>(nqb * 2 * kBlockM);
+  p.ws_o = ws_o;
+  p.ws_lse = ws_lse;
   if (d == 64)
     e = f16 ? launch_attn_tc<64, true>(tq, tk, tv, to, p, stream)
             : launch_attn_tc<64, false>(tq, tk, tv, to, p, stream);
   else
     e = f16 ? launch_attn_tc<128, true>(tq, tk, tv, to, p, stream)
             : launch_attn_tc<128, false>(tq, tk, tv, to, p, stream);
-  return from_cuda(e);
+  if (e != cudaSuccess || splits == 1) return from_cuda(e);
+  return from_cuda(launch_splitkv_combine(ws_o, ws_lse, o, lse, bh, N, p.n_pad, d, splits, f16,
+                                          stream));
+}
+
+// Workspace of the split-KV forward: fp32 partial O then fp32 partial LSE.
+long long splitkv_ws_bytes(long long BH, int N, int d, int splits) {
+  const long long n_pad = nqb_of(N) * 2 * kBlockM;
+  return static_cast<long long>(splits) * BH * n_pad * (d + 1) * 4;
+}
+
+}  // namespace
+}  // namespace osfa
+
+extern "C" {
+
+fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                    cudaStream_t stream) {
+  if (dtype == FA_F32) {
+    if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID;
+    if (d < 1 || d > 128) return FA_ERR_UNSUPPORTED;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH > INT_MAX) return FA_ERR_INVALID;
+    if (BH == 0 || N == 0) return FA_OK;  // empty problem
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID;
+    if (lse != nullptr && !aligned(lse, 4)) return FA_ERR_ALIGN;
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(o, 4)) return FA_ERR_ALIGN;
+    if ((static_cast<long long>(N) + 15) / 16 * BH > INT_MAX) return FA_ERR_INVALID;
+    return from_cuda(launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                     static_cast<const float*>(v), static_cast<float*>(o), lse,
+                                     static_cast<int>(BH), N, d, scale, causal, stream));
+  }
+  fa_status st = check_tc_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype);
+  if (st != FA_OK || static_cast<long long>(B) * H == 0 || N == 0) return st;
+  return run_tc(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, 1, nullptr, nullptr, stream);
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
+  if (B < 0 || H < 0 || N < 0 || num_splits < 1 || (d != 64 && d != 128)) return 0;
+  return static_cast<size_t>(splitkv_ws_bytes(static_cast<long long>(B) * H, N, d, num_splits));
+}
+
+int fa_fwd_splitkv_default_splits(int B, int H, int N) {
+  if (B <= 0 || H <= 0 || N <= 0) return 1;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long blocks = nqb_of(N) * B * H;
+  const long long kv_tiles = (static_cast<long long>(N) + kBlockN - 1) / kBlockN;
+  // Enough blocks for two waves of the SMs, at least two K/V tiles per split.
+  long long s = (2LL * sms + blocks - 1) / blocks;
+  s = std::min<long long>(s, std::max<long long>(1, kv_tiles / 2));
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(s, kMaxSplits)));
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal, int num_splits,
+                         void* workspace, size_t workspace_bytes, fa_dtype dtype,
+                         cudaStream_t stream) {
+  fa_status st = check_tc_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype);
+  if (st != FA_OK) return st;
+  if (num_splits < 1 || num_splits > kMaxSplits) return FA_ERR_INVALID;
+  if (static_cast<long long>(B) * H == 0 || N == 0) return FA_OK;
+  if (num_splits == 1)
+    return run_tc(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, 1, nullptr, nullptr, stream);
+  const long long BH = static_cast<long long>(B) * H;
+  if (workspace == nullptr) return FA_ERR_INVALID;
+  if (!aligned(workspace, 16)) return FA_ERR_ALIGN;
+  if (static_cast<long long>(workspace_bytes) < splitkv_ws_bytes(BH, N, d, num_splits))
+    return FA_ERR_INVALID;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_lse = ws_o + static_cast<long long>(num_splits) * BH * nqb_of(N) * 2 * kBlockM * d;
+  return run_tc(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, num_splits, ws_o, ws_lse,
+                stream);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

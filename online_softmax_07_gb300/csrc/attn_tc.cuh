@@ -41,8 +41,8 @@ constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 128 bytes
 // 10-11 idle (they complete the third warpgroup so that it can hand its registers to
 // the softmax warpgroups).
 constexpr int kAttnThreads = 384;
-constexpr int kRegsSoftmax = 216;  // per thread, softmax warpgroups
-constexpr int kRegsIssue = 72;     // per thread, MMA / TMA warpgroup (384 x 168 = 256 x 216 + 128 x 72)
+constexpr int kRegsSoftmax = 208;  // per thread, softmax warpgroups
+constexpr int kRegsIssue = 88;     // per thread, MMA / TMA warpgroup (384 x 168 = 256 x 208 + 128 x 88)
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr float kRescaleLog2 = 8.0f;
@@ -72,6 +72,14 @@ struct AttnTcParams {
   int head_group;      // heads scheduled together (1 <= head_group <= BH)
   int causal;
   float scale_log2;    // scale * log2(e)
+  // Split-KV: with splits > 1 block (q block, split) takes the split-th chunk of the
+  // K/V tiles its query block needs and writes fp32 partials (O normalised by its own
+  // l, and LSE) to ws_o [splits, BH, n_pad, d] and ws_lse [splits, BH, n_pad] instead
+  // of O; splits == 1 is the plain forward.
+  int splits;
+  int n_pad;           // nqb * 256
+  float* ws_o;
+  float* ws_lse;
 };
 
 // F16 = false: bf16 Q, K, V, O (and P); F16 = true: fp16.

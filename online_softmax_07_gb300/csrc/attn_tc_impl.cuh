@@ -70,8 +70,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // the group's K and V fit in L2); inside a group, the heavy (late) query blocks of
   // all its heads come first, so that causal tails overlap lighter work.
   int bh, qb;
+  const int split = blockIdx.x % p.splits;
   {
-    const int L = blockIdx.x;
+    const int L = blockIdx.x / p.splits;
     const int per_group = p.head_group * p.nqb;
     const int full = p.BH / p.head_group;
     const int g = L / per_group;
@@ -90,6 +91,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // K/V tiles each Q tile needs: all of them, or up to its diagonal tile (causal).
   const int nb0 = p.causal ? min(nblk, (qb * 2 * kBlockM + kBlockM - 1) / kBlockN + 1) : nblk;
   const int nb1 = p.causal ? min(nblk, (qb * 2 * kBlockM + 2 * kBlockM - 1) / kBlockN + 1) : nblk;
+  // This block's K/V tiles: all of them, or (split-KV) the split-th chunk of the tiles
+  // tile 1 needs; tile 0 takes the part of the chunk below its own limit.  Tiles are
+  // numbered from jlo; n0, n1 count them (n0 may be 0, and with splits > 1 so may n1).
+  const int chunk = (nb1 + p.splits - 1) / p.splits;
+  const int jlo = split * chunk;
+  const int n1 = max(0, min(nb1, jlo + chunk) - jlo);
+  const int n0 = max(0, min(nb0, jlo + chunk) - jlo);
+  const bool split_mode = p.splits > 1;
+  auto part_row = [&](int r) {  // index of query row r of this head in the partials
+    return (static_cast<int64_t>(split) * p.BH + bh) * p.n_pad + r;
+  };
+  if (n1 == 0) {
+    // Nothing to do for this split: the empty partial (LSE = -inf, O = 0) for its rows.
+    for (int rr = threadIdx.x; rr < 2 * kBlockM; rr += blockDim.x) {
+      const int64_t pr = part_row(qb * 2 * kBlockM + rr);
+      p.ws_lse[pr] = -INFINITY;
+      float4* orow = reinterpret_cast<float4*>(p.ws_o + pr * D);
+#pragma unroll
+      for (int c = 0; c < D / 4; ++c) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->q_full), 1);
@@ -138,7 +161,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tma_load_3d(sbase + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0) + b * kBoxBytes, &tm_q, qbar,
                       b * kBoxCols, qb * 2 * kBlockM + t * kBlockM, bh);
       int issued = 0;
-      const int nload = 2 * nb1;  // K_j, V_j for j < nb1 (tile 1 needs the most)
+      const int nload = 2 * n1;  // K_j, V_j for j < n1 (tile 1 needs the most)
       for (int it = 0; it < nload; ++it) {
         const int slot = it % Cfg::kSlots;
         const int phase = (it / Cfg::kSlots) & 1;
@@ -149,7 +172,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t dst = sbase + Cfg::kSmemSlots + slot * Cfg::kTileBytes;
 #pragma unroll
         for (int b = 0; b < Cfg::kBoxes; ++b)
-          tma_load_3d(dst + b * kBoxBytes, tm, full, b * kBoxCols, (it >> 1) * kBlockN, bh);
+          tma_load_3d(dst + b * kBoxBytes, tm, full, b * kBoxCols, (jlo + (it >> 1)) * kBlockN, bh);
         issued = it + 1;
       }
       // Every issued copy must land before the block's shared memory goes away: wait
@@ -205,22 +228,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
-      issue_s(tS0, dQ0, 0);
-      mma_commit_elect(smem_u32(&bars->s_full[0]));
+      if (n0 > 0) {
+        issue_s(tS0, dQ0, 0);
+        mma_commit_elect(smem_u32(&bars->s_full[0]));
+      }
       issue_s(tS1, dQ1, 0);
       mma_commit_elect(smem_u32(&bars->s_full[1]));
       mma_commit_elect(smem_u32(&bars->slot_empty[0]));
     }
-    for (int j = 0; ok && j < nb1; ++j) {
+    for (int j = 0; ok && j < n1; ++j) {
       const int itV = 2 * j + 1, itK = 2 * j + 2;
       if (!(ok = __all_sync(0xffffffffu, wait_full(itV)))) break;
-      if (j < nb0) {
+      if (j < n0) {
         if (!(ok = __all_sync(0xffffffffu,
                               mbar_wait(smem_u32(&bars->p_ready[0]), j & 1, abort, p.status))))
           break;
         tc_fence_after();
         issue_pv(tO0, tS0, itV, j > 0);
-        if (j + 1 < nb0) {
+        if (j + 1 < n0) {
           if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
           tc_fence_after();
           issue_s(tS0, dQ0, itK);
@@ -235,7 +260,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       issue_pv(tO1, tS1, itV, j > 0);
       mma_commit_elect(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
-      if (j + 1 < nb1) {
+      if (j + 1 < n1) {
         if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
         tc_fence_after();
         issue_s(tS1, dQ1, itK);
@@ -265,7 +290,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     float l = 0.f;
     bool ok = true;
 
-    const int nbt = t ? nb1 : nb0;
+    const int nbt = t ? n1 : n0;
     for (int j = 0; j < nbt; ++j) {
       ok = mbar_wait(smem_u32(&bars->s_full[t]), j & 1, abort, p.status);
       ok = __all_sync(0xffffffffu, ok);
@@ -276,7 +301,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float* s = reinterpret_cast<float*>(sr);
 
       // Mask: keys >= N (ragged last tile) and, on the diagonal tile, keys > row.
-      const int key0 = j * kBlockN;
+      const int key0 = (jlo + j) * kBlockN;
       const bool diag = p.causal && (key0 + kBlockN - 1 > r0);
       if (diag || key0 + kBlockN > p.N) {
         int lim = p.N - 1 - key0;
@@ -341,45 +366,71 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready[t]));
     }
 
-    if (ok) {
+    if (ok && nbt > 0) {
       ok = mbar_wait(smem_u32(&bars->o_final[t]), 0, abort, p.status);
       ok = __all_sync(0xffffffffu, ok);
     }
-    // Epilogue: O / l -> bf16 -> swizzled staging in the (now unused) Q_t buffer ->
-    // TMA store; LSE = m + ln l in natural-log units of the scaled score.
-    uint8_t* stage = smem + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0);
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l;
+    if (split_mode) {
+      // Split-KV partial of this row: O / l (fp32) and LSE; an empty range (tile 0
+      // past its diagonal in this chunk) gives LSE = -inf and O = 0.
+      const int64_t pr = part_row(r0 + rr);
+      float4* orow = reinterpret_cast<float4*>(p.ws_o + pr * D);
+      if (ok && nbt > 0) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32_wait(tO + 32 * c, o);
-        uint32_t pk[16];
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32_wait(tO + 32 * c, o);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_elem2<F16>(__uint_as_float(o[2 * i]) * inv_l,
-                                  __uint_as_float(o[2 * i + 1]) * inv_l);
-        // columns 32c .. 32c+31 = box (32c / 64), 16-byte chunks (32c % 64) / 8 .. +3
-        uint8_t* rowp = stage + (c >> 1) * kBoxBytes + rr * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk = ((c & 1) * 4 + q) ^ (rr & 7);
-          *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 8; ++q)
+            orow[8 * c + q] = make_float4(
+                __uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
         }
-      }
-      if (p.lse != nullptr && r0 + rr < p.N)
-        p.lse[static_cast<int64_t>(bh) * p.N + r0 + rr] = m2 * 0.69314718055994531f + logf(l);
-    }
-    fence_proxy_async_smem();
-    named_barrier_sync(1 + t, 128);
-    if (rr == 0 && ok && !*abort && r0 < p.N) {
+        p.ws_lse[pr] = m2 * 0.69314718055994531f + logf(l);
+      } else if (ok) {
 #pragma unroll
-      for (int b = 0; b < Cfg::kBoxes; ++b)
-        tma_store_3d(&tm_o, smem_u32(stage + b * kBoxBytes), b * kBoxCols, r0, bh);
-      bulk_commit_group();
-      bulk_wait_group_0();
+        for (int c = 0; c < D / 4; ++c) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.ws_lse[pr] = -INFINITY;
+      }
+    } else {
+      // Epilogue: O / l -> bf16 -> swizzled staging in the (now unused) Q_t buffer ->
+      // TMA store; LSE = m + ln l in natural-log units of the scaled score.
+      uint8_t* stage = smem + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32_wait(tO + 32 * c, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_elem2<F16>(__uint_as_float(o[2 * i]) * inv_l,
+                                    __uint_as_float(o[2 * i + 1]) * inv_l);
+          // columns 32c .. 32c+31 = box (32c / 64), 16-byte chunks (32c % 64) / 8 .. +3
+          uint8_t* rowp = stage + (c >> 1) * kBoxBytes + rr * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int chunk = ((c & 1) * 4 + q) ^ (rr & 7);
+            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+        if (p.lse != nullptr && r0 + rr < p.N)
+          p.lse[static_cast<int64_t>(bh) * p.N + r0 + rr] = m2 * 0.69314718055994531f + logf(l);
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1 + t, 128);
+      if (rr == 0 && ok && !*abort && r0 < p.N) {
+#pragma unroll
+        for (int b = 0; b < Cfg::kBoxes; ++b)
+          tma_store_3d(&tm_o, smem_u32(stage + b * kBoxBytes), b * kBoxCols, r0, bh);
+        bulk_commit_group();
+        bulk_wait_group_0();
+      }
     }
   }
 
@@ -400,7 +451,7 @@ cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const C
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>(p.nqb) * p.BH;
+  const long long grid = static_cast<long long>(p.nqb) * p.BH * p.splits;
   attn_fwd_tc_kernel<D, F16><<<static_cast<unsigned>(grid), kAttnThreads, Cfg::kSmemBytes, stream>>>(
       tq, tk, tv, to, p);
   return cudaGetLastError();

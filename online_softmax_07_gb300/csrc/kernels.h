@@ -15,6 +15,10 @@ cudaError_t launch_row_state(const float* x, float* m_out, float* l_out, int row
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m_out, float* l_out, int rows,
                                 int len, cudaStream_t stream);
 
+cudaError_t launch_splitkv_combine(const float* ws_o, const float* ws_lse, void* o, float* lse,
+                                   int BH, int N, int n_pad, int d, int splits, bool f16,
+                                   cudaStream_t stream);
+
 cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned long long limit_ns,
                                          cudaStream_t stream);
 

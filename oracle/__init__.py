@@ -30,6 +30,7 @@ from .online import (
     online_state,
     merge_state,
     tiled_attention_forward,
+    combine_partials,
 )
 
 __all__ = [
@@ -41,4 +42,5 @@ __all__ = [
     "online_state",
     "merge_state",
     "tiled_attention_forward",
+    "combine_partials",
 ]

@@ -103,3 +103,25 @@ def tiled_attention_forward(q, k, v, scale: float, causal: bool, block: int):
                 out[b, h, i] = o / l
                 lse[b, h, i] = m + math.log(l)
     return out, lse
+
+
+def combine_partials(o_parts, lse_parts):
+    """Merge attention results computed over disjoint key subsets.
+
+    lihaoran.work FlashAttention note, section "为什么不能平均各块的softmax": results of
+    blocks normalised separately cannot be averaged; they must be brought to the same
+    reference maximum.  With each part s given as its normalised output O_s and its
+    LSE_s = m_s + ln l_s, the common reference is M = max_s LSE_s, the weights are
+    w_s = exp(LSE_s - M), and O = sum_s w_s O_s / sum_s w_s, LSE = M + ln sum_s w_s
+    ("Softmax 数值稳定性与 IO-Aware Attention", §4.1 merge rule applied to (O, l) pairs).
+    A part with LSE_s = -inf (no visible key) has weight 0.
+
+    o_parts: [S, ..., d]; lse_parts: [S, ...].  Returns (O [..., d], LSE [...]).
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    M = lse_parts.max(axis=0)
+    w = np.where(np.isneginf(lse_parts), 0.0, np.exp(lse_parts - M))
+    wsum = w.sum(axis=0)
+    o = (w[..., None] * o_parts).sum(axis=0) / wsum[..., None]
+    return o, M + np.log(wsum)

@@ -109,3 +109,30 @@ def test_binding_has_no_fallback(tmp_path):
             abi.load(str(tmp_path / "libosfa.so"))
     finally:
         abi._lib = saved
+
+
+def test_splitkv_workspace_size(lib):
+    # splits * B * H * ceil(N/256)*256 * (d + 1) * 4
+    assert abi.fa_fwd_splitkv_workspace_bytes(1, 2, 300, 128, 3) == 3 * 2 * 512 * 129 * 4
+    assert abi.fa_fwd_splitkv_workspace_bytes(2, 1, 256, 64, 1) == 1 * 2 * 256 * 65 * 4
+    assert abi.fa_fwd_splitkv_workspace_bytes(1, 1, 100, 96, 2) == 0      # unsupported d
+    assert abi.fa_fwd_splitkv_workspace_bytes(1, 1, 100, 64, 0) == 0      # no splits
+
+
+@pytest.mark.parametrize("splits,ws,ws_bytes,expect", [
+    (0, FAKE, 1 << 30, abi.FA_ERR_INVALID),
+    (65, FAKE, 1 << 30, abi.FA_ERR_INVALID),
+    (2, None, 1 << 30, abi.FA_ERR_INVALID),
+    (2, FAKE, 100, abi.FA_ERR_INVALID),        # workspace too small
+    (2, FAKE + 8, 1 << 30, abi.FA_ERR_ALIGN),
+])
+def test_splitkv_argument_checks(lib, splits, ws, ws_bytes, expect):
+    st = lib.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 1000, 128, 0.1, 1, splits, ws,
+                            ws_bytes, abi.FA_BF16, None)
+    assert st == expect, abi.status_str(st)
+
+
+def test_splitkv_rejects_f32(lib):
+    st = lib.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 100, 64, 0.1, 0, 2, FAKE, 1 << 30,
+                            abi.FA_F32, None)
+    assert st == abi.FA_ERR_UNSUPPORTED

@@ -417,3 +417,52 @@ def test_softmax_rows_properties():
     # all-equal rows are uniform, length-1 rows are 1
     assert np.all(oracle.softmax_rows(np.full((2, 8), -7.0)) == 0.125)
     assert np.all(oracle.softmax_rows(np.array([[1e4], [-3.0]])) == 1.0)
+
+
+# ----------------------------------------------------------------------------
+# Merging results over key subsets (split-KV combine)
+# ----------------------------------------------------------------------------
+
+def _attention_on_keys(q, k, v, scale, causal, key_lo, key_hi):
+    """Attention restricted to keys [key_lo, key_hi), by enumeration (plain exponentials
+    and math.fsum, as in the brute-force pin).  Rows with no visible key in the range
+    give LSE = -inf and O = 0 (the empty part)."""
+    B, H, N, d = q.shape
+    o = np.zeros((B, H, N, d))
+    lse = np.full((B, H, N), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                keys = [j for j in range(key_lo, key_hi) if (not causal or j <= i)]
+                if not keys:
+                    continue
+                w = [math.exp(scale * float(q[b, h, i] @ k[b, h, j])) for j in keys]
+                z = math.fsum(w)
+                lse[b, h, i] = math.log(z)
+                for t in range(d):
+                    o[b, h, i, t] = math.fsum(wj * v[b, h, j, t] for wj, j in zip(w, keys)) / z
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_combine_of_key_splits_equals_whole(causal):
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((1, 2, 11, 4)) * 2
+    k = rng.standard_normal((1, 2, 11, 4))
+    v = rng.standard_normal((1, 2, 11, 4))
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, 0.6, causal)
+    for cuts in ([0, 11], [0, 4, 11], [0, 1, 2, 7, 11], [0, 3, 6, 9, 11]):
+        parts = [_attention_on_keys(q, k, v, 0.6, causal, a, b) for a, b in zip(cuts, cuts[1:])]
+        o, lse = oracle.combine_partials([p[0] for p in parts], [p[1] for p in parts])
+        assert np.allclose(o, o_ref, rtol=1e-12, atol=1e-13)
+        assert np.allclose(lse, lse_ref, rtol=1e-12, atol=1e-13)
+
+
+def test_combine_rejects_averaging():
+    """The note's point: averaging per-block softmax results is wrong; the combine is
+    not the mean of the parts (unless their denominators agree)."""
+    o_parts = np.array([[1.0], [3.0]])
+    lse_parts = np.array([0.0, np.log(3.0)])
+    o, lse = oracle.combine_partials(o_parts[:, None, :], lse_parts[:, None])
+    assert abs(o[0, 0] - (1 * 1 + 3 * 3) / 4) < 1e-15 and abs(o[0, 0] - 2.0) > 0.4
+    assert abs(lse[0] - np.log(4.0)) < 1e-15
