@@ -46,7 +46,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,  /* head dimension or dtype outside what is built          */
   FA_ERR_ALIGN = 3,        /* a pointer without the alignment the call needs         */
   FA_ERR_CUDA = 4,         /* the CUDA runtime or driver returned an error           */
-  FA_ERR_TIMEOUT = 5       /* a kernel gave up a bounded wait (fa_last_device_error) */
+  FA_ERR_TIMEOUT = 5,      /* a kernel gave up a bounded wait (fa_last_device_error) */
+  FA_ERR_TOO_LARGE = 6     /* fa_fwd_splitkv_static: the partials exceed its scratch  */
 } fa_status;
 
 typedef enum {
@@ -115,6 +116,27 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits
 /* A split count for fa_fwd_splitkv on the current device: enough thread blocks for two
  * waves of its SMs, at least two K/V tiles per split, at most 64 (1 when no split pays). */
 int fa_fwd_splitkv_default_splits(int B, int H, int N);
+
+/*
+ * Split-KV forward for callers that cannot allocate device memory (memory pools or arenas
+ * that own all device memory, plugin interfaces without an allocator, paths where a
+ * cudaMalloc would synchronise the device).  The pages have no counterpart: this is a
+ * deployment convenience around fa_fwd_splitkv, same arguments and results minus the
+ * workspace.
+ *
+ * The partials go to a scratch array in the library's static device memory: 64 MiB,
+ * reserved on every GPU that loads the library until it is unloaded.  Problems needing
+ * more (fa_fwd_splitkv_workspace_bytes > 64 MiB) return FA_ERR_TOO_LARGE and launch
+ * nothing.  The call allocates nothing.  The first call on a device looks up the array's
+ * device address (once per device, with that device current); make that first call before
+ * any stream capture.  All calls share the array and it keeps the last call's partials;
+ * nothing needs clearing (every partial read is written by the same call), but calls that
+ * overlap on the GPU (other streams or host threads) race on it.
+ */
+fa_status fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o,
+                                float* lse, int B, int H, int N, int d, float scale,
+                                int causal, int num_splits, fa_dtype dtype,
+                                cudaStream_t stream);
 
 /*
  * Row online-softmax state.

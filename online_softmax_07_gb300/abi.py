@@ -15,7 +15,8 @@ from __future__ import annotations
 import ctypes
 import os
 
-FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
+(FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN, FA_ERR_CUDA, FA_ERR_TIMEOUT,
+ FA_ERR_TOO_LARGE) = range(7)
 FA_BF16, FA_F32, FA_F16 = 0, 1, 2
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libosfa.so")
@@ -30,6 +31,9 @@ _SIGNATURES = {
                        + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                           ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 5),
+    "fa_fwd_splitkv_static": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p]
+                              + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_splitkv_default_splits": (ctypes.c_int, [ctypes.c_int] * 3),
     "online_softmax_rows": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2
                             + [ctypes.c_void_p]),
@@ -118,6 +122,15 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, works
                                  float(scale), int(causal), int(num_splits), _ptr(workspace),
                                  int(workspace_bytes), int(dtype), _stream(stream)),
            "fa_fwd_splitkv")
+
+
+def fa_fwd_splitkv_static(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, dtype,
+                          stream=None) -> None:
+    """fa_fwd_splitkv with the partials in the library's static scratch: no workspace
+    argument and no allocation (for callers that cannot allocate device memory)."""
+    _check(load().fa_fwd_splitkv_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                        float(scale), int(causal), int(num_splits), int(dtype),
+                                        _stream(stream)), "fa_fwd_splitkv_static")
 
 
 def fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits) -> int:

@@ -117,6 +117,7 @@ const char* fa_status_str(fa_status s) {
     case FA_ERR_ALIGN: return "misaligned pointer";
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    case FA_ERR_TOO_LARGE: return "problem needs more than the library's 64 MiB static scratch";
   }
   return "unknown status";
 }
