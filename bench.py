@@ -484,6 +484,125 @@ def our_arm(args, rank, world, local_rank):
     return out
 
 
+# ------------------------------------------------------------------ per-workload suite
+def suite(args):
+    """One JSON line per workload (not the bench contract line): the five configurations,
+    fp16 inputs, split-KV against the plain kernel on a small-B*H long sequence, and the
+    normalised row softmax.  CUDA events around `reps` back-to-back launches after 5
+    warm-up launches; inputs larger than L2 except the tiny fp32 case."""
+    import torch
+
+    from online_softmax_07_gb300 import abi, synth
+    from online_softmax_07_gb300.build import build_library
+
+    build_library()
+    abi.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    def timed(fn, reps):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if abi.fa_last_device_error() != abi.FA_OK:
+            raise RuntimeError("device-side error")
+        return e0.elapsed_time(e1) / reps
+
+    def attn_line(name, q, k, v, causal, dtype, splits=None, label=None):
+        B, H, N, d = q.shape
+        tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
+        code = {"bf16": abi.FA_BF16, "f16": abi.FA_F16, "f32": abi.FA_F32}[dtype]
+        dq, dk, dv = (torch.from_numpy(t).to(dev, tdt) for t in (q, k, v))
+        o = torch.empty_like(dq)
+        lse = torch.empty((B, H, N), device=dev)
+        scale = 1.0 / math.sqrt(d)
+        if splits is None:
+            fn = lambda: abi.fa_fwd_dt(dq, dk, dv, o, lse, B, H, N, d, scale, int(causal), code,
+                                       stream)
+        else:
+            nbytes = abi.fa_fwd_splitkv_workspace_bytes(B, H, N, d, splits)
+            ws = torch.empty(max(1, nbytes // 4), device=dev)
+            fn = lambda: abi.fa_fwd_splitkv(dq, dk, dv, o, lse, B, H, N, d, scale, int(causal),
+                                            splits, ws, nbytes, code, stream)
+        ms = timed(fn, 20 if N * N * B * H > 1e9 else 200)
+        tf = attn_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
+        line = {"workload": label or name, "dtype": dtype, "ms": ms, "TFLOP/s": tf,
+                "pct_of_bf16_peak": 100 * tf / peaks["bf16_tflops"]}
+        line.update(attn_errors(q, k, v, o, lse, scale, causal))
+        if splits is not None:
+            line["splits"] = splits
+        print(json.dumps(line), flush=True)
+
+    def attn_errors(q, k, v, o, lse, scale, causal):
+        """Errors against the fp64 oracle: every row for small problems, else 32 seeded
+        rows (plus the first and last) of each of up to 4 heads."""
+        import oracle
+        B, H, N, d = q.shape
+        errs, lerrs = [], []
+        heads = [(b, h) for b in range(B) for h in range(H)][:4]
+        for (b, h) in heads:
+            rows = np.arange(N) if N * N <= 1 << 24 else np.unique(np.concatenate(
+                [[0, N - 1], np.random.Generator(np.random.PCG64(7 + h)).choice(N, 32, False)]))
+            o_ref, lse_ref = oracle.attention_forward(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                                      v[b:b + 1, h:h + 1], scale, causal, rows=rows)
+            idx = torch.from_numpy(rows).to(dev)
+            errs.append(np.abs(o[b, h].index_select(0, idx).float().cpu().numpy() - o_ref[0, 0]))
+            lerrs.append(np.abs(lse[b, h].index_select(0, idx).cpu().numpy() - lse_ref[0, 0]))
+        e = np.concatenate([x.ravel() for x in errs])
+        le = np.concatenate([x.ravel() for x in lerrs])
+        return {"o_max_abs_err": float(e.max()), "o_mean_abs_err": float(e.mean()),
+                "lse_max_abs_err": float(le.max()), "rows_checked": int(le.size)}
+
+    for name in ("attn_f32_b1h1n128d64", "attn_bf16_b4h16n4096d64",
+                 "attn_bf16_b2h16n8192d128_causal", "attn_bf16_b2h16n8191d128_causal",
+                 "attn_bf16_b1h8n32768d128_causal_qstd4"):
+        w = synth.WORKLOADS[name]
+        q, k, v = synth.workload_attention_inputs(name)
+        attn_line(name, q, k, v, w["causal"], w["dtype"])
+        if name == "attn_bf16_b2h16n8192d128_causal":
+            qh, kh, vh = (synth.round_to_f16(t) for t in (q, k, v))
+            attn_line(name, qh, kh, vh, True, "f16", label=name.replace("bf16", "f16"))
+    # split-KV where the grid is small: B=1 H=2 N=32768 d=128 causal (256 query blocks)
+    q, k, v = synth.attention_inputs(1, 2, 32768, 128, seed=96000)
+    label = "attn_bf16_b1h2n32768d128_causal"
+    attn_line(label, q, k, v, True, "bf16", label=label + " (no split)")
+    s_def = abi.fa_fwd_splitkv_default_splits(1, 2, 32768)
+    attn_line(label, q, k, v, True, "bf16", splits=s_def, label=label + " (split-KV)")
+    # and where the grid is smaller still: B=1 H=1 N=16384 (64 query blocks)
+    q, k, v = synth.attention_inputs(1, 1, 16384, 128, seed=96100)
+    label = "attn_bf16_b1h1n16384d128_causal"
+    attn_line(label, q, k, v, True, "bf16", label=label + " (no split)")
+    s_def = abi.fa_fwd_splitkv_default_splits(1, 1, 16384)
+    attn_line(label, q, k, v, True, "bf16", splits=s_def, label=label + " (split-KV)")
+    # row state and normalised softmax on the 4096 x 32768 array
+    x = torch.from_numpy(synth.workload_row_inputs()[0]).to(dev)
+    rows, length = x.shape
+    m = torch.empty(rows, device=dev)
+    l = torch.empty(rows, device=dev)
+    y = torch.empty_like(x)
+    ms = timed(lambda: abi.online_softmax_rows(x, m, l, rows, length, stream), 100)
+    gbs = row_bytes(rows, length) / (ms * 1e-3) / 1e9
+    import oracle
+    xs = x[:256].cpu().numpy()
+    m_ref, l_ref = oracle.row_state(xs)
+    l_rel = float(np.max(np.abs(l[:256].cpu().numpy() - l_ref) / l_ref))
+    m_exact = bool(np.all(m[:256].cpu().numpy() == m_ref))
+    print(json.dumps({"workload": "rows_4096x32768 state", "ms": ms, "GB/s": gbs,
+                      "frac_of_hbm": gbs / peaks["hbm_gbs"], "l_max_rel_err_256_rows": l_rel,
+                      "m_exact_256_rows": m_exact}), flush=True)
+    ms = timed(lambda: abi.online_softmax_forward(x, y, m, l, rows, length, stream), 100)
+    gbs = (2 * rows * length * 4 + rows * 8) / (ms * 1e-3) / 1e9
+    print(json.dumps({"workload": "rows_4096x32768 softmax output", "ms": ms, "GB/s": gbs,
+                      "frac_of_hbm": gbs / peaks["hbm_gbs"]}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -492,11 +611,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--suite", action="store_true",
+                    help="one line per workload instead of the bench line (1 GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
     world, rank, local_rank = rank_env()
+    if args.suite:
+        suite(args)
+        return
     if world > 1 and args.impl == "ours":
         import torch
         import torch.distributed as dist

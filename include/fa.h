@@ -153,8 +153,9 @@ fa_status online_softmax_rows(const float* x, float* m_out, float* l_out,
 /*
  * Row softmax: y[r, t] = exp(x[r, t] - m_r) / l_r with m_r, l_r as in
  * online_softmax_rows ("Softmax 数值稳定性与 IO-Aware Attention", §三: the third pass,
- * here fused with the (m, l) reduction).  Rows of up to 32768 floats are read from
- * device memory once; longer rows twice.
+ * here fused with the (m, l) reduction).  One block per row (a warp per row up to 1024
+ * floats) reads the row for (m, l), then again for y; the second read normally hits L2,
+ * so device memory sees one read of x and one write of y.
  *
  * x:     device fp32 [rows, len], contiguous; any 4-byte alignment.
  * y:     device fp32 [rows, len], written; may alias x (in place); any 4-byte alignment.

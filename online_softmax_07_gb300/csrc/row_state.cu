@@ -166,26 +166,17 @@ __global__ void __launch_bounds__(256)
 
 // ---------------------------------------------------------------------------------------
 // Normalised row softmax y = exp(x - m) / l ("Softmax 数值稳定性与 IO-Aware Attention", §三,
-// pass three), with the state (m, l) from the same reduction as above.  A row of up to
-// kCacheVec * 4 * kBlockThreads floats stays in registers between the state and the
-// output, so x is read once and y written once; longer rows are streamed twice.
+// pass three), with the state (m, l) from the same reduction as above.
 
-constexpr int kCacheVec = 16;  // float4 per thread kept in registers (32768 floats per row)
+// Long rows, low registers: pass one streams the row for (m, l); pass two reads it
+// again (from L2: the row was just read and only ~rows-in-flight x len x 4 bytes are
+// live) and writes y.  Several blocks per SM keep enough loads in flight.
+constexpr int kL2Threads = 256;
 
-__device__ __forceinline__ State block_merge(State st, State* warp_states) {
-  st = warp_merge(st);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();  // warp_states may still be read from a previous merge
-  if (lane == 0) warp_states[warp] = st;
-  __syncthreads();
-  st = (lane < kBlockThreads / 32) ? warp_states[lane] : State{-INFINITY, 0.f};
-  return warp_merge(st);  // every warp computes the block result
-}
-
-__global__ void __launch_bounds__(kBlockThreads)
-    softmax_rows_block_kernel(const float* x, float* y,  // y may alias x
-                              float* __restrict__ m_out, float* __restrict__ l_out, int len) {
-  __shared__ State warp_states[kBlockThreads / 32];
+__global__ void __launch_bounds__(kL2Threads)
+    softmax_rows_l2_kernel(const float* x, float* y, float* __restrict__ m_out,
+                           float* __restrict__ l_out, int len) {  // y may alias x
+  __shared__ State warp_states[kL2Threads / 32];
   const int64_t row = blockIdx.x;
   const float* xr = x + row * static_cast<int64_t>(len);
   float* yr = y + row * static_cast<int64_t>(len);
@@ -196,9 +187,7 @@ __global__ void __launch_bounds__(kBlockThreads)
   const int tail0 = head + 4 * nvec;
   const int extra = head + (len - tail0);
   const float4* xv = reinterpret_cast<const float4*>(xr + head);
-  // y can take 16-byte stores only where it has x's alignment
   const bool y_vec = ((reinterpret_cast<uintptr_t>(yr) ^ reinterpret_cast<uintptr_t>(xr)) & 15) == 0;
-  const bool cached = nvec <= kCacheVec * kBlockThreads;
 
   State st = {-INFINITY, 0.f};
   float e0 = 0.f;
@@ -207,48 +196,31 @@ __global__ void __launch_bounds__(kBlockThreads)
     float e[1] = {e0};
     fold<1>(st, e, 1);
   }
-  float4 c[kCacheVec];
-  if (cached) {
+  for (int base = 0; base < nvec; base += kUnroll * kL2Threads) {
+    float v[4 * kUnroll];
+    int cnt = 0;
 #pragma unroll
-    for (int u = 0; u < kCacheVec; ++u) {
-      const int i = u * kBlockThreads + tid;
-      c[u] = (i < nvec) ? __ldcs(xv + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u0 = 0; u0 < kCacheVec; u0 += 8) {
-      float v[32];
-      int cnt = 0;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        v[4 * u] = c[u0 + u].x;
-        v[4 * u + 1] = c[u0 + u].y;
-        v[4 * u + 2] = c[u0 + u].z;
-        v[4 * u + 3] = c[u0 + u].w;
-        if ((u0 + u) * kBlockThreads + tid < nvec) cnt = 4 * (u + 1);
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * kL2Threads + tid;
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < nvec) {
+        f = xv[i];
+        cnt = 4 * (u + 1);
       }
-      fold<32>(st, v, cnt);
+      v[4 * u] = f.x;
+      v[4 * u + 1] = f.y;
+      v[4 * u + 2] = f.z;
+      v[4 * u + 3] = f.w;
     }
-  } else {
-    for (int base = 0; base < nvec; base += kUnroll * kBlockThreads) {
-      float v[4 * kUnroll];
-      int cnt = 0;
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = base + u * kBlockThreads + tid;
-        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < nvec) {
-          f = xv[i];
-          cnt = 4 * (u + 1);
-        }
-        v[4 * u] = f.x;
-        v[4 * u + 1] = f.y;
-        v[4 * u + 2] = f.z;
-        v[4 * u + 3] = f.w;
-      }
-      fold<4 * kUnroll>(st, v, cnt);
-    }
+    fold<4 * kUnroll>(st, v, cnt);
   }
-  st = block_merge(st, warp_states);
+  // block merge
+  st = warp_merge(st);
+  const int warp = tid >> 5, lane = tid & 31;
+  if (lane == 0) warp_states[warp] = st;
+  __syncthreads();
+  st = (lane < kL2Threads / 32) ? warp_states[lane] : State{-INFINITY, 0.f};
+  st = warp_merge(st);
   if (tid == 0) {
     if (m_out != nullptr) m_out[row] = st.m;
     if (l_out != nullptr) l_out[row] = st.l;
@@ -257,25 +229,27 @@ __global__ void __launch_bounds__(kBlockThreads)
   auto out = [&](float xv_) { return exp_diff(xv_, m) * inv_l; };
   if (tid < extra) yr[tid < head ? tid : tail0 + (tid - head)] = out(e0);
   float* yv = yr + head;
-  auto store4 = [&](int i, float4 f) {
-    const float4 r = make_float4(out(f.x), out(f.y), out(f.z), out(f.w));
-    if (y_vec) {
-      __stcs(reinterpret_cast<float4*>(yv) + i, r);
-    } else {
-      yv[4 * i] = r.x;
-      yv[4 * i + 1] = r.y;
-      yv[4 * i + 2] = r.z;
-      yv[4 * i + 3] = r.w;
-    }
-  };
-  if (cached) {
+  for (int base = 0; base < nvec; base += kUnroll * kL2Threads) {
+    float4 f[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kCacheVec; ++u) {
-      const int i = u * kBlockThreads + tid;
-      if (i < nvec) store4(i, c[u]);
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * kL2Threads + tid;
+      if (i < nvec) f[u] = __ldcs(xv + i);
     }
-  } else {
-    for (int i = tid; i < nvec; i += kBlockThreads) store4(i, __ldcs(xv + i));
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * kL2Threads + tid;
+      if (i >= nvec) continue;
+      const float4 r = make_float4(out(f[u].x), out(f[u].y), out(f[u].z), out(f[u].w));
+      if (y_vec) {
+        __stcs(reinterpret_cast<float4*>(yv) + i, r);
+      } else {
+        yv[4 * i] = r.x;
+        yv[4 * i + 1] = r.y;
+        yv[4 * i + 2] = r.z;
+        yv[4 * i + 3] = r.w;
+      }
+    }
   }
 }
 
@@ -335,7 +309,7 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m_out, float* l
     const unsigned grid = static_cast<unsigned>((static_cast<long long>(rows) + 7) / 8);
     softmax_rows_warp_kernel<<<grid, 256, 0, stream>>>(x, y, m_out, l_out, rows, len);
   } else {
-    softmax_rows_block_kernel<<<static_cast<unsigned>(rows), kBlockThreads, 0, stream>>>(
+    softmax_rows_l2_kernel<<<static_cast<unsigned>(rows), kL2Threads, 0, stream>>>(
         x, y, m_out, l_out, len);
   }
   return cudaGetLastError();
