@@ -18,6 +18,10 @@ blocking, fusion or reordering beyond what the definition states:
                             scale follows "为什么 Flash Attention 算出来的结果和标准
                             注意力有微小差异？有损但值得", section "它没省计算，只是
                             把矩阵拆开再算").
+* ``attention_backward`` -- dQ, dK, dV of that function for an upstream dO, by the
+                            chain rule (``oracle.backward``; §7.2 of the first page
+                            named above says the backward recomputes the scores from
+                            kept statistics, §九 9.1 asks for gradient checks).
 
 The online forms in ``oracle.online`` restate the pages' recurrences and are used
 only to cross-check the three-pass forms above.  Parity status of every function
@@ -25,6 +29,7 @@ is pinned by ``tests/test_oracle_pins.py``; no function here is unpinned.
 """
 
 from .reference import attention_forward, row_state, softmax_rows, visible_mask
+from .backward import attention_backward, attention_backward_rows
 from .online import (
     online_weighted_sum,
     online_state,
@@ -35,6 +40,8 @@ from .online import (
 
 __all__ = [
     "attention_forward",
+    "attention_backward",
+    "attention_backward_rows",
     "row_state",
     "softmax_rows",
     "visible_mask",
