@@ -1,7 +1,7 @@
 /*
  * fa.h -- C ABI of the GB300 (sm_103a) online-softmax attention library.
  *
- * Two operations, both from the pages on online softmax and FlashAttention:
+ * The operations, all from the pages on online softmax and FlashAttention:
  *
  *  - fa_fwd / fa_fwd_dt: exact dense attention forward O = softmax(scale * Q K^T) V,
  *    computed tile by tile with the online-softmax state (row max m, denominator l,
@@ -11,6 +11,9 @@
  *    the per-Q-tile loop; the 1/sqrt(d) factor as in "为什么 Flash Attention 算出来的
  *    结果和标准注意力有微小差异？有损但值得", section "罪魁祸首是 online softmax 里那步
  *    rescale".)
+ *
+ *  - fa_bwd: the gradients of that forward, recomputing the scores from the kept LSE
+ *    (same page, §7.2).
  *
  *  - online_softmax_rows: the per-row softmax state (m, l), m = max_t x_t,
  *    l = sum_t exp(x_t - m), reduced thread -> warp shuffle -> shared memory -> first
@@ -164,6 +167,36 @@ fa_status online_softmax_rows(const float* x, float* m_out, float* l_out,
  */
 fa_status online_softmax_forward(const float* x, float* y, float* m_out, float* l_out,
                                  int rows, int len, cudaStream_t stream);
+
+/*
+ * Attention backward (bf16 or fp16, d = 64 or 128): the gradients dQ, dK, dV of the
+ * forward above for an upstream gradient dO.  "Softmax 数值稳定性与 IO-Aware Attention"
+ * §7.2: only per-row statistics of the forward are kept (here LSE) and the scores are
+ * recomputed tile by tile, never stored.  With P = exp(scale Q K^T - LSE):
+ *   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  D_i = sum_c dO_ic O_ic,
+ *   dQ = scale dS K,  dK = scale dS^T Q
+ * (the chain rule through the softmax; the pages print no gradient formula).
+ *
+ *   q, k, v, o, dout    [B, H, N, d], dtype; o and lse as fa_fwd wrote them for q, k, v
+ *                       (same scale and causal)
+ *   lse                 [B, H, N] fp32, required
+ *   dq, dk, dv          [B, H, N, d], dtype, written (fp32 accumulation inside)
+ *   workspace           caller-owned device scratch of at least
+ *                       fa_bwd_workspace_bytes(B, H, N) bytes (fp32 LSE*log2(e) and D
+ *                       per query row); its contents are overwritten
+ * Alignment: every pointer but lse 16 bytes, lse 4.  B*H*N == 0 is a no-op (FA_OK).
+ * Every output element is written exactly once by one block (no atomics), so results
+ * are deterministic.  Errors: FA_ERR_INVALID (null pointer, lse missing, negative size,
+ * scale not finite and > 0, causal not 0/1, workspace too small), FA_ERR_UNSUPPORTED
+ * (d or dtype), FA_ERR_ALIGN, FA_ERR_CUDA.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, void* workspace, size_t workspace_bytes,
+                 fa_dtype dtype, cudaStream_t stream);
+
+/* Workspace fa_bwd needs, in bytes: 8 * B * H * ceil(N / 128) * 128 (0 for negative sizes). */
+size_t fa_bwd_workspace_bytes(int B, int H, int N);
 
 /* Static, never-NULL description of a status code. */
 const char* fa_status_str(fa_status status);

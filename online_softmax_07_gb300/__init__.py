@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) online-softmax attention forward and row softmax state.
+"""GB300 (sm_103a) online-softmax attention forward and backward, and row softmax state.
 
 The compute lives in ``lib/libosfa.so`` (hand-written CUDA, C ABI in include/fa.h);
 this package only binds it.  ``abi`` exposes the C calls by their C names; the two
@@ -12,11 +12,12 @@ from __future__ import annotations
 import math
 
 from . import abi
-from .abi import (FAError, fa_fwd, fa_fwd_dt, online_softmax_rows, online_softmax_forward,
-                  fa_last_device_error)
+from .abi import (FAError, fa_fwd, fa_fwd_dt, fa_bwd, online_softmax_rows,
+                  online_softmax_forward, fa_last_device_error)
 
-__all__ = ["attention_forward", "row_state", "softmax", "abi", "FAError", "fa_fwd", "fa_fwd_dt",
-           "online_softmax_rows", "online_softmax_forward", "fa_last_device_error"]
+__all__ = ["attention_forward", "attention_backward", "row_state", "softmax", "abi", "FAError",
+           "fa_fwd", "fa_fwd_dt", "fa_bwd", "online_softmax_rows", "online_softmax_forward",
+           "fa_last_device_error"]
 
 
 def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=True,
@@ -72,6 +73,40 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
         lse_h.copy_(lse, non_blocking=True)
     torch.cuda.current_stream().synchronize()
     return o_h, lse_h
+
+
+def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, stream=None):
+    """(dQ, dK, dV) of attention_forward for the upstream gradient ``dout``.
+
+    q, k, v, o, dout: CUDA [B, H, N, d] tensors, all bf16 or all fp16, d in {64, 128};
+    o and lse (fp32 [B, H, N]) as attention_forward returned them for the same scale and
+    causal flag.  The outputs and the library's workspace are allocated here with torch;
+    the computation runs in the library's kernels (fa_bwd).
+    """
+    import torch
+
+    if stream is not None:
+        with torch.cuda.stream(stream):
+            return attention_backward(q, k, v, o, lse, dout, scale, causal, None)
+    ts = (q, k, v, o, dout)
+    if q.dim() != 4 or any(t.shape != q.shape for t in ts):
+        raise ValueError("q, k, v, o, dout must be [B, H, N, d] of one shape")
+    if any(t.dtype != q.dtype for t in ts) or q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v, o, dout must all be bf16 or all fp16")
+    if not all(t.is_cuda for t in ts) or not lse.is_cuda:
+        raise ValueError("attention_backward takes CUDA tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    q, k, v, o, dout = (t.contiguous() for t in ts)
+    lse = lse.contiguous()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = abi.fa_bwd_workspace_bytes(B, H, N)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    dtype = abi.FA_BF16 if q.dtype == torch.bfloat16 else abi.FA_F16
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, int(bool(causal)), ws, ws_bytes,
+           dtype)
+    return dq, dk, dv
 
 
 def row_state(x, stream=None):

@@ -35,6 +35,10 @@ _SIGNATURES = {
                               + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                                       ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_splitkv_default_splits": (ctypes.c_int, [ctypes.c_int] * 3),
+    "fa_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 4
+               + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                  ctypes.c_void_p]),
+    "fa_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 3),
     "online_softmax_rows": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2
                             + [ctypes.c_void_p]),
     "online_softmax_forward": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 2
@@ -139,6 +143,18 @@ def fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits) -> int:
 
 def fa_fwd_splitkv_default_splits(B, H, N) -> int:
     return int(load().fa_fwd_splitkv_default_splits(B, H, N))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+           workspace_bytes, dtype, stream=None) -> None:
+    _check(load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(causal),
+                         _ptr(workspace), int(workspace_bytes), int(dtype), _stream(stream)),
+           "fa_bwd")
+
+
+def fa_bwd_workspace_bytes(B, H, N) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, H, N))
 
 
 def online_softmax_rows(x, m_out, l_out, rows, length, stream=None) -> None:

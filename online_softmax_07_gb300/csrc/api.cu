@@ -13,6 +13,7 @@
 
 #include "attn_tc.cuh"
 #include "fa.h"
+#include "host_util.h"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -26,6 +27,8 @@ constexpr int kMaxSplits = 64;
 std::mutex g_mutex;
 unsigned* g_status_ptr[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+}  // namespace
 
 // Address of this device's status word (looked up once per device).
 cudaError_t status_word(unsigned** out) {
@@ -81,6 +84,8 @@ bool encode_bhnd(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const vo
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+namespace {
 
 __global__ void wait_timeout_selftest_kernel(unsigned* status, unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t bar;

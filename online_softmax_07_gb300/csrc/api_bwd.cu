@@ -1,0 +1,98 @@
+// api_bwd.cu -- the backward entry points declared in include/fa.h: argument checks,
+// TMA descriptors and dispatch to the three backward launches (attn_bwd_impl.cuh).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "attn_bwd.cuh"
+#include "fa.h"
+#include "host_util.h"
+
+namespace osfa {
+namespace {
+
+long long bwd_n_pad(int N) { return (static_cast<long long>(N) + kBlockM - 1) / kBlockM * kBlockM; }
+
+// fp32 LSE * log2(e) and fp32 D per (head, padded query row).
+long long bwd_ws_bytes(long long BH, int N) { return 2 * BH * bwd_n_pad(N) * 4; }
+
+}  // namespace
+}  // namespace osfa
+
+using namespace osfa;
+
+extern "C" {
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N) {
+  if (B < 0 || H < 0 || N < 0) return 0;
+  return static_cast<size_t>(bwd_ws_bytes(static_cast<long long>(B) * H, N));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, void* workspace, size_t workspace_bytes, fa_dtype dtype,
+                 cudaStream_t stream) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID;
+  if (dtype != FA_BF16 && dtype != FA_F16) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > INT_MAX) return FA_ERR_INVALID;
+  if (BH == 0 || N == 0) return FA_OK;
+  const void* ptrs16[] = {q, k, v, o, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs16)
+    if (ptr == nullptr) return FA_ERR_INVALID;
+  if (lse == nullptr) return FA_ERR_INVALID;
+  for (const void* ptr : ptrs16)
+    if (!aligned(ptr, 16)) return FA_ERR_ALIGN;
+  if (!aligned(lse, 4)) return FA_ERR_ALIGN;
+  if (workspace_bytes < static_cast<size_t>(bwd_ws_bytes(BH, N))) return FA_ERR_INVALID;
+  const long long nblk = bwd_n_pad(N) / kBlockM;
+  if (nblk * BH > INT_MAX) return FA_ERR_INVALID;
+
+  unsigned* status = nullptr;
+  cudaError_t e = status_word(&status);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if ((e = encode_fn(&enc)) != cudaSuccess) return FA_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo;
+  const int bh = static_cast<int>(BH);
+  const bool f16 = dtype == FA_F16;
+  if (!encode_bhnd(enc, &tq, q, bh, N, d, f16) || !encode_bhnd(enc, &tk, k, bh, N, d, f16) ||
+      !encode_bhnd(enc, &tv, v, bh, N, d, f16) || !encode_bhnd(enc, &tdo, dout, bh, N, d, f16))
+    return FA_ERR_CUDA;
+  AttnBwdParams p;
+  p.lse2 = nullptr;  // set by the launcher from the workspace
+  p.dd = nullptr;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.status = status;
+  p.N = N;
+  p.BH = bh;
+  p.nblk = static_cast<int>(nblk);
+  p.n_pad = static_cast<int>(nblk * kBlockM);
+  // Heads scheduled together: as many as keep the tiles each pass streams (two [N, d]
+  // tensors per head) within about 64 MB of L2.
+  const long long stream_head_bytes = 2LL * N * d * 2;
+  p.head_group = static_cast<int>(
+      std::max(1LL, std::min(BH, (64LL << 20) / std::max(1LL, stream_head_bytes))));
+  p.causal = causal;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  float* ws = static_cast<float*>(workspace);
+  if (d == 64)
+    e = f16 ? launch_attn_bwd<64, true>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream)
+            : launch_attn_bwd<64, false>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream);
+  else
+    e = f16 ? launch_attn_bwd<128, true>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream)
+            : launch_attn_bwd<128, false>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream);
+  return from_cuda(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+// attn_bwd.cuh -- backward of the tcgen05 attention forward (sm_103a).
+//
+// "Softmax 数值稳定性与 IO-Aware Attention：从在线归一化到 FlashAttention" §7.2: the
+// backward keeps only per-row statistics of the forward (here LSE) and recomputes the
+// scores tile by tile instead of reading a stored probability matrix.  With
+// P = exp(scale * Q K^T - LSE) recomputed per tile, the gradients of the exact
+// attention function are
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D) with D_i = sum_c dO_ic O_ic,
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+//
+// GB300 mapping, three launches:
+//  * bwd_prep: D_i and LSE_i * log2(e) for every query row into the caller's workspace
+//    (rows past N get D = 0 and +inf, so that padded queries drop out of every sum);
+//  * bwd_dkdv: one CTA per 128-key tile j keeps K_j, V_j in shared memory and dV_j, dK_j
+//    in tensor memory while Q_i, dO_i stream through by TMA; per query tile it computes
+//    S^T = K_j Q_i^T and dP^T = V_j dO_i^T (tcgen05, keys on TMEM lanes), the element-
+//    wise warps turn them into P^T and dS^T (16-bit, stored back over S^T and dP^T in
+//    TMEM), and dV += P^T dO_i, dK += dS^T Q_i take P^T and dS^T straight from TMEM;
+//  * bwd_dq: one CTA per 128-query tile i keeps Q_i, dO_i and accumulates
+//    dQ += dS K_j the same way while K_j, V_j stream.
+// Splitting dQ into its own pass recomputes S and dP once more (7 tile products per
+// tile pair instead of 5) but needs no atomic accumulation: every output element is
+// written once, by one CTA, so the result is deterministic.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "attn_tc.cuh"
+
+namespace osfa {
+
+// Warps 0-7: element-wise work, warp w on TMEM lanes 32 (w % 4) .. +31 and on the
+// column half w / 4 of each tile; 8: MMA issue; 9: TMA loads; 10-11 idle.
+constexpr int kBwdThreads = 384;
+constexpr int kBwdWarpMma = 8;
+constexpr int kBwdWarpLoad = 9;
+
+template <int D>
+struct AttnBwdCfg {
+  static_assert(D == 64 || D == 128, "head dimension");
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D, 16-bit
+  static constexpr int kStages = (D == 128) ? 2 : 4;      // streamed tile pairs in flight
+  // A stage holds two streamed tiles and, for the key-outer pass, 128 LSE*log2(e)
+  // and 128 D values of the query tile (1 KB).
+  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kSmemFixed0 = 0;           // resident tile 0 (K_j or Q_i)
+  static constexpr int kSmemFixed1 = kTileBytes;  // resident tile 1 (V_j or dO_i)
+  static constexpr int kSmemStages = 2 * kTileBytes;
+  static constexpr int kSmemBars = kSmemStages + kStages * kStageBytes;
+  static constexpr int kSmemBytes = kSmemBars + 512 + 1024;  // + barriers + alignment slack
+  // TMEM columns: S (or S^T), dP (or dP^T), then one or two fp32 accumulators.
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+struct AttnBwdParams {
+  const float* lse2;   // [BH, n_pad]: LSE * log2(e), +inf for rows >= N
+  const float* dd;     // [BH, n_pad]: D = rowsum(dO * O), 0 for rows >= N
+  void* dq;            // [BH, N, d] outputs, 16-bit
+  void* dk;
+  void* dv;
+  unsigned* status;    // device status word
+  int N;
+  int BH;
+  int nblk;            // ceil(N / 128)
+  int n_pad;           // nblk * 128
+  int head_group;      // heads scheduled together (1 <= head_group <= BH)
+  int causal;
+  float scale;
+  float scale_log2;    // scale * log2(e)
+};
+
+template <int D, bool F16>
+cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const void* o, const void* dout,
+                            const float* lse, float* ws, const AttnBwdParams& p,
+                            cudaStream_t stream);
+
+}  // namespace osfa

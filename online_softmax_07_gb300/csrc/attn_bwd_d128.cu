@@ -1,0 +1,13 @@
+// Head dimension 128 instances of the tcgen05 attention backward.
+#include "attn_bwd_impl.cuh"
+
+namespace osfa {
+template cudaError_t launch_attn_bwd<128, false>(const CUtensorMap&, const CUtensorMap&,
+                                                 const CUtensorMap&, const CUtensorMap&,
+                                                 const void*, const void*, const float*, float*,
+                                                 const AttnBwdParams&, cudaStream_t);
+template cudaError_t launch_attn_bwd<128, true>(const CUtensorMap&, const CUtensorMap&,
+                                                const CUtensorMap&, const CUtensorMap&,
+                                                const void*, const void*, const float*, float*,
+                                                const AttnBwdParams&, cudaStream_t);
+}  // namespace osfa

@@ -1,0 +1,13 @@
+// Head dimension 64 instances of the tcgen05 attention backward.
+#include "attn_bwd_impl.cuh"
+
+namespace osfa {
+template cudaError_t launch_attn_bwd<64, false>(const CUtensorMap&, const CUtensorMap&,
+                                                 const CUtensorMap&, const CUtensorMap&,
+                                                 const void*, const void*, const float*, float*,
+                                                 const AttnBwdParams&, cudaStream_t);
+template cudaError_t launch_attn_bwd<64, true>(const CUtensorMap&, const CUtensorMap&,
+                                                const CUtensorMap&, const CUtensorMap&,
+                                                const void*, const void*, const float*, float*,
+                                                const AttnBwdParams&, cudaStream_t);
+}  // namespace osfa

@@ -1,0 +1,597 @@
+// attn_bwd_impl.cuh -- kernel bodies of the tcgen05 attention backward (see attn_bwd.cuh).
+// Included by one translation unit per head dimension.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "attn_bwd.cuh"
+#include "attn_tc_impl.cuh"  // shared-memory / instruction descriptors, 16-bit packing
+
+namespace osfa {
+
+struct AttnBwdBarriers {
+  uint64_t fixed_full;   // TMA -> all: the two resident tiles are in shared memory
+  uint64_t sp_full;      // MMA -> element-wise: S and dP of the current tile pair in TMEM
+  uint64_t ds_ready;     // element-wise -> MMA: the 16-bit operands stored back in TMEM
+  uint64_t acc_final;    // MMA -> element-wise: the last accumulation finished
+  uint64_t mma_drain;    // MMA warp: all of its MMAs finished (before TMEM is freed)
+  uint64_t stage_full[4];
+  uint64_t stage_empty[4];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// 1-D bulk copy global -> shared memory, completion counted on `bar` (both addresses
+// 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Two 16-bit values of the kernel's element type (lower address in bits 0..15) to fp32.
+template <bool F16>
+__device__ __forceinline__ void unpack_elem2(uint32_t v, float& lo, float& hi) {
+  if constexpr (F16) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(v));
+  } else {
+    lo = __uint_as_float(v << 16);
+    hi = __uint_as_float(v & 0xFFFF0000u);
+  }
+}
+
+// Tile order shared by both passes: heads in groups of p.head_group (their streamed
+// tiles fit in L2 together); inside a group tile-major, heavy tiles first.  For the
+// key-outer pass the heavy causal tiles are the low ones (they meet the most query
+// tiles), for the query-outer pass the high ones.
+__device__ __forceinline__ void bwd_work(const AttnBwdParams& p, bool low_first, int* bh,
+                                         int* tile) {
+  const int L = blockIdx.x;
+  const int per_group = p.head_group * p.nblk;
+  const int full = p.BH / p.head_group;
+  const int g = L / per_group;
+  int r, hg, base;
+  if (g < full) {
+    r = L - g * per_group;
+    hg = p.head_group;
+    base = g * p.head_group;
+  } else {
+    r = L - full * per_group;
+    hg = p.BH - full * p.head_group;
+    base = full * p.head_group;
+  }
+  const int t = r / hg;
+  *tile = low_first ? t : p.nblk - 1 - t;
+  *bh = base + r % hg;
+}
+
+// D_i = sum_c dO_ic O_ic and LSE_i * log2(e), one warp per query row; rows N .. n_pad-1
+// of each head get D = 0 and +inf.
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __restrict__ o,
+                                                            const uint16_t* __restrict__ dout,
+                                                            const float* __restrict__ lse,
+                                                            float* __restrict__ lse2,
+                                                            float* __restrict__ dd, int BH, int N,
+                                                            int n_pad) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<long long>(BH) * n_pad) return;
+  const long long bh = row / n_pad;
+  const int q = static_cast<int>(row - bh * n_pad);
+  if (q >= N) {
+    if (lane == 0) {
+      dd[row] = 0.f;
+      lse2[row] = INFINITY;
+    }
+    return;
+  }
+  const long long off = (bh * N + q) * D;
+  constexpr int kPer = D / 32;  // 16-bit elements per lane: 2 or 4
+  float acc = 0.f;
+  if constexpr (kPer == 4) {
+    const uint2 a = *reinterpret_cast<const uint2*>(o + off + lane * 4);
+    const uint2 b = *reinterpret_cast<const uint2*>(dout + off + lane * 4);
+    const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float a0, a1, b0, b1;
+      unpack_elem2<F16>(av[i], a0, a1);
+      unpack_elem2<F16>(bv[i], b0, b1);
+      acc = fmaf(a0, b0, acc);
+      acc = fmaf(a1, b1, acc);
+    }
+  } else {
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + off + lane * 2);
+    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + off + lane * 2);
+    float a0, a1, b0, b1;
+    unpack_elem2<F16>(a, a0, a1);
+    unpack_elem2<F16>(b, b0, b1);
+    acc = fmaf(a0, b0, acc);
+    acc = fmaf(a1, b1, acc);
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) {
+    dd[row] = acc;
+    lse2[row] = lse[bh * N + q] * 1.4426950408889634f;
+  }
+}
+
+// Writes 32 fp32 accumulator columns (times `mul`) of one row as 16-bit values.
+template <bool F16>
+__device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t* a, float mul) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    pk[i] = pack_elem2<F16>(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+
+// ------------------------------------------------------------------------------------
+// Key-outer pass: dK_j, dV_j.
+// ------------------------------------------------------------------------------------
+template <int D, bool F16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do, const AttnBwdParams p) {
+  using Cfg = AttnBwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  AttnBwdBarriers* bars = reinterpret_cast<AttnBwdBarriers*>(smem + Cfg::kSmemBars);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int bh, j;
+  bwd_work(p, true, &bh, &j);
+  const int i0 = p.causal ? j : 0;  // query tiles i < j see none of these keys
+  const int nq = p.nblk - i0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->fixed_full), 1);
+    mbar_init(smem_u32(&bars->sp_full), 1);
+    mbar_init(smem_u32(&bars->ds_ready), 8);  // one arrival per element-wise warp
+    mbar_init(smem_u32(&bars->acc_final), 1);
+    mbar_init(smem_u32(&bars->mma_drain), 1);
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(smem_u32(&bars->stage_full[s]), 1);
+      mbar_init(smem_u32(&bars->stage_empty[s]), 1);
+    }
+    bars->abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == kBwdWarpMma) {
+    tmem_alloc(smem_u32(&bars->tmem_base), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+  auto stage_addr = [&](int s) { return sbase + Cfg::kSmemStages + s * Cfg::kStageBytes; };
+
+  if (warp >= 10) {
+    // idle
+  } else if (warp == kBwdWarpLoad) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      const uint32_t fbar = smem_u32(&bars->fixed_full);
+      mbar_arrive_expect_tx(fbar, 2 * Cfg::kTileBytes);
+#pragma unroll
+      for (int b = 0; b < Cfg::kBoxes; ++b) {
+        tma_load_3d(sbase + Cfg::kSmemFixed0 + b * kBoxBytes, &tm_k, fbar, b * kBoxCols, j * kBlockM, bh);
+        tma_load_3d(sbase + Cfg::kSmemFixed1 + b * kBoxBytes, &tm_v, fbar, b * kBoxCols, j * kBlockM, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < nq; ++it) {
+        const int s = it % Cfg::kStages;
+        if (!mbar_wait(smem_u32(&bars->stage_empty[s]), ((it / Cfg::kStages) & 1) ^ 1, abort,
+                       p.status))
+          break;
+        const uint32_t full = smem_u32(&bars->stage_full[s]);
+        const int i = i0 + it;
+        const uint32_t dst = stage_addr(s);
+        mbar_arrive_expect_tx(full, 2 * Cfg::kTileBytes + 1024);
+#pragma unroll
+        for (int b = 0; b < Cfg::kBoxes; ++b) {
+          tma_load_3d(dst + b * kBoxBytes, &tm_q, full, b * kBoxCols, i * kBlockM, bh);
+          tma_load_3d(dst + Cfg::kTileBytes + b * kBoxBytes, &tm_do, full, b * kBoxCols, i * kBlockM, bh);
+        }
+        const long long srow = static_cast<long long>(bh) * p.n_pad + i * kBlockM;
+        bulk_load_1d(dst + 2 * Cfg::kTileBytes, p.lse2 + srow, 512, full);
+        bulk_load_1d(dst + 2 * Cfg::kTileBytes + 512, p.dd + srow, 512, full);
+        issued = it + 1;
+      }
+      // Every issued copy must land before the block's shared memory goes away.
+      int no_abort = 0;
+      mbar_wait(fbar, 0, &no_abort, p.status);
+      for (int it = max(0, issued - Cfg::kStages); it < issued; ++it)
+        mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]), (it / Cfg::kStages) & 1,
+                  &no_abort, p.status);
+    }
+  } else if (warp == kBwdWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdescS = idesc_f16kind(kBlockM, kBlockM, false, F16);
+    constexpr uint32_t kIdescAcc = idesc_f16kind(kBlockM, D, true, F16);
+    const uint64_t dK = desc_sw128(sbase + Cfg::kSmemFixed0, 16, 1024);   // A of S^T
+    const uint64_t dV = desc_sw128(sbase + Cfg::kSmemFixed1, 16, 1024);   // A of dP^T
+    const uint32_t tS = tbase + Cfg::kColS, tDP = tbase + Cfg::kColDP;
+    const uint32_t tDV = tbase + Cfg::kColAcc0, tDK = tbase + Cfg::kColAcc1;
+    auto wait_bar = [&](uint64_t* bar, int parity) {
+      const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, abort, p.status));
+      if (r) tc_fence_after();
+      return r;
+    };
+    bool ok = wait_bar(&bars->fixed_full, 0);
+    for (int it = 0; ok && it < nq; ++it) {
+      const int s = it % Cfg::kStages;
+      if (!(ok = wait_bar(&bars->stage_full[s], (it / Cfg::kStages) & 1))) break;
+      const uint32_t st = stage_addr(s);
+      const uint64_t dQk = desc_sw128(st, 16, 1024);                          // B of S^T
+      const uint64_t dDOk = desc_sw128(st + Cfg::kTileBytes, 16, 1024);       // B of dP^T
+      const uint64_t dDOmn = desc_sw128(st + Cfg::kTileBytes, kBoxBytes, 1024);  // B of dV
+      const uint64_t dQmn = desc_sw128(st, kBoxBytes, 1024);                   // B of dK
+      // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: keys on lanes, queries on columns.
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_elect(tS, dK + off16, dQk + off16, kIdescS, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_elect(tDP, dV + off16, dDOk + off16, kIdescS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(smem_u32(&bars->sp_full));
+      if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
+      // dV += P^T dO_i and dK += dS^T Q_i: A (16 queries = 8 packed columns per step)
+      // from TMEM, where column half h of the tile was packed into columns 64h .. 64h+31.
+#pragma unroll
+      for (int kk = 0; kk < kBlockM / 16; ++kk) {
+        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+        mma_bf16_ts_elect(tDV, tS + acol, dDOmn + ((kk * 2048) >> 4), kIdescAcc,
+                          (it > 0 || kk > 0) ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < kBlockM / 16; ++kk) {
+        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+        mma_bf16_ts_elect(tDK, tDP + acol, dQmn + ((kk * 2048) >> 4), kIdescAcc,
+                          (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit_elect(smem_u32(&bars->stage_empty[s]));
+    }
+    if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
+    mma_commit_elect(smem_u32(&bars->mma_drain));
+    int no_abort = 0;
+    mbar_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ element-wise warps
+    const int h = warp >> 2;         // column half of the tile
+    const int wq = warp & 3;         // TMEM lane quarter
+    const int r = wq * 32 + lane;    // key within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off + Cfg::kColS, tDP = tbase + lane_off + Cfg::kColDP;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < nq; ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sp_full), it & 1, abort, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const int i = i0 + it;
+      // The statistics came in by TMA with the stage; wait on the stage's own barrier
+      // (complete already: the MMAs that consumed the stage are done) to see them.
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]),
+                                (it / Cfg::kStages) & 1, abort, p.status));
+      if (!ok) break;
+      const float* lse2s = reinterpret_cast<const float*>(
+          smem + Cfg::kSmemStages + (it % Cfg::kStages) * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
+      const float* dds = lse2s + 128;
+      const bool diag = p.causal && i == j;  // query q sees key r iff r <= q
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * h + 32 * ch;    // first query (column) of this chunk
+        uint32_t s[32], dp[32];
+        tmem_ld32_wait(tS + c0, s);
+        tmem_ld32_wait(tDP + c0, dp);
+        uint32_t pk[16], pd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float pr[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = c0 + c + e;
+            float pv = ex2_approx(fmaf(__uint_as_float(s[c + e]), sl2, -lse2s[q]));
+            if (diag && q < r) pv = 0.f;
+            pr[e] = pv;
+            dsv[e] = pv * (__uint_as_float(dp[c + e]) - dds[q]);
+          }
+          pk[c >> 1] = pack_elem2<F16>(pr[0], pr[1]);
+          pd[c >> 1] = pack_elem2<F16>(dsv[0], dsv[1]);
+        }
+        tmem_st16(tS + 64 * h + 16 * ch, pk);
+        tmem_st16(tDP + 64 * h + 16 * ch, pd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
+    }
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
+    }
+    const int kg = j * kBlockM + r;
+    if (ok) {
+      tc_fence_after();
+      uint8_t* dv_row = static_cast<uint8_t*>(p.dv) + (static_cast<long long>(bh) * p.N + kg) * D * 2;
+      uint8_t* dk_row = static_cast<uint8_t*>(p.dk) + (static_cast<long long>(bh) * p.N + kg) * D * 2;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = h * (D / 2) + 32 * c;
+        uint32_t a[32];
+        tmem_ld32_wait(tbase + lane_off + Cfg::kColAcc0 + col, a);
+        if (kg < p.N) store_row32<F16>(dv_row + col * 2, a, 1.0f);
+        tmem_ld32_wait(tbase + lane_off + Cfg::kColAcc1 + col, a);
+        if (kg < p.N) store_row32<F16>(dk_row + col * 2, a, p.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tbase, Cfg::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Query-outer pass: dQ_i.
+// ------------------------------------------------------------------------------------
+template <int D, bool F16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do, const AttnBwdParams p) {
+  using Cfg = AttnBwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  AttnBwdBarriers* bars = reinterpret_cast<AttnBwdBarriers*>(smem + Cfg::kSmemBars);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int bh, i;
+  bwd_work(p, false, &bh, &i);
+  const int nk = p.causal ? i + 1 : p.nblk;  // key tiles j > i are all above the diagonal
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->fixed_full), 1);
+    mbar_init(smem_u32(&bars->sp_full), 1);
+    mbar_init(smem_u32(&bars->ds_ready), 8);
+    mbar_init(smem_u32(&bars->acc_final), 1);
+    mbar_init(smem_u32(&bars->mma_drain), 1);
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(smem_u32(&bars->stage_full[s]), 1);
+      mbar_init(smem_u32(&bars->stage_empty[s]), 1);
+    }
+    bars->abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == kBwdWarpMma) {
+    tmem_alloc(smem_u32(&bars->tmem_base), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+  auto stage_addr = [&](int s) { return sbase + Cfg::kSmemStages + s * Cfg::kStageBytes; };
+
+  if (warp >= 10) {
+    // idle
+  } else if (warp == kBwdWarpLoad) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      const uint32_t fbar = smem_u32(&bars->fixed_full);
+      mbar_arrive_expect_tx(fbar, 2 * Cfg::kTileBytes);
+#pragma unroll
+      for (int b = 0; b < Cfg::kBoxes; ++b) {
+        tma_load_3d(sbase + Cfg::kSmemFixed0 + b * kBoxBytes, &tm_q, fbar, b * kBoxCols, i * kBlockM, bh);
+        tma_load_3d(sbase + Cfg::kSmemFixed1 + b * kBoxBytes, &tm_do, fbar, b * kBoxCols, i * kBlockM, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < nk; ++it) {
+        const int s = it % Cfg::kStages;
+        if (!mbar_wait(smem_u32(&bars->stage_empty[s]), ((it / Cfg::kStages) & 1) ^ 1, abort,
+                       p.status))
+          break;
+        const uint32_t full = smem_u32(&bars->stage_full[s]);
+        const uint32_t dst = stage_addr(s);
+        mbar_arrive_expect_tx(full, 2 * Cfg::kTileBytes);
+#pragma unroll
+        for (int b = 0; b < Cfg::kBoxes; ++b) {
+          tma_load_3d(dst + b * kBoxBytes, &tm_k, full, b * kBoxCols, it * kBlockM, bh);
+          tma_load_3d(dst + Cfg::kTileBytes + b * kBoxBytes, &tm_v, full, b * kBoxCols, it * kBlockM, bh);
+        }
+        issued = it + 1;
+      }
+      int no_abort = 0;
+      mbar_wait(fbar, 0, &no_abort, p.status);
+      for (int it = max(0, issued - Cfg::kStages); it < issued; ++it)
+        mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]), (it / Cfg::kStages) & 1,
+                  &no_abort, p.status);
+    }
+  } else if (warp == kBwdWarpMma) {
+    constexpr uint32_t kIdescS = idesc_f16kind(kBlockM, kBlockM, false, F16);
+    constexpr uint32_t kIdescAcc = idesc_f16kind(kBlockM, D, true, F16);
+    const uint64_t dQ = desc_sw128(sbase + Cfg::kSmemFixed0, 16, 1024);   // A of S
+    const uint64_t dDO = desc_sw128(sbase + Cfg::kSmemFixed1, 16, 1024);  // A of dP
+    const uint32_t tS = tbase + Cfg::kColS, tDP = tbase + Cfg::kColDP, tDQ = tbase + Cfg::kColAcc0;
+    auto wait_bar = [&](uint64_t* bar, int parity) {
+      const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, abort, p.status));
+      if (r) tc_fence_after();
+      return r;
+    };
+    bool ok = wait_bar(&bars->fixed_full, 0);
+    for (int it = 0; ok && it < nk; ++it) {
+      const int s = it % Cfg::kStages;
+      if (!(ok = wait_bar(&bars->stage_full[s], (it / Cfg::kStages) & 1))) break;
+      const uint32_t st = stage_addr(s);
+      const uint64_t dKk = desc_sw128(st, 16, 1024);                        // B of S
+      const uint64_t dVk = desc_sw128(st + Cfg::kTileBytes, 16, 1024);      // B of dP
+      const uint64_t dKmn = desc_sw128(st, kBoxBytes, 1024);                // B of dQ
+      // S = Q_i K_j^T and dP = dO_i V_j^T: queries on lanes, keys on columns.
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_elect(tS, dQ + off16, dKk + off16, kIdescS, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_elect(tDP, dDO + off16, dVk + off16, kIdescS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(smem_u32(&bars->sp_full));
+      if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
+      // dQ += dS K_j: dS (16 keys = 8 packed columns per step) from TMEM.
+#pragma unroll
+      for (int kk = 0; kk < kBlockM / 16; ++kk) {
+        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+        mma_bf16_ts_elect(tDQ, tS + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
+                          (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit_elect(smem_u32(&bars->stage_empty[s]));
+    }
+    if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
+    mma_commit_elect(smem_u32(&bars->mma_drain));
+    int no_abort = 0;
+    mbar_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
+    __syncwarp();
+  } else {
+    const int h = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // query within the tile
+    const int qg = i * kBlockM + r;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off + Cfg::kColS, tDP = tbase + lane_off + Cfg::kColDP;
+    const float sl2 = p.scale_log2;
+    const long long srow = static_cast<long long>(bh) * p.n_pad + qg;
+    const float lse2 = p.lse2[srow];
+    const float dd = p.dd[srow];
+    bool ok = true;
+    for (int it = 0; it < nk; ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sp_full), it & 1, abort, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const int key0 = it * kBlockM;
+      // Keys past N, and (causal) keys after the query, drop out.
+      const bool need_mask = (p.causal && it == i) || key0 + kBlockM > p.N;
+      int lim = p.N - 1 - key0;
+      if (p.causal) lim = min(lim, qg - key0);
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * h + 32 * ch;   // first key (column) of this chunk
+        uint32_t s[32], dp[32];
+        tmem_ld32_wait(tS + c0, s);
+        tmem_ld32_wait(tDP + c0, dp);
+        uint32_t pd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float pv = ex2_approx(fmaf(__uint_as_float(s[c + e]), sl2, -lse2));
+            if (need_mask && c0 + c + e > lim) pv = 0.f;
+            dsv[e] = pv * (__uint_as_float(dp[c + e]) - dd);
+          }
+          pd[c >> 1] = pack_elem2<F16>(dsv[0], dsv[1]);
+        }
+        tmem_st16(tS + 64 * h + 16 * ch, pd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
+    }
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
+    }
+    if (ok) {
+      tc_fence_after();
+      uint8_t* dq_row = static_cast<uint8_t*>(p.dq) + (static_cast<long long>(bh) * p.N + qg) * D * 2;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = h * (D / 2) + 32 * c;
+        uint32_t a[32];
+        tmem_ld32_wait(tbase + lane_off + Cfg::kColAcc0 + col, a);
+        if (qg < p.N) store_row32<F16>(dq_row + col * 2, a, p.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tbase, Cfg::kTmemCols);
+  }
+}
+
+template <int D, bool F16>
+cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const void* o, const void* dout,
+                            const float* lse, float* ws, const AttnBwdParams& p0,
+                            cudaStream_t stream) {
+  using Cfg = AttnBwdCfg<D>;
+  static_assert(sizeof(AttnBwdBarriers) <= 512, "barrier block");
+  AttnBwdParams p = p0;
+  float* lse2 = ws;
+  float* dd = ws + static_cast<long long>(p.BH) * p.n_pad;
+  p.lse2 = lse2;
+  p.dd = dd;
+  const long long rows = static_cast<long long>(p.BH) * p.n_pad;
+  attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dd, p.BH,
+      p.N, p.n_pad);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, F16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, F16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes)) !=
+      cudaSuccess)
+    return e;
+  const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.BH) * p.nblk);
+  attn_bwd_dkdv_kernel<D, F16><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace osfa

@@ -1,0 +1,25 @@
+// host_util.h -- host helpers of the C ABI shared by its translation units (api.cu,
+// api_bwd.cu).  Internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+
+#include "fa.h"
+
+namespace osfa {
+
+// Device address of the status word the kernels report bounded-wait time-outs in.
+cudaError_t status_word(unsigned** out);
+// cuTensorMapEncodeTiled from the driver (looked up once).
+cudaError_t encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out);
+// TMA map of a [BH, N, d] bf16/fp16 tensor, 128-row x 64-column boxes, 128-byte swizzle.
+bool encode_bhnd(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base,
+                 int BH, int N, int d, bool f16);
+bool aligned(const void* p, uintptr_t a);
+fa_status from_cuda(cudaError_t e);
+
+}  // namespace osfa

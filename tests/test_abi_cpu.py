@@ -136,3 +136,36 @@ def test_splitkv_rejects_f32(lib):
     st = lib.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 100, 64, 0.1, 0, 2, FAKE, 1 << 30,
                             abi.FA_F32, None)
     assert st == abi.FA_ERR_UNSUPPORTED
+
+
+def test_bwd_workspace_size(lib):
+    # 2 fp32 per (head, query row), rows padded to a multiple of 128
+    assert abi.fa_bwd_workspace_bytes(2, 3, 300) == 2 * 6 * 384 * 4
+    assert abi.fa_bwd_workspace_bytes(1, 1, 128) == 2 * 128 * 4
+    assert abi.fa_bwd_workspace_bytes(0, 4, 100) == 0
+    assert abi.fa_bwd_workspace_bytes(-1, 4, 100) == 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(B=0), abi.FA_OK),                       # empty problems launch nothing
+    (dict(N=0, q=None), abi.FA_OK),
+    (dict(d=96), abi.FA_ERR_UNSUPPORTED),
+    (dict(dtype=abi.FA_F32), abi.FA_ERR_UNSUPPORTED),
+    (dict(scale=0.0), abi.FA_ERR_INVALID),
+    (dict(causal=3), abi.FA_ERR_INVALID),
+    (dict(lse=None), abi.FA_ERR_INVALID),         # the backward needs the forward's LSE
+    (dict(dout=None), abi.FA_ERR_INVALID),
+    (dict(ws=None), abi.FA_ERR_INVALID),
+    (dict(ws_bytes=100), abi.FA_ERR_INVALID),     # workspace too small
+    (dict(dq=FAKE + 8), abi.FA_ERR_ALIGN),
+    (dict(ws=FAKE + 4), abi.FA_ERR_ALIGN),
+    (dict(lse=FAKE + 2), abi.FA_ERR_ALIGN),
+])
+def test_fa_bwd_argument_checks(lib, args, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1,
+             H=2, N=300, d=128, scale=0.1, causal=1, ws=FAKE, ws_bytes=1 << 20, dtype=abi.FA_BF16)
+    a.update(args)
+    st = lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dout"], a["dq"], a["dk"], a["dv"],
+                    a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], a["ws"], a["ws_bytes"],
+                    a["dtype"], None)
+    assert st == expect, abi.status_str(st)

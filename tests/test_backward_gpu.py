@@ -1,0 +1,130 @@
+"""Parity of the attention backward (fa_bwd, through the C ABI) with the fp64 oracle.
+
+O and LSE come from the library's own forward (fa_fwd_dt), as in use; the oracle's
+gradients are the exact ones of the inputs as rounded to the kernel's dtype.
+
+Tolerance, from the arithmetic: the backward rounds three things to the 16-bit type,
+each with relative error <= 2^-9 (bf16): P before dV = P^T dO, dS before dK and dQ,
+and the outputs.  Over many terms the errors are independent, so the relative RMS
+error of each gradient tensor should be a few times 2^-9 / sqrt(1) ~ 2e-3..4e-3;
+the gate is 1e-2 on ||g - g_ref|| / ||g_ref|| and 2e-2 * max|g_ref| on the largest
+element error (the forward's 2e-2 on O, taken relative to the gradient's scale).
+fp16 rounds with 2^-11 and gets the same gates.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from online_softmax_07_gb300 import abi, synth
+
+from gpu_helpers import sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+REL_RMS = 1e-2
+MAX_REL = 2e-2
+
+
+def _run_bwd(q, k, v, do, scale, causal, dtype="bf16"):
+    """fa_fwd_dt then fa_bwd through the C ABI; returns numpy fp32 dq, dk, dv."""
+    import torch
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    code = {"bf16": abi.FA_BF16, "f16": abi.FA_F16}[dtype]
+    B, H, N, d = q.shape
+    tq, tk, tv, tdo = (to_device(x, tdt) for x in (q, k, v, do))
+    o = torch.empty_like(tq)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    abi.fa_fwd_dt(tq, tk, tv, o, lse, B, H, N, d, scale, int(causal), code)
+    ws_bytes = abi.fa_bwd_workspace_bytes(B, H, N)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    outs = [torch.full_like(tq, float("nan")) for _ in range(3)]
+    abi.fa_bwd(tq, tk, tv, o, lse, tdo, *outs, B, H, N, d, scale, int(causal), ws, ws_bytes, code)
+    assert abi.fa_last_device_error() == abi.FA_OK
+    return [t.float().cpu().numpy() for t in outs]
+
+
+def _inputs(B, H, N, d, seed, dtype="bf16"):
+    q, k, v = synth.attention_inputs(B, H, N, d, seed, dtype=dtype)
+    do = synth.attention_inputs(B, H, N, d, seed + 7, dtype=dtype)[0]
+    return q, k, v, do
+
+
+def _check(name, got, ref):
+    got = got.astype(np.float64)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    err = got - ref
+    scale = np.abs(ref).max()
+    rel_rms = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-30)
+    assert rel_rms <= REL_RMS, f"{name}: relative RMS error {rel_rms:.3e}"
+    assert np.abs(err).max() <= MAX_REL * scale, (
+        f"{name}: max error {np.abs(err).max():.3e} vs max |ref| {scale:.3e}")
+    return rel_rms
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [
+    (1, 2, 300, 64, True),
+    (1, 2, 300, 128, False),
+    (2, 1, 129, 128, True),
+    (1, 1, 64, 64, False),
+    (1, 2, 256, 128, True),
+    (1, 1, 383, 64, False),
+])
+def test_backward_all_rows(B, H, N, d, causal):
+    q, k, v, do = _inputs(B, H, N, d, seed=900 + N + d)
+    scale = 1.0 / np.sqrt(d)
+    dq, dk, dv = _run_bwd(q, k, v, do, scale, causal)
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, scale, causal)
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        _check(name, g, r)
+
+
+def test_backward_single_key():
+    """N = 1: P = 1, so dV = dO and dQ = dK = 0 (up to rounding of LSE)."""
+    q, k, v, do = _inputs(1, 2, 1, 64, seed=950)
+    dq, dk, dv = _run_bwd(q, k, v, do, 0.125, False)
+    assert np.abs(dv - do).max() <= 2 ** -8 * np.abs(do).max()
+    assert np.abs(dq).max() < 1e-3 and np.abs(dk).max() < 1e-3
+
+
+def test_backward_f16():
+    q, k, v, do = _inputs(1, 2, 200, 128, seed=960, dtype="f16")
+    dq, dk, dv = _run_bwd(q, k, v, do, 1.0 / np.sqrt(128), True, dtype="f16")
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, 1.0 / np.sqrt(128), True)
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        _check(name, g, r)
+
+
+def test_backward_deterministic():
+    """Every output element is written once by one block: two runs agree bitwise."""
+    q, k, v, do = _inputs(1, 4, 1000, 128, seed=970)
+    a = _run_bwd(q, k, v, do, 0.09, True)
+    b = _run_bwd(q, k, v, do, 0.09, True)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,n_sample", [
+    (2, 16, 8192, 128, True, 48),
+    (2, 16, 8191, 128, True, 32),
+    (4, 16, 4096, 64, False, 48),
+])
+def test_backward_workload_sampled(B, H, N, d, causal, n_sample):
+    """Workload sizes: sampled query rows (dQ) and key rows (dK, dV) of two heads against
+    the oracle, plus the sum invariants over every head."""
+    q, k, v, do = _inputs(B, H, N, d, seed=980 + d)
+    scale = 1.0 / np.sqrt(d)
+    dq, dk, dv = _run_bwd(q, k, v, do, scale, causal)
+    rows = sample_rows(N, n_sample, seed=N + d)
+    for bh in ((0, 0), (B - 1, H - 1)):
+        rq, rk, rv = oracle.attention_backward_rows(q, k, v, do, scale, causal, bh, rows, rows)
+        b, h = bh
+        _check("dQ", dq[b, h, rows], rq)
+        _check("dK", dk[b, h, rows], rk)
+        _check("dV", dv[b, h, rows], rv)
+    # Rows of P sum to one: sum_j dV_j = sum_i dO_i; rows of dS sum to zero: sum_j dK_j = 0.
+    dv_sum = dv.astype(np.float64).sum(axis=2)
+    do_sum = do.astype(np.float64).sum(axis=2)
+    assert np.abs(dv_sum - do_sum).max() <= 1e-2 * np.abs(dv).sum(axis=2).max()
+    dk_sum = np.abs(dk.astype(np.float64).sum(axis=2))
+    assert (dk_sum <= 1e-2 * np.abs(dk.astype(np.float64)).sum(axis=2)).all()
