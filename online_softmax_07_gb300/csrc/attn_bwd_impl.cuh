@@ -11,8 +11,10 @@ namespace osfa {
 
 struct AttnBwdBarriers {
   uint64_t fixed_full;   // TMA -> all: the two resident tiles are in shared memory
-  uint64_t sp_full;      // MMA -> element-wise: S and dP of the current tile pair in TMEM
-  uint64_t ds_ready;     // element-wise -> MMA: the 16-bit operands stored back in TMEM
+  uint64_t s_full;       // MMA -> element-wise: S (or S^T) of the current tile pair in TMEM
+  uint64_t dp_full;      // MMA -> element-wise: dP (or dP^T) in TMEM
+  uint64_t p_done;       // element-wise -> MMA: P^T stored (key-outer) / S read (query-outer)
+  uint64_t ds_ready;     // element-wise -> MMA: dS (or dS^T) stored in TMEM
   uint64_t acc_final;    // MMA -> element-wise: the last accumulation finished
   uint64_t mma_drain;    // MMA warp: all of its MMAs finished (before TMEM is freed)
   uint64_t stage_full[4];
@@ -43,6 +45,12 @@ __device__ __forceinline__ void unpack_elem2(uint32_t v, float& lo, float& hi) {
     lo = __uint_as_float(v << 16);
     hi = __uint_as_float(v & 0xFFFF0000u);
   }
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 // Tile order shared by both passes: heads in groups of p.head_group (their streamed
@@ -160,8 +168,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->fixed_full), 1);
-    mbar_init(smem_u32(&bars->sp_full), 1);
-    mbar_init(smem_u32(&bars->ds_ready), 8);  // one arrival per element-wise warp
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->dp_full), 1);
+    mbar_init(smem_u32(&bars->p_done), 8);    // one arrival per element-wise warp
+    mbar_init(smem_u32(&bars->ds_ready), 8);
     mbar_init(smem_u32(&bars->acc_final), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
     for (int s = 0; s < Cfg::kStages; ++s) {
@@ -238,43 +248,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (r) tc_fence_after();
       return r;
     };
-    bool ok = wait_bar(&bars->fixed_full, 0);
+    auto desc_k = [&](int it, int tile) {  // K-major view of a streamed tile
+      return desc_sw128(stage_addr(it % Cfg::kStages) + tile * Cfg::kTileBytes, 16, 1024);
+    };
+    auto desc_mn = [&](int it, int tile) {  // MN-major view of a streamed tile
+      return desc_sw128(stage_addr(it % Cfg::kStages) + tile * Cfg::kTileBytes, kBoxBytes, 1024);
+    };
+    // S^T = K_j Q_i^T into tS, or dP^T = V_j dO_i^T into tDP: keys on lanes, queries on
+    // columns; the streamed tile is the K-major B operand.
+    auto issue_t = [&](uint32_t tD, uint64_t dA, uint64_t dB) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_elect(tD, dA + off16, dB + off16, kIdescS, kk > 0 ? 1u : 0u);
+      }
+    };
+    // tAcc += A^T-part from TMEM (16 queries = 8 packed columns per step; column half h
+    // of the tile was packed into columns 64h .. 64h+31) times a streamed MN-major tile.
+    auto issue_acc = [&](uint32_t tAcc, uint32_t tA, uint64_t dB, bool acc) {
+#pragma unroll
+      for (int kk = 0; kk < kBlockM / 16; ++kk) {
+        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+        mma_bf16_ts_elect(tAcc, tA + acol, dB + ((kk * 2048) >> 4), kIdescAcc,
+                          (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    // Software pipeline on the tensor pipe, per query tile it:
+    //   dV += P^T(it) dO_it  |  S^T(it+1)  |  dK += dS^T(it) Q_it  |  dP^T(it+1)
+    // dV needs only P^T, so it and the next S^T run while the element-wise warps form
+    // dS^T; the next element-wise step starts on S^T(it+1) while dK and dP^T(it+1) run.
+    // Each TMEM region is overwritten only after the product that reads it (one issuing
+    // thread: products complete in issue order).
+    bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0);
+    if (ok) {
+      issue_t(tS, dK, desc_k(0, 0));
+      mma_commit_elect(smem_u32(&bars->s_full));
+      issue_t(tDP, dV, desc_k(0, 1));
+      mma_commit_elect(smem_u32(&bars->dp_full));
+    }
     for (int it = 0; ok && it < nq; ++it) {
-      const int s = it % Cfg::kStages;
-      if (!(ok = wait_bar(&bars->stage_full[s], (it / Cfg::kStages) & 1))) break;
-      const uint32_t st = stage_addr(s);
-      const uint64_t dQk = desc_sw128(st, 16, 1024);                          // B of S^T
-      const uint64_t dDOk = desc_sw128(st + Cfg::kTileBytes, 16, 1024);       // B of dP^T
-      const uint64_t dDOmn = desc_sw128(st + Cfg::kTileBytes, kBoxBytes, 1024);  // B of dV
-      const uint64_t dQmn = desc_sw128(st, kBoxBytes, 1024);                   // B of dK
-      // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: keys on lanes, queries on columns.
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_elect(tS, dK + off16, dQk + off16, kIdescS, kk > 0 ? 1u : 0u);
+      const bool more = it + 1 < nq;
+      if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
+      issue_acc(tDV, tS, desc_mn(it, 1), it > 0);
+      if (more) {
+        if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
+                            ((it + 1) / Cfg::kStages) & 1)))
+          break;
+        issue_t(tS, dK, desc_k(it + 1, 0));
+        mma_commit_elect(smem_u32(&bars->s_full));
       }
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_elect(tDP, dV + off16, dDOk + off16, kIdescS, kk > 0 ? 1u : 0u);
-      }
-      mma_commit_elect(smem_u32(&bars->sp_full));
       if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
-      // dV += P^T dO_i and dK += dS^T Q_i: A (16 queries = 8 packed columns per step)
-      // from TMEM, where column half h of the tile was packed into columns 64h .. 64h+31.
-#pragma unroll
-      for (int kk = 0; kk < kBlockM / 16; ++kk) {
-        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
-        mma_bf16_ts_elect(tDV, tS + acol, dDOmn + ((kk * 2048) >> 4), kIdescAcc,
-                          (it > 0 || kk > 0) ? 1u : 0u);
+      issue_acc(tDK, tDP, desc_mn(it, 0), it > 0);
+      mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
+      if (more) {
+        issue_t(tDP, dV, desc_k(it + 1, 1));
+        mma_commit_elect(smem_u32(&bars->dp_full));
       }
-#pragma unroll
-      for (int kk = 0; kk < kBlockM / 16; ++kk) {
-        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
-        mma_bf16_ts_elect(tDK, tDP + acol, dQmn + ((kk * 2048) >> 4), kIdescAcc,
-                          (it > 0 || kk > 0) ? 1u : 0u);
-      }
-      mma_commit_elect(smem_u32(&bars->stage_empty[s]));
     }
     if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
     mma_commit_elect(smem_u32(&bars->mma_drain));
@@ -290,43 +319,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tS = tbase + lane_off + Cfg::kColS, tDP = tbase + lane_off + Cfg::kColDP;
     const float sl2 = p.scale_log2;
     bool ok = true;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     for (int it = 0; it < nq; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sp_full), it & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
       if (!ok) break;
-      tc_fence_after();
-      const int i = i0 + it;
       // The statistics came in by TMA with the stage; wait on the stage's own barrier
-      // (complete already: the MMAs that consumed the stage are done) to see them.
+      // (complete already: S^T of this stage is done) to see them.
       ok = __all_sync(0xffffffffu,
                       mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]),
                                 (it / Cfg::kStages) & 1, abort, p.status));
       if (!ok) break;
+      tc_fence_after();
+      const int i = i0 + it;
       const float* lse2s = reinterpret_cast<const float*>(
           smem + Cfg::kSmemStages + (it % Cfg::kStages) * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
       const float* dds = lse2s + 128;
       const bool diag = p.causal && i == j;  // query q sees key r iff r <= q
+      // P^T = exp2(S^T * scale * log2 e - LSE * log2 e): kept in registers for dS^T and
+      // stored (16-bit) over the first half of this warp's S^T columns for dV.
+      uint64_t pv[32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * h + 32 * ch;    // first query (column) of this chunk
-        uint32_t s[32], dp[32];
-        tmem_ld32_wait(tS + c0, s);
-        tmem_ld32_wait(tDP + c0, dp);
-        uint32_t pk[16], pd[16];
+        uint32_t sr[32];
+        tmem_ld32_wait(tS + c0, sr);
+        const float4* l4 = reinterpret_cast<const float4*>(lse2s + c0);
+        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pr[2], dsv[2];
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l = l4[c4];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int q = c0 + c + e;
-            float pv = ex2_approx(fmaf(__uint_as_float(s[c + e]), sl2, -lse2s[q]));
-            if (diag && q < r) pv = 0.f;
-            pr[e] = pv;
-            dsv[e] = pv * (__uint_as_float(dp[c + e]) - dds[q]);
+            const int c = 4 * c4 + 2 * e;
+            const uint64_t negl = e ? f2_pack(-l.z, -l.w) : f2_pack(-l.x, -l.y);
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
+                             negl),
+                      x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (diag) {
+              if (c0 + c < r) p0 = 0.f;
+              if (c0 + c + 1 < r) p1 = 0.f;
+            }
+            pv[16 * ch + (c >> 1)] = f2_pack(p0, p1);
+            pk[c >> 1] = pack_elem2<F16>(p0, p1);
           }
-          pk[c >> 1] = pack_elem2<F16>(pr[0], pr[1]);
-          pd[c >> 1] = pack_elem2<F16>(dsv[0], dsv[1]);
         }
         tmem_st16(tS + 64 * h + 16 * ch, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
+
+      // dS^T = P^T * (dP^T - D), stored over the first half of this warp's dP^T columns.
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * h + 32 * ch;
+        uint32_t dr[32];
+        tmem_ld32_wait(tDP + c0, dr);
+        const float4* d4 = reinterpret_cast<const float4*>(dds + c0);
+        uint32_t pd[16];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dq4 = d4[c4];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = 4 * c4 + 2 * e;
+            const uint64_t negd = e ? f2_pack(-dq4.z, -dq4.w) : f2_pack(-dq4.x, -dq4.y);
+            const uint64_t ds = f2_mul(
+                pv[16 * ch + (c >> 1)],
+                f2_add(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), negd));
+            float d0, d1;
+            f2_unpack(ds, d0, d1);
+            pd[c >> 1] = pack_elem2<F16>(d0, d1);
+          }
+        }
         tmem_st16(tDP + 64 * h + 16 * ch, pd);
       }
       tmem_wait_st();
@@ -386,7 +457,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->fixed_full), 1);
-    mbar_init(smem_u32(&bars->sp_full), 1);
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->dp_full), 1);
+    mbar_init(smem_u32(&bars->p_done), 8);    // one arrival per element-wise warp
     mbar_init(smem_u32(&bars->ds_ready), 8);
     mbar_init(smem_u32(&bars->acc_final), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
@@ -456,35 +529,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (r) tc_fence_after();
       return r;
     };
-    bool ok = wait_bar(&bars->fixed_full, 0);
+    auto stage_desc = [&](int it, int tile, uint32_t lbo) {
+      return desc_sw128(stage_addr(it % Cfg::kStages) + tile * Cfg::kTileBytes, lbo, 1024);
+    };
+    // S = Q_i K_j^T into tS, or dP = dO_i V_j^T into tDP: queries on lanes, keys on
+    // columns; the streamed tile is the K-major B operand.
+    auto issue_n = [&](uint32_t tD, uint64_t dA, uint64_t dB) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_elect(tD, dA + off16, dB + off16, kIdescS, kk > 0 ? 1u : 0u);
+      }
+    };
+    // Software pipeline on the tensor pipe, per key tile it:
+    //   S(it+1) (once the element-wise warps hold S(it) in registers)  |
+    //   dQ += dS(it) K_it (dS stored over dP(it))  |  dP(it+1)
+    // so the next S is computed while dS(it) is being formed.
+    bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0);
+    if (ok) {
+      issue_n(tS, dQ, stage_desc(0, 0, 16));
+      mma_commit_elect(smem_u32(&bars->s_full));
+      issue_n(tDP, dDO, stage_desc(0, 1, 16));
+      mma_commit_elect(smem_u32(&bars->dp_full));
+    }
     for (int it = 0; ok && it < nk; ++it) {
-      const int s = it % Cfg::kStages;
-      if (!(ok = wait_bar(&bars->stage_full[s], (it / Cfg::kStages) & 1))) break;
-      const uint32_t st = stage_addr(s);
-      const uint64_t dKk = desc_sw128(st, 16, 1024);                        // B of S
-      const uint64_t dVk = desc_sw128(st + Cfg::kTileBytes, 16, 1024);      // B of dP
-      const uint64_t dKmn = desc_sw128(st, kBoxBytes, 1024);                // B of dQ
-      // S = Q_i K_j^T and dP = dO_i V_j^T: queries on lanes, keys on columns.
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_elect(tS, dQ + off16, dKk + off16, kIdescS, kk > 0 ? 1u : 0u);
+      const bool more = it + 1 < nk;
+      if (more) {
+        if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
+        if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
+                            ((it + 1) / Cfg::kStages) & 1)))
+          break;
+        issue_n(tS, dQ, stage_desc(it + 1, 0, 16));
+        mma_commit_elect(smem_u32(&bars->s_full));
       }
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_elect(tDP, dDO + off16, dVk + off16, kIdescS, kk > 0 ? 1u : 0u);
-      }
-      mma_commit_elect(smem_u32(&bars->sp_full));
       if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
-      // dQ += dS K_j: dS (16 keys = 8 packed columns per step) from TMEM.
+      // dQ += dS K_j: dS (16 keys = 8 packed columns per step) from the dP columns.
+      const uint64_t dKmn = stage_desc(it, 0, kBoxBytes);
 #pragma unroll
       for (int kk = 0; kk < kBlockM / 16; ++kk) {
         const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
-        mma_bf16_ts_elect(tDQ, tS + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
+        mma_bf16_ts_elect(tDQ, tDP + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
                           (it > 0 || kk > 0) ? 1u : 0u);
       }
-      mma_commit_elect(smem_u32(&bars->stage_empty[s]));
+      mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
+      if (more) {
+        issue_n(tDP, dDO, stage_desc(it + 1, 1, 16));
+        mma_commit_elect(smem_u32(&bars->dp_full));
+      }
     }
     if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
     mma_commit_elect(smem_u32(&bars->mma_drain));
@@ -503,8 +594,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float lse2 = p.lse2[srow];
     const float dd = p.dd[srow];
     bool ok = true;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    const uint64_t negl2 = f2_pack(-lse2, -lse2);
+    const uint64_t negd2 = f2_pack(-dd, -dd);
     for (int it = 0; it < nk; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sp_full), it & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
       const int key0 = it * kBlockM;
@@ -512,25 +606,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool need_mask = (p.causal && it == i) || key0 + kBlockM > p.N;
       int lim = p.N - 1 - key0;
       if (p.causal) lim = min(lim, qg - key0);
+      // P = exp2(S * scale * log2 e - LSE * log2 e), in registers.
+      uint64_t pv[32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * h + 32 * ch;   // first key (column) of this chunk
-        uint32_t s[32], dp[32];
-        tmem_ld32_wait(tS + c0, s);
-        tmem_ld32_wait(tDP + c0, dp);
+        uint32_t sr[32];
+        tmem_ld32_wait(tS + c0, sr);
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
+                           negl2),
+                    x0, x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (need_mask) {
+            if (c0 + c > lim) p0 = 0.f;
+            if (c0 + c + 1 > lim) p1 = 0.f;
+          }
+          pv[16 * ch + (c >> 1)] = f2_pack(p0, p1);
+        }
+      }
+      if (it + 1 < nk) {  // S(it) is in registers: the next S may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
+      }
+      // dS = P * (dP - D), stored (16-bit) over the first half of this warp's dP columns.
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * h + 32 * ch;
+        uint32_t dr[32];
+        tmem_ld32_wait(tDP + c0, dr);
         uint32_t pd[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          float dsv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float pv = ex2_approx(fmaf(__uint_as_float(s[c + e]), sl2, -lse2));
-            if (need_mask && c0 + c + e > lim) pv = 0.f;
-            dsv[e] = pv * (__uint_as_float(dp[c + e]) - dd);
-          }
-          pd[c >> 1] = pack_elem2<F16>(dsv[0], dsv[1]);
+          const uint64_t ds = f2_mul(
+              pv[16 * ch + (c >> 1)],
+              f2_add(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), negd2));
+          float d0, d1;
+          f2_unpack(ds, d0, d1);
+          pd[c >> 1] = pack_elem2<F16>(d0, d1);
         }
-        tmem_st16(tS + 64 * h + 16 * ch, pd);
+        tmem_st16(tDP + 64 * h + 16 * ch, pd);
       }
       tmem_wait_st();
       tc_fence_before();
