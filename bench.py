@@ -69,19 +69,32 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def kernel_sources_hash():
+# Source files each measured kernel is built from (its launch configuration included):
+# recorded DRAM traffic stays valid only while these files are unchanged.
+KERNEL_FILES = {
+    "attn_fwd_tc_kernel": ["attn_tc.cuh", "attn_tc_impl.cuh", "ptx.cuh", "attn_tc_d128.cu",
+                           "api.cu"],
+    "row_state_block_kernel": ["row_state.cu", "api.cu"],
+    "attn_bwd_dkdv_kernel": ["attn_bwd.cuh", "attn_bwd_impl.cuh", "attn_tc.cuh",
+                             "attn_tc_impl.cuh", "ptx.cuh", "attn_bwd_d128.cu", "api_bwd.cu"],
+    "attn_bwd_dq_kernel": ["attn_bwd.cuh", "attn_bwd_impl.cuh", "attn_tc.cuh",
+                           "attn_tc_impl.cuh", "ptx.cuh", "attn_bwd_d128.cu", "api_bwd.cu"],
+}
+
+
+def kernel_sources_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "online_softmax_07_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in sorted(KERNEL_FILES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
+    current sources of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -89,7 +102,7 @@ def recorded_traffic(kernel):
     except (OSError, ValueError):
         return None
     ent = rec.get(kernel)
-    if not ent or ent.get("sources") != kernel_sources_hash():
+    if not ent or ent.get("sources") != kernel_sources_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -560,6 +573,39 @@ def suite(args):
         return {"o_max_abs_err": float(e.max()), "o_mean_abs_err": float(e.mean()),
                 "lse_max_abs_err": float(le.max()), "rows_checked": int(le.size)}
 
+    def bwd_line(name, q, k, v, do, causal):
+        """fa_bwd after fa_fwd; TFLOP/s counts the five algorithmic products
+        (2.5 x the forward's FLOPs); errors against the oracle on 32 seeded query and
+        key rows (plus the first and last) of the first and last head."""
+        import oracle
+        B, H, N, d = q.shape
+        tq, tk, tv, tdo = (torch.from_numpy(t).to(dev, torch.bfloat16) for t in (q, k, v, do))
+        o = torch.empty_like(tq)
+        lse = torch.empty((B, H, N), device=dev)
+        scale = 1.0 / math.sqrt(d)
+        abi.fa_fwd_dt(tq, tk, tv, o, lse, B, H, N, d, scale, int(causal), abi.FA_BF16, stream)
+        nbytes = abi.fa_bwd_workspace_bytes(B, H, N)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        gq, gk, gv = torch.empty_like(tq), torch.empty_like(tq), torch.empty_like(tq)
+        fn = lambda: abi.fa_bwd(tq, tk, tv, o, lse, tdo, gq, gk, gv, B, H, N, d, scale,
+                                int(causal), ws, nbytes, abi.FA_BF16, stream)
+        ms = timed(fn, 20)
+        tf = 2.5 * attn_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
+        rows = np.unique(np.concatenate(
+            [[0, N - 1], np.random.Generator(np.random.PCG64(11)).choice(N, 32, False)]))
+        rel = {"dQ": [], "dK": [], "dV": []}
+        for (b, h) in ((0, 0), (B - 1, H - 1)):
+            ref = oracle.attention_backward_rows(q, k, v, do, scale, causal, (b, h), rows, rows)
+            idx = torch.from_numpy(rows).to(dev)
+            for key, t, r in zip(("dQ", "dK", "dV"), (gq, gk, gv), ref):
+                got = t[b, h].index_select(0, idx).float().cpu().numpy()
+                rel[key].append(float(np.linalg.norm(got - r) / np.linalg.norm(r)))
+        line = {"workload": name.replace("attn_", "attn_bwd_"), "dtype": "bf16", "ms": ms,
+                "TFLOP/s": tf, "pct_of_bf16_peak": 100 * tf / peaks["bf16_tflops"],
+                "executed_TFLOP/s": tf * 7 / 5}
+        line.update({f"{k}_rel_rms_err": max(v) for k, v in rel.items()})
+        print(json.dumps(line), flush=True)
+
     for name in ("attn_f32_b1h1n128d64", "attn_bf16_b4h16n4096d64",
                  "attn_bf16_b2h16n8192d128_causal", "attn_bf16_b2h16n8191d128_causal",
                  "attn_bf16_b1h8n32768d128_causal_qstd4"):
@@ -581,6 +627,14 @@ def suite(args):
     attn_line(label, q, k, v, True, "bf16", label=label + " (no split)")
     s_def = abi.fa_fwd_splitkv_default_splits(1, 1, 16384)
     attn_line(label, q, k, v, True, "bf16", splits=s_def, label=label + " (split-KV)")
+    # backward (fa_bwd) on the attention workloads with a seeded dO of the same shape
+    for name in ("attn_bf16_b4h16n4096d64", "attn_bf16_b2h16n8192d128_causal",
+                 "attn_bf16_b1h8n32768d128_causal_qstd4"):
+        w = synth.WORKLOADS[name]
+        q, k, v = synth.workload_attention_inputs(name)
+        B, H, N, d = q.shape
+        do = synth.attention_inputs(B, H, N, d, seed=97000 + d)[0]
+        bwd_line(name, q, k, v, do, w["causal"])
     # row state and normalised softmax on the 4096 x 32768 array
     x = torch.from_numpy(synth.workload_row_inputs()[0]).to(dev)
     rows, length = x.shape
