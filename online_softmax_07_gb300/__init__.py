@@ -44,34 +44,67 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    host = not q.is_cuda
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-
-        def up(t):
-            t = t.contiguous()
-            if not t.is_pinned():
-                t = t.pin_memory()
-            return t.to(dev, non_blocking=True)
-
-        q, k, v = up(q), up(k), up(v)
-    else:
-        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if with_lse else None
     dtype = {torch.bfloat16: abi.FA_BF16, torch.float16: abi.FA_F16,
              torch.float32: abi.FA_F32}[q.dtype]
-    fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), dtype)
-    if not host:
+    if q.is_cuda:
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if with_lse else None
+        fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), dtype)
         return o, lse
-    o_h = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    o_h.copy_(o, non_blocking=True)
+    return _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype)
+
+
+def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype):
+    """Host tensors in, host tensors out, with the copies overlapped with the kernels:
+    the (batch, head) slabs are split into chunks; chunk c is copied in on one stream,
+    computed on the caller's stream and copied out on a third, so the copy of chunk c+1
+    runs while chunk c computes and the copy out of chunk c overlaps both."""
+    import torch
+
+    B, H, N, d = q.shape
+    BH = B * H
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def pinned(t):
+        t = t.contiguous()
+        return t if t.is_pinned() else t.pin_memory()
+
+    qh, kh, vh = (pinned(t).view(BH, N, d) for t in (q, k, v))
+    o_h = out if out is not None else torch.empty((B, H, N, d), dtype=q.dtype, pin_memory=True)
     lse_h = None
-    if lse is not None:
-        lse_h = lse_out if lse_out is not None else torch.empty(lse.shape, dtype=torch.float32,
+    if with_lse:
+        lse_h = lse_out if lse_out is not None else torch.empty((B, H, N), dtype=torch.float32,
                                                                 pin_memory=True)
-        lse_h.copy_(lse, non_blocking=True)
-    torch.cuda.current_stream().synchronize()
+    o_hv = o_h.view(BH, N, d)
+    lse_hv = lse_h.view(BH, N) if lse_h is not None else None
+    qd, kd, vd = (torch.empty((BH, N, d), dtype=q.dtype, device=dev) for _ in range(3))
+    od = torch.empty((BH, N, d), dtype=q.dtype, device=dev)
+    lsed = torch.empty((BH, N), dtype=torch.float32, device=dev) if with_lse else None
+    compute = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_in.wait_stream(compute)      # device buffers are ordered after earlier work
+    # About 8 chunks: enough overlap, while each launch still fills most SMs.
+    n_chunks = max(1, min(BH, 8))
+    bounds = [BH * c // n_chunks for c in range(n_chunks + 1)]
+    for c in range(n_chunks):
+        h0, h1 = bounds[c], bounds[c + 1]
+        if h1 == h0:
+            continue
+        with torch.cuda.stream(s_in):
+            for dst, src in ((qd, qh), (kd, kh), (vd, vh)):
+                dst[h0:h1].copy_(src[h0:h1], non_blocking=True)
+        compute.wait_stream(s_in)
+        fa_fwd_dt(qd[h0:h1], kd[h0:h1], vd[h0:h1], od[h0:h1],
+                  lsed[h0:h1] if lsed is not None else None, 1, h1 - h0, N, d, scale,
+                  int(bool(causal)), dtype)
+        s_out.wait_stream(compute)
+        with torch.cuda.stream(s_out):
+            o_hv[h0:h1].copy_(od[h0:h1], non_blocking=True)
+            if lsed is not None:
+                lse_hv[h0:h1].copy_(lsed[h0:h1], non_blocking=True)
+    s_out.synchronize()
+    compute.synchronize()
     return o_h, lse_h
 
 

@@ -1,0 +1,71 @@
+"""The public Python API (online_softmax_07_gb300.attention_forward / attention_backward /
+row_state / softmax): host tensors in and out, with the copies pipelined against the
+kernels in chunks of heads, must give exactly what the device path gives (the kernels
+compute every head independently, so chunking changes no arithmetic)."""
+
+import numpy as np
+import pytest
+import torch
+
+import online_softmax_07_gb300 as osf
+from online_softmax_07_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,pin", [
+    (1, 3, 300, 128, True, True),     # 3 chunks of one head
+    (2, 5, 257, 64, False, False),    # 10 heads in 8 uneven chunks, inputs not pinned
+    (1, 1, 129, 128, True, True),     # a single chunk
+    (4, 16, 1024, 128, True, True),   # 64 heads in 8 chunks of 8
+])
+def test_host_path_equals_device_path(B, H, N, d, causal, pin):
+    q, k, v = (torch.from_numpy(t).to(torch.bfloat16)
+               for t in synth.attention_inputs(B, H, N, d, seed=991 + N))
+    if pin:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o_h, lse_h = osf.attention_forward(q, k, v, causal=causal)
+    assert not o_h.is_cuda and o_h.is_pinned()
+    o_d, lse_d = osf.attention_forward(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(lse_h, lse_d.cpu())
+
+
+def test_host_path_into_given_buffers_and_without_lse():
+    B, H, N, d = 2, 4, 200, 64
+    q, k, v = (torch.from_numpy(t).to(torch.bfloat16).pin_memory()
+               for t in synth.attention_inputs(B, H, N, d, seed=995))
+    out = torch.full((B, H, N, d), float("nan"), dtype=torch.bfloat16, pin_memory=True)
+    lse_out = torch.full((B, H, N), float("nan"), pin_memory=True)
+    o1, l1 = osf.attention_forward(q, k, v, scale=0.2, out=out, lse_out=lse_out)
+    assert o1.data_ptr() == out.data_ptr() and l1.data_ptr() == lse_out.data_ptr()
+    o2, l2 = osf.attention_forward(q, k, v, scale=0.2, with_lse=False)
+    assert l2 is None
+    assert torch.equal(o1, o2)
+    o_d, _ = osf.attention_forward(q.cuda(), k.cuda(), v.cuda(), scale=0.2)
+    assert torch.equal(o1, o_d.cpu())
+
+
+def test_backward_api_matches_abi():
+    B, H, N, d = 1, 2, 300, 128
+    q, k, v = (torch.from_numpy(t).to("cuda", torch.bfloat16)
+               for t in synth.attention_inputs(B, H, N, d, seed=996))
+    do = torch.from_numpy(synth.attention_inputs(B, H, N, d, seed=997)[0]).to("cuda", torch.bfloat16)
+    o, lse = osf.attention_forward(q, k, v, causal=True)
+    g1 = osf.attention_backward(q, k, v, o, lse, do, causal=True)
+    g2 = osf.attention_backward(q, k, v, o, lse, do, causal=True)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+        assert torch.isfinite(a.float()).all()
+
+
+def test_row_state_and_softmax_host_and_device():
+    x = torch.from_numpy(synth.row_inputs(37, 3001, seed=998))
+    m_h, l_h = osf.row_state(x)
+    m_d, l_d = osf.row_state(x.cuda())
+    assert torch.equal(m_h, m_d.cpu()) and torch.equal(l_h, l_d.cpu())
+    y, m, l = osf.softmax(x.cuda())
+    assert torch.equal(m.cpu(), m_h)
+    rows_sum = y.double().sum(dim=1).cpu().numpy()
+    assert np.abs(rows_sum - 1).max() < 1e-5
