@@ -55,6 +55,18 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
     return _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype)
 
 
+_COPY_STREAMS = {}
+
+
+def _copy_streams(dev):
+    """The copy-in and copy-out streams of a device, created once."""
+    import torch
+
+    if dev.index not in _COPY_STREAMS:
+        _COPY_STREAMS[dev.index] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    return _COPY_STREAMS[dev.index]
+
+
 def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype):
     """Host tensors in, host tensors out, with the copies overlapped with the kernels:
     the (batch, head) slabs are split into chunks; chunk c is copied in on one stream,
@@ -82,10 +94,11 @@ def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtyp
     od = torch.empty((BH, N, d), dtype=q.dtype, device=dev)
     lsed = torch.empty((BH, N), dtype=torch.float32, device=dev) if with_lse else None
     compute = torch.cuda.current_stream()
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_in, s_out = _copy_streams(dev)
     s_in.wait_stream(compute)      # device buffers are ordered after earlier work
-    # About 8 chunks: enough overlap, while each launch still fills most SMs.
-    n_chunks = max(1, min(BH, 8))
+    # Four chunks: measured on B2 H16 N8192 d128 as fast as eight (1.30 ms against
+    # 1.73 ms unchunked); sixteen and more are held back by the per-call host overhead.
+    n_chunks = max(1, min(BH, 4))
     bounds = [BH * c // n_chunks for c in range(n_chunks + 1)]
     for c in range(n_chunks):
         h0, h1 = bounds[c], bounds[c + 1]
