@@ -58,8 +58,13 @@ struct AttnTcCfg {
   static constexpr int kSmemSlots = 2 * kTileBytes;
   static constexpr int kSmemBars = kSmemSlots + kSlots * kTileBytes;
   static constexpr int kSmemBytes = kSmemBars + 512 + 1024;  // + barriers + alignment slack
-  // TMEM columns: S/P of tile 0 and 1, then O of tile 0 and 1.
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  // TMEM columns.  d = 128: S/P of tile 0 and 1, then O of tile 0 and 1.  d = 64: the O
+  // accumulators take only 128 columns, which leaves room for a third S/P buffer; the
+  // two tiles then use three S/P buffers in rotation (kTripleS), so that the next S of a
+  // tile can be computed while its current P is still being formed.
+  static constexpr bool kTripleS = (D == 64);
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColS2 = 256;
+  static constexpr uint32_t kColO0 = kTripleS ? 384 : 256, kColO1 = kColO0 + D;
   static constexpr uint32_t kTmemCols = 512;
 };
 

@@ -13,6 +13,7 @@ struct AttnTcBarriers {
   uint64_t s_full[2];    // MMA -> softmax t: S_t of the current K/V tile is in TMEM
   uint64_t p_ready[2];   // softmax t -> MMA: P_t stored in TMEM and O_t rescaled
   uint64_t o_final[2];   // MMA -> softmax t: last P_t V product done
+  uint64_t pv_done[2];   // MMA -> softmax t: P_t V of a K/V tile done (three-buffer mode)
   uint64_t mma_drain;    // MMA thread: all of its MMAs finished (before TMEM is freed)
   uint64_t slot_full[8];
   uint64_t slot_empty[8];
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(smem_u32(&bars->s_full[t]), 1);
       mbar_init(smem_u32(&bars->p_ready[t]), 4);  // one arrival per softmax warp
       mbar_init(smem_u32(&bars->o_final[t]), 1);
+      mbar_init(smem_u32(&bars->pv_done[t]), 1);
     }
     mbar_init(smem_u32(&bars->mma_drain), 1);
     for (int s = 0; s < Cfg::kSlots; ++s) {
@@ -226,48 +228,105 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort, p.status) && wait_full(0);
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after();
-      if (n0 > 0) {
-        issue_s(tS0, dQ0, 0);
-        mma_commit_elect(smem_u32(&bars->s_full[0]));
+    if constexpr (Cfg::kTripleS) {
+      // Three S/P buffers in rotation: the S issued at position pos of the sequence
+      // S_0(0), S_1(0), S_0(1), S_1(1), ... (S_0(j) at 2j, S_1(j) at min(j+1, n0) + j once
+      // tile 0 has run out) goes to buffer pos % 3.  Per K/V tile j the pipe receives
+      // S_0(j+1), P_0(j) V, S_1(j+1), P_1(j) V: the next S of a tile is computed while its
+      // softmax still works on the current one.  The buffer an S overwrites last held the
+      // S three positions earlier, whose P V was issued before (in-order pipe).
+      auto colS = [&](int pos) { return tbase + static_cast<uint32_t>((pos % 3) * 128); };
+      auto wait_bar = [&](uint64_t* bar, int parity) {
+        const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, abort, p.status));
+        if (r) tc_fence_after();
+        return r;
+      };
+      if (ok) {
+        tc_fence_after();
+        if (n0 > 0) {
+          issue_s(colS(0), dQ0, 0);
+          mma_commit_elect(smem_u32(&bars->s_full[0]));
+        }
+        issue_s(colS(n0 > 0 ? 1 : 0), dQ1, 0);
+        mma_commit_elect(smem_u32(&bars->s_full[1]));
+        mma_commit_elect(smem_u32(&bars->slot_empty[0]));
       }
-      issue_s(tS1, dQ1, 0);
-      mma_commit_elect(smem_u32(&bars->s_full[1]));
-      mma_commit_elect(smem_u32(&bars->slot_empty[0]));
-    }
-    for (int j = 0; ok && j < n1; ++j) {
-      const int itV = 2 * j + 1, itK = 2 * j + 2;
-      if (!(ok = __all_sync(0xffffffffu, wait_full(itV)))) break;
-      if (j < n0) {
+      for (int j = 0; ok && j < n1; ++j) {
+        const int itV = 2 * j + 1, itK = 2 * j + 2;
+        if (!(ok = __all_sync(0xffffffffu, wait_full(itV)))) break;
+        bool k_ready = false;
+        if (j < n0) {
+          if (j + 1 < n0) {
+            if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
+            k_ready = true;
+            tc_fence_after();
+            issue_s(colS(2 * j + 2), dQ0, itK);
+            mma_commit_elect(smem_u32(&bars->s_full[0]));
+          }
+          if (!(ok = wait_bar(&bars->p_ready[0], j & 1))) break;
+          issue_pv(tO0, colS(2 * j), itV, j > 0);
+          mma_commit_elect(smem_u32(&bars->pv_done[0]));
+          if (j + 1 == n0) mma_commit_elect(smem_u32(&bars->o_final[0]));
+        }
+        if (j + 1 < n1) {
+          if (!k_ready) {
+            if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
+            tc_fence_after();
+          }
+          issue_s(colS(min(j + 2, n0) + j + 1), dQ1, itK);
+          mma_commit_elect(smem_u32(&bars->s_full[1]));
+          mma_commit_elect(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
+        }
+        if (!(ok = wait_bar(&bars->p_ready[1], j & 1))) break;
+        issue_pv(tO1, colS(min(j + 1, n0) + j), itV, j > 0);
+        mma_commit_elect(smem_u32(&bars->pv_done[1]));
+        mma_commit_elect(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
+        if (j + 1 == n1) mma_commit_elect(smem_u32(&bars->o_final[1]));
+      }
+    } else {
+      if (ok) {
+        tc_fence_after();
+        if (n0 > 0) {
+          issue_s(tS0, dQ0, 0);
+          mma_commit_elect(smem_u32(&bars->s_full[0]));
+        }
+        issue_s(tS1, dQ1, 0);
+        mma_commit_elect(smem_u32(&bars->s_full[1]));
+        mma_commit_elect(smem_u32(&bars->slot_empty[0]));
+      }
+      for (int j = 0; ok && j < n1; ++j) {
+        const int itV = 2 * j + 1, itK = 2 * j + 2;
+        if (!(ok = __all_sync(0xffffffffu, wait_full(itV)))) break;
+        if (j < n0) {
+          if (!(ok = __all_sync(0xffffffffu,
+                                mbar_wait(smem_u32(&bars->p_ready[0]), j & 1, abort, p.status))))
+            break;
+          tc_fence_after();
+          issue_pv(tO0, tS0, itV, j > 0);
+          if (j + 1 < n0) {
+            if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
+            tc_fence_after();
+            issue_s(tS0, dQ0, itK);
+            mma_commit_elect(smem_u32(&bars->s_full[0]));
+          } else {
+            mma_commit_elect(smem_u32(&bars->o_final[0]));
+          }
+        }
         if (!(ok = __all_sync(0xffffffffu,
-                              mbar_wait(smem_u32(&bars->p_ready[0]), j & 1, abort, p.status))))
+                              mbar_wait(smem_u32(&bars->p_ready[1]), j & 1, abort, p.status))))
           break;
         tc_fence_after();
-        issue_pv(tO0, tS0, itV, j > 0);
-        if (j + 1 < n0) {
+        issue_pv(tO1, tS1, itV, j > 0);
+        mma_commit_elect(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
+        if (j + 1 < n1) {
           if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
           tc_fence_after();
-          issue_s(tS0, dQ0, itK);
-          mma_commit_elect(smem_u32(&bars->s_full[0]));
+          issue_s(tS1, dQ1, itK);
+          mma_commit_elect(smem_u32(&bars->s_full[1]));
+          mma_commit_elect(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
         } else {
-          mma_commit_elect(smem_u32(&bars->o_final[0]));
+          mma_commit_elect(smem_u32(&bars->o_final[1]));
         }
-      }
-      if (!(ok = __all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(&bars->p_ready[1]), j & 1, abort, p.status))))
-        break;
-      tc_fence_after();
-      issue_pv(tO1, tS1, itV, j > 0);
-      mma_commit_elect(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
-      if (j + 1 < n1) {
-        if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
-        tc_fence_after();
-        issue_s(tS1, dQ1, itK);
-        mma_commit_elect(smem_u32(&bars->s_full[1]));
-        mma_commit_elect(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
-      } else {
-        mma_commit_elect(smem_u32(&bars->o_final[1]));
       }
     }
     // Drain: nothing may still read shared memory or TMEM when the block exits.
@@ -283,7 +342,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int rr = wq * 32 + lane; // row within the tile
     const int r0 = qb * 2 * kBlockM + t * kBlockM;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tbase + lane_off + (t ? Cfg::kColS1 : Cfg::kColS0);
+    const uint32_t tS_fixed = tbase + lane_off + (t ? Cfg::kColS1 : Cfg::kColS0);
     const uint32_t tO = tbase + lane_off + (t ? Cfg::kColO1 : Cfg::kColO0);
     const float sl2 = p.scale_log2;
     float m2 = -INFINITY;  // rescale reference, log2 units of the scaled score
@@ -296,6 +355,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      // With three S buffers, S_t(j) is in buffer (its position in the rotation) % 3.
+      const uint32_t tS =
+          Cfg::kTripleS
+              ? tbase + lane_off + static_cast<uint32_t>(((t ? min(j + 1, n0) + j : 2 * j) % 3) * 128)
+              : tS_fixed;
       uint32_t sr[128];
       tmem_ld128_wait(tS, sr);
       float* s = reinterpret_cast<float*>(sr);
@@ -320,8 +384,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float alpha = ex2_approx(m2 - m2_use);  // 1 if unchanged, 0 on the first tile
 
       // Rescale O_t by alpha.  S_t(j) complete implies P_t(j-1) V done (one issuing
-      // thread, completion tracked in order), so O_t is stable here.
-      if (j > 0 && __any_sync(0xffffffffu, m2_use != m2)) {
+      // thread, completion tracked in order), so O_t is stable here.  (With three S
+      // buffers that does not hold; the rescale then comes after the exponentials.)
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, m2_use != m2);
+      if (!Cfg::kTripleS && rescale) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -360,6 +426,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       f2_unpack(acc[2], a4, a5);
       f2_unpack(acc[3], a6, a7);
       l = l * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
+      if constexpr (Cfg::kTripleS) {
+        if (rescale) {
+          // S_t(j) may have finished before P_t(j-1) V: wait for that product (the
+          // barrier has completed j-1 or j phases here, so the parity wait is
+          // unambiguous), then rescale O_t before P_t(j) V is issued.
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[t]), (j - 1) & 1,
+                                                 abort, p.status));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_wait(tO + 32 * c, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + 32 * c, o);
+          }
+        }
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
