@@ -169,7 +169,8 @@ fa_status online_softmax_forward(const float* x, float* y, float* m_out, float* 
                                  int rows, int len, cudaStream_t stream);
 
 /*
- * Attention backward (bf16 or fp16, d = 64 or 128): the gradients dQ, dK, dV of the
+ * Attention backward (bf16 or fp16 with d = 64 or 128 on the tensor cores; fp32 with any
+ * d in 1..128 on CUDA cores): the gradients dQ, dK, dV of the
  * forward above for an upstream gradient dO.  "Softmax 数值稳定性与 IO-Aware Attention"
  * §7.2: only per-row statistics of the forward are kept (here LSE) and the scores are
  * recomputed tile by tile, never stored.  With P = exp(scale Q K^T - LSE):
@@ -184,7 +185,8 @@ fa_status online_softmax_forward(const float* x, float* y, float* m_out, float* 
  *   workspace           caller-owned device scratch of at least
  *                       fa_bwd_workspace_bytes(B, H, N) bytes (fp32 LSE*log2(e) and D
  *                       per query row); its contents are overwritten
- * Alignment: every pointer but lse 16 bytes, lse 4.  B*H*N == 0 is a no-op (FA_OK).
+ * Alignment: bf16/fp16: every pointer but lse 16 bytes, lse 4; fp32: 4 bytes, the
+ * workspace 16.  B*H*N == 0 is a no-op (FA_OK).
  * Every output element is written exactly once by one block (no atomics), so results
  * are deterministic.  Errors: FA_ERR_INVALID (null pointer, lse missing, negative size,
  * scale not finite and > 0, causal not 0/1, workspace too small), FA_ERR_UNSUPPORTED

@@ -11,6 +11,7 @@
 #include "attn_bwd.cuh"
 #include "fa.h"
 #include "host_util.h"
+#include "kernels.h"
 
 namespace osfa {
 namespace {
@@ -39,21 +40,32 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID;
-  if (dtype != FA_BF16 && dtype != FA_F16) return FA_ERR_UNSUPPORTED;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_BF16 && dtype != FA_F16 && dtype != FA_F32) return FA_ERR_UNSUPPORTED;
+  const bool f32 = dtype == FA_F32;
+  if (f32 ? (d < 1 || d > 128) : (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > INT_MAX) return FA_ERR_INVALID;
   if (BH == 0 || N == 0) return FA_OK;
-  const void* ptrs16[] = {q, k, v, o, dout, dq, dk, dv, workspace};
-  for (const void* ptr : ptrs16)
+  const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs)
     if (ptr == nullptr) return FA_ERR_INVALID;
   if (lse == nullptr) return FA_ERR_INVALID;
-  for (const void* ptr : ptrs16)
-    if (!aligned(ptr, 16)) return FA_ERR_ALIGN;
-  if (!aligned(lse, 4)) return FA_ERR_ALIGN;
+  for (const void* ptr : ptrs)
+    if (!aligned(ptr, f32 ? 4 : 16)) return FA_ERR_ALIGN;
+  if (!aligned(lse, 4) || !aligned(workspace, 16)) return FA_ERR_ALIGN;
   if (workspace_bytes < static_cast<size_t>(bwd_ws_bytes(BH, N))) return FA_ERR_INVALID;
   const long long nblk = bwd_n_pad(N) / kBlockM;
   if (nblk * BH > INT_MAX) return FA_ERR_INVALID;
+  if (f32) {
+    // CUDA cores, warp per row: D (fp32, first B*H*N floats of the workspace), then the
+    // key pass and the query pass.
+    if ((BH * N + 3) / 4 > INT_MAX) return FA_ERR_INVALID;
+    return from_cuda(launch_attn_bwd_f32(
+        static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+        static_cast<const float*>(o), lse, static_cast<const float*>(dout),
+        static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv),
+        static_cast<float*>(workspace), static_cast<int>(BH), N, d, scale, causal, stream));
+  }
 
   unsigned* status = nullptr;
   cudaError_t e = status_word(&status);

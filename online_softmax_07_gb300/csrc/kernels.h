@@ -9,6 +9,11 @@ namespace osfa {
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                             int BH, int N, int d, float scale, int causal, cudaStream_t stream);
 
+cudaError_t launch_attn_bwd_f32(const float* q, const float* k, const float* v, const float* o,
+                                const float* lse, const float* dout, float* dq, float* dk,
+                                float* dv, float* dd, int BH, int N, int d, float scale,
+                                int causal, cudaStream_t stream);
+
 cudaError_t launch_row_state(const float* x, float* m_out, float* l_out, int rows, int len,
                              cudaStream_t stream);
 

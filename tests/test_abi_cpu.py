@@ -150,7 +150,11 @@ def test_bwd_workspace_size(lib):
     (dict(B=0), abi.FA_OK),                       # empty problems launch nothing
     (dict(N=0, q=None), abi.FA_OK),
     (dict(d=96), abi.FA_ERR_UNSUPPORTED),
-    (dict(dtype=abi.FA_F32), abi.FA_ERR_UNSUPPORTED),
+    (dict(dtype=7), abi.FA_ERR_UNSUPPORTED),
+    (dict(dtype=abi.FA_F32, d=129), abi.FA_ERR_UNSUPPORTED),
+    (dict(dtype=abi.FA_F32, d=0), abi.FA_ERR_UNSUPPORTED),
+    (dict(dtype=abi.FA_F32, d=17, dq=FAKE + 2), abi.FA_ERR_ALIGN),
+    (dict(dtype=abi.FA_F32, d=17, ws=FAKE + 4), abi.FA_ERR_ALIGN),
     (dict(scale=0.0), abi.FA_ERR_INVALID),
     (dict(causal=3), abi.FA_ERR_INVALID),
     (dict(lse=None), abi.FA_ERR_INVALID),         # the backward needs the forward's LSE

@@ -9,7 +9,9 @@ and the outputs.  Over many terms the errors are independent, so the relative RM
 error of each gradient tensor should be a few times 2^-9 / sqrt(1) ~ 2e-3..4e-3;
 the gate is 1e-2 on ||g - g_ref|| / ||g_ref|| and 2e-2 * max|g_ref| on the largest
 element error (the forward's 2e-2 on O, taken relative to the gradient's scale).
-fp16 rounds with 2^-11 and gets the same gates.
+fp16 rounds with 2^-11 and gets the same gates.  fp32 (CUDA cores, no 16-bit rounding):
+unit roundoff 6e-8, dot products of <= 128 terms and sums over <= a few hundred keys keep
+the relative error near 1e-6; gates 1e-5 relative RMS and 1e-4 * max|g_ref|.
 """
 
 import numpy as np
@@ -29,8 +31,8 @@ MAX_REL = 2e-2
 def _run_bwd(q, k, v, do, scale, causal, dtype="bf16"):
     """fa_fwd_dt then fa_bwd through the C ABI; returns numpy fp32 dq, dk, dv."""
     import torch
-    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
-    code = {"bf16": abi.FA_BF16, "f16": abi.FA_F16}[dtype]
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
+    code = {"bf16": abi.FA_BF16, "f16": abi.FA_F16, "f32": abi.FA_F32}[dtype]
     B, H, N, d = q.shape
     tq, tk, tv, tdo = (to_device(x, tdt) for x in (q, k, v, do))
     o = torch.empty_like(tq)
@@ -50,14 +52,16 @@ def _inputs(B, H, N, d, seed, dtype="bf16"):
     return q, k, v, do
 
 
-def _check(name, got, ref):
+def _check(name, got, ref, rel_rms_gate=None, max_rel_gate=None):
+    rel_rms_gate = REL_RMS if rel_rms_gate is None else rel_rms_gate
+    max_rel_gate = MAX_REL if max_rel_gate is None else max_rel_gate
     got = got.astype(np.float64)
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
     err = got - ref
     scale = np.abs(ref).max()
     rel_rms = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-30)
-    assert rel_rms <= REL_RMS, f"{name}: relative RMS error {rel_rms:.3e}"
-    assert np.abs(err).max() <= MAX_REL * scale, (
+    assert rel_rms <= rel_rms_gate, f"{name}: relative RMS error {rel_rms:.3e}"
+    assert np.abs(err).max() <= max_rel_gate * scale, (
         f"{name}: max error {np.abs(err).max():.3e} vs max |ref| {scale:.3e}")
     return rel_rms
 
@@ -128,3 +132,23 @@ def test_backward_workload_sampled(B, H, N, d, causal, n_sample):
     assert np.abs(dv_sum - do_sum).max() <= 1e-2 * np.abs(dv).sum(axis=2).max()
     dk_sum = np.abs(dk.astype(np.float64).sum(axis=2))
     assert (dk_sum <= 1e-2 * np.abs(dk.astype(np.float64)).sum(axis=2)).all()
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [
+    (1, 1, 128, 64, False),   # the fp32 configuration
+    (1, 1, 128, 64, True),
+    (2, 2, 100, 17, True),
+    (1, 2, 257, 128, False),
+    (1, 1, 1, 1, False),
+    (1, 3, 70, 1, True),
+])
+def test_backward_f32(B, H, N, d, causal):
+    q, k, v, do = _inputs(B, H, N, d, seed=1900 + N + d, dtype="f32")
+    scale = 1.0 / np.sqrt(d)
+    dq, dk, dv = _run_bwd(q, k, v, do, scale, causal, dtype="f32")
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, scale, causal)
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        if np.abs(r).max() == 0:          # N = 1: dQ = dK = 0 exactly
+            assert np.abs(g).max() < 1e-6
+            continue
+        _check(name, g, r, rel_rms_gate=1e-5, max_rel_gate=1e-4)
