@@ -50,8 +50,12 @@ struct AttnBwdCfg {
   static constexpr int kSmemStages = 2 * kTileBytes;
   static constexpr int kSmemBars = kSmemStages + kStages * kStageBytes;
   static constexpr int kSmemBytes = kSmemBars + 512 + 1024;  // + barriers + alignment slack
-  // TMEM columns: S (or S^T), dP (or dP^T), then one or two fp32 accumulators.
+  // TMEM columns: S (or S^T), dP (or dP^T), then one or two fp32 accumulators.  At
+  // d = 64 these take 384 columns and a second S^T buffer (key-outer pass) or dP buffer
+  // (query-outer pass) fits at kColX (kDouble).
+  static constexpr bool kDouble = (D == 64);
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+  static constexpr uint32_t kColX = 384;
   static constexpr uint32_t kTmemCols = 512;
 };
 

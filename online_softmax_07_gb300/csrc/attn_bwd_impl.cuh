@@ -11,10 +11,12 @@ namespace osfa {
 
 struct AttnBwdBarriers {
   uint64_t fixed_full;   // TMA -> all: the two resident tiles are in shared memory
-  uint64_t s_full;       // MMA -> element-wise: S (or S^T) of the current tile pair in TMEM
-  uint64_t dp_full;      // MMA -> element-wise: dP (or dP^T) in TMEM
-  uint64_t p_done;       // element-wise -> MMA: P^T stored (key-outer) / S read (query-outer)
-  uint64_t ds_ready;     // element-wise -> MMA: dS (or dS^T) stored in TMEM
+  // With one S (dP) buffer only index 0 of these is used; with two (d = 64), index b
+  // belongs to buffer b (s_full, dp_full) or to tile pairs of parity b (p_done, ds_ready).
+  uint64_t s_full[2];    // MMA -> element-wise: S (or S^T) of a tile pair in TMEM
+  uint64_t dp_full[2];   // MMA -> element-wise: dP (or dP^T) in TMEM
+  uint64_t p_done[2];    // element-wise -> MMA: P^T stored (key-outer) / S read (query-outer)
+  uint64_t ds_ready[2];  // element-wise -> MMA: dS (or dS^T) stored in TMEM
   uint64_t acc_final;    // MMA -> element-wise: the last accumulation finished
   uint64_t mma_drain;    // MMA warp: all of its MMAs finished (before TMEM is freed)
   uint64_t stage_full[4];
@@ -168,10 +170,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->fixed_full), 1);
-    mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->dp_full), 1);
-    mbar_init(smem_u32(&bars->p_done), 8);    // one arrival per element-wise warp
-    mbar_init(smem_u32(&bars->ds_ready), 8);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->s_full[b]), 1);
+      mbar_init(smem_u32(&bars->dp_full[b]), 1);
+      mbar_init(smem_u32(&bars->p_done[b]), 8);    // one arrival per element-wise warp
+      mbar_init(smem_u32(&bars->ds_ready[b]), 8);
+    }
     mbar_init(smem_u32(&bars->acc_final), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
     for (int s = 0; s < Cfg::kStages; ++s) {
@@ -280,30 +284,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Each TMEM region is overwritten only after the product that reads it (one issuing
     // thread: products complete in issue order).
     bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0);
+    if constexpr (Cfg::kDouble) {
+      // Two S^T buffers (d = 64): S^T(it) in buffer it % 2, so S^T(it+2) is issued right
+      // after dV(it) has consumed P^T(it) and the element-wise warps never wait for their
+      // next S^T on this chain.  Order per query tile it:
+      //   dV(it)  |  S^T(it+2)  |  dK(it)  |  dP^T(it+1)
+      // p_done alternates between two barriers: the element-wise warps may finish P^T(it+1)
+      // before this warp has taken P^T(it).
+      auto colS = [&](int i) { return tbase + ((i & 1) ? Cfg::kColX : Cfg::kColS); };
+      if (ok) {
+        issue_t(colS(0), dK, desc_k(0, 0));
+        mma_commit_elect(smem_u32(&bars->s_full[0]));
+        issue_t(tDP, dV, desc_k(0, 1));
+        mma_commit_elect(smem_u32(&bars->dp_full[0]));
+        if (nq > 1 && (ok = wait_bar(&bars->stage_full[1 % Cfg::kStages], (1 / Cfg::kStages) & 1))) {
+          issue_t(colS(1), dK, desc_k(1, 0));
+          mma_commit_elect(smem_u32(&bars->s_full[1]));
+        }
+      }
+      for (int it = 0; ok && it < nq; ++it) {
+        if (!(ok = wait_bar(&bars->p_done[it & 1], (it >> 1) & 1))) break;
+        issue_acc(tDV, colS(it), desc_mn(it, 1), it > 0);
+        if (it + 2 < nq) {
+          if (!(ok = wait_bar(&bars->stage_full[(it + 2) % Cfg::kStages],
+                              ((it + 2) / Cfg::kStages) & 1)))
+            break;
+          issue_t(colS(it), dK, desc_k(it + 2, 0));
+          mma_commit_elect(smem_u32(&bars->s_full[it & 1]));
+        }
+        if (!(ok = wait_bar(&bars->ds_ready[0], it & 1))) break;
+        issue_acc(tDK, tDP, desc_mn(it, 0), it > 0);
+        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
+        if (it + 1 < nq) {
+          issue_t(tDP, dV, desc_k(it + 1, 1));
+          mma_commit_elect(smem_u32(&bars->dp_full[0]));
+        }
+      }
+    } else {
     if (ok) {
       issue_t(tS, dK, desc_k(0, 0));
-      mma_commit_elect(smem_u32(&bars->s_full));
+      mma_commit_elect(smem_u32(&bars->s_full[0]));
       issue_t(tDP, dV, desc_k(0, 1));
-      mma_commit_elect(smem_u32(&bars->dp_full));
+      mma_commit_elect(smem_u32(&bars->dp_full[0]));
     }
     for (int it = 0; ok && it < nq; ++it) {
       const bool more = it + 1 < nq;
-      if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
+      if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
       issue_acc(tDV, tS, desc_mn(it, 1), it > 0);
       if (more) {
         if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
                             ((it + 1) / Cfg::kStages) & 1)))
           break;
         issue_t(tS, dK, desc_k(it + 1, 0));
-        mma_commit_elect(smem_u32(&bars->s_full));
+        mma_commit_elect(smem_u32(&bars->s_full[0]));
       }
-      if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
+      if (!(ok = wait_bar(&bars->ds_ready[0], it & 1))) break;
       issue_acc(tDK, tDP, desc_mn(it, 0), it > 0);
       mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
       if (more) {
         issue_t(tDP, dV, desc_k(it + 1, 1));
-        mma_commit_elect(smem_u32(&bars->dp_full));
+        mma_commit_elect(smem_u32(&bars->dp_full[0]));
       }
+    }
     }
     if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
     mma_commit_elect(smem_u32(&bars->mma_drain));
@@ -321,7 +363,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     for (int it = 0; it < nq; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
+      // S^T of this query tile: buffer it % 2 with two buffers (barrier phase it / 2).
+      const uint32_t tSb = Cfg::kDouble && (it & 1) ? tbase + lane_off + Cfg::kColX : tS;
+      ok = __all_sync(0xffffffffu,
+                      Cfg::kDouble
+                          ? mbar_wait(smem_u32(&bars->s_full[it & 1]), (it >> 1) & 1, abort, p.status)
+                          : mbar_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
       if (!ok) break;
       // The statistics came in by TMA with the stage; wait on the stage's own barrier
       // (complete already: S^T of this stage is done) to see them.
@@ -342,7 +389,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * h + 32 * ch;    // first query (column) of this chunk
         uint32_t sr[32];
-        tmem_ld32_wait(tS + c0, sr);
+        tmem_ld32_wait(tSb + c0, sr);
         const float4* l4 = reinterpret_cast<const float4*>(lse2s + c0);
         uint32_t pk[16];
 #pragma unroll
@@ -365,15 +412,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pk[c >> 1] = pack_elem2<F16>(p0, p1);
           }
         }
-        tmem_st16(tS + 64 * h + 16 * ch, pk);
+        tmem_st16(tSb + 64 * h + 16 * ch, pk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_done[Cfg::kDouble ? (it & 1) : 0]));
 
       // dS^T = P^T * (dP^T - D), stored over the first half of this warp's dP^T columns.
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -403,7 +450,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready[0]));
     }
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
@@ -457,10 +504,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->fixed_full), 1);
-    mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->dp_full), 1);
-    mbar_init(smem_u32(&bars->p_done), 8);    // one arrival per element-wise warp
-    mbar_init(smem_u32(&bars->ds_ready), 8);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->s_full[b]), 1);
+      mbar_init(smem_u32(&bars->dp_full[b]), 1);
+      mbar_init(smem_u32(&bars->p_done[b]), 8);    // one arrival per element-wise warp
+      mbar_init(smem_u32(&bars->ds_ready[b]), 8);
+    }
     mbar_init(smem_u32(&bars->acc_final), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
     for (int s = 0; s < Cfg::kStages; ++s) {
@@ -546,35 +595,71 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //   dQ += dS(it) K_it (dS stored over dP(it))  |  dP(it+1)
     // so the next S is computed while dS(it) is being formed.
     bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0);
-    if (ok) {
-      issue_n(tS, dQ, stage_desc(0, 0, 16));
-      mma_commit_elect(smem_u32(&bars->s_full));
-      issue_n(tDP, dDO, stage_desc(0, 1, 16));
-      mma_commit_elect(smem_u32(&bars->dp_full));
-    }
-    for (int it = 0; ok && it < nk; ++it) {
-      const bool more = it + 1 < nk;
-      if (more) {
-        if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
-        if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
-                            ((it + 1) / Cfg::kStages) & 1)))
-          break;
-        issue_n(tS, dQ, stage_desc(it + 1, 0, 16));
-        mma_commit_elect(smem_u32(&bars->s_full));
+    if constexpr (Cfg::kDouble) {
+      // Two dP buffers (d = 64): dP(it) and dS(it) in buffer it % 2, so dP(it+1) is issued
+      // together with S(it+1) instead of after dQ(it).  Order per key tile it:
+      //   S(it+1), dP(it+1) (once S(it) is in registers)  |  dQ += dS(it) K_it
+      // ds_ready alternates between two barriers: the element-wise warps may finish dS(it+1)
+      // before this warp has taken dS(it).
+      auto colDP = [&](int i) { return tbase + ((i & 1) ? Cfg::kColX : Cfg::kColDP); };
+      if (ok) {
+        issue_n(tS, dQ, stage_desc(0, 0, 16));
+        mma_commit_elect(smem_u32(&bars->s_full[0]));
+        issue_n(colDP(0), dDO, stage_desc(0, 1, 16));
+        mma_commit_elect(smem_u32(&bars->dp_full[0]));
       }
-      if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
-      // dQ += dS K_j: dS (16 keys = 8 packed columns per step) from the dP columns.
-      const uint64_t dKmn = stage_desc(it, 0, kBoxBytes);
+      for (int it = 0; ok && it < nk; ++it) {
+        if (it + 1 < nk) {
+          if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
+          if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
+                              ((it + 1) / Cfg::kStages) & 1)))
+            break;
+          issue_n(tS, dQ, stage_desc(it + 1, 0, 16));
+          mma_commit_elect(smem_u32(&bars->s_full[0]));
+          issue_n(colDP(it + 1), dDO, stage_desc(it + 1, 1, 16));
+          mma_commit_elect(smem_u32(&bars->dp_full[(it + 1) & 1]));
+        }
+        if (!(ok = wait_bar(&bars->ds_ready[it & 1], (it >> 1) & 1))) break;
+        const uint64_t dKmn = stage_desc(it, 0, kBoxBytes);
 #pragma unroll
-      for (int kk = 0; kk < kBlockM / 16; ++kk) {
-        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
-        mma_bf16_ts_elect(tDQ, tDP + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
-                          (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBlockM / 16; ++kk) {
+          const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+          mma_bf16_ts_elect(tDQ, colDP(it) + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
+                            (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
       }
-      mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
-      if (more) {
-        issue_n(tDP, dDO, stage_desc(it + 1, 1, 16));
-        mma_commit_elect(smem_u32(&bars->dp_full));
+    } else {
+      if (ok) {
+        issue_n(tS, dQ, stage_desc(0, 0, 16));
+        mma_commit_elect(smem_u32(&bars->s_full[0]));
+        issue_n(tDP, dDO, stage_desc(0, 1, 16));
+        mma_commit_elect(smem_u32(&bars->dp_full[0]));
+      }
+      for (int it = 0; ok && it < nk; ++it) {
+        const bool more = it + 1 < nk;
+        if (more) {
+          if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
+          if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
+                              ((it + 1) / Cfg::kStages) & 1)))
+            break;
+          issue_n(tS, dQ, stage_desc(it + 1, 0, 16));
+          mma_commit_elect(smem_u32(&bars->s_full[0]));
+        }
+        if (!(ok = wait_bar(&bars->ds_ready[0], it & 1))) break;
+        // dQ += dS K_j: dS (16 keys = 8 packed columns per step) from the dP columns.
+        const uint64_t dKmn = stage_desc(it, 0, kBoxBytes);
+  #pragma unroll
+        for (int kk = 0; kk < kBlockM / 16; ++kk) {
+          const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+          mma_bf16_ts_elect(tDQ, tDP + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
+                            (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
+        if (more) {
+          issue_n(tDP, dDO, stage_desc(it + 1, 1, 16));
+          mma_commit_elect(smem_u32(&bars->dp_full[0]));
+        }
       }
     }
     if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
@@ -598,7 +683,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t negl2 = f2_pack(-lse2, -lse2);
     const uint64_t negd2 = f2_pack(-dd, -dd);
     for (int it = 0; it < nk; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
       const int key0 = it * kBlockM;
@@ -630,17 +715,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (it + 1 < nk) {  // S(it) is in registers: the next S may overwrite it
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_done[0]));
       }
-      // dS = P * (dP - D), stored (16-bit) over the first half of this warp's dP columns.
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
+      // dS = P * (dP - D), stored (16-bit) over the first half of this warp's dP columns
+      // (dP of this key tile: buffer it % 2 with two buffers, barrier phase it / 2).
+      const uint32_t tDPb = Cfg::kDouble && (it & 1) ? tbase + lane_off + Cfg::kColX : tDP;
+      ok = __all_sync(0xffffffffu,
+                      Cfg::kDouble
+                          ? mbar_wait(smem_u32(&bars->dp_full[it & 1]), (it >> 1) & 1, abort, p.status)
+                          : mbar_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * h + 32 * ch;
         uint32_t dr[32];
-        tmem_ld32_wait(tDP + c0, dr);
+        tmem_ld32_wait(tDPb + c0, dr);
         uint32_t pd[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
@@ -651,12 +741,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           f2_unpack(ds, d0, d1);
           pd[c >> 1] = pack_elem2<F16>(d0, d1);
         }
-        tmem_st16(tDP + 64 * h + 16 * ch, pd);
+        tmem_st16(tDPb + 64 * h + 16 * ch, pd);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready[Cfg::kDouble ? (it & 1) : 0]));
     }
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
