@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_store_3d(&tm_o, smem_u32(stage + b * kBoxBytes), b * kBoxCols, r0, bh);
         bulk_commit_group();
-        bulk_wait_group_0();
+        bulk_wait_group_read_0();  // staging read: the block may exit
       }
     }
   }

@@ -109,6 +109,13 @@ __device__ __forceinline__ void bulk_wait_group_0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Waits until every committed bulk copy of this thread has finished READING its source
+// (shared memory may then be reused or released); the writes complete asynchronously,
+// before the kernel is complete.
+__device__ __forceinline__ void bulk_wait_group_read_0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // (TMA store) reads of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -152,3 +152,50 @@ def test_backward_f32(B, H, N, d, causal):
             assert np.abs(g).max() < 1e-6
             continue
         _check(name, g, r, rel_rms_gate=1e-5, max_rel_gate=1e-4)
+
+
+def test_backward_noncausal_d128_sampled():
+    B, H, N, d = 1, 4, 4096, 128
+    q, k, v, do = _inputs(B, H, N, d, seed=2100)
+    scale = 1.0 / np.sqrt(d)
+    dq, dk, dv = _run_bwd(q, k, v, do, scale, False)
+    rows = sample_rows(N, 40, seed=2101)
+    for bh in ((0, 1), (0, 3)):
+        rq, rk, rv = oracle.attention_backward_rows(q, k, v, do, scale, False, bh, rows, rows)
+        b, h = bh
+        _check("dQ", dq[b, h, rows], rq)
+        _check("dK", dk[b, h, rows], rk)
+        _check("dV", dv[b, h, rows], rv)
+
+
+def test_backward_from_splitkv_forward():
+    """fa_bwd takes O and LSE from the split-KV forward as well (same LSE convention):
+    the gradients agree with those from the plain forward's O and LSE."""
+    import torch
+    B, H, N, d = 1, 2, 3000, 128
+    q, k, v, do = _inputs(B, H, N, d, seed=2200)
+    scale = 1.0 / np.sqrt(d)
+    tq, tk, tv, tdo = (to_device(x, torch.bfloat16) for x in (q, k, v, do))
+    grads = []
+    for splits in (1, 4):
+        o = torch.empty_like(tq)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        if splits == 1:
+            abi.fa_fwd(tq, tk, tv, o, lse, B, H, N, d, scale, 1)
+        else:
+            nbytes = abi.fa_fwd_splitkv_workspace_bytes(B, H, N, d, splits)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+            abi.fa_fwd_splitkv(tq, tk, tv, o, lse, B, H, N, d, scale, 1, splits, ws, nbytes,
+                               abi.FA_BF16)
+        nb = abi.fa_bwd_workspace_bytes(B, H, N)
+        wsb = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        outs = [torch.empty_like(tq) for _ in range(3)]
+        abi.fa_bwd(tq, tk, tv, o, lse, tdo, *outs, B, H, N, d, scale, 1, wsb, nb, abi.FA_BF16)
+        assert abi.fa_last_device_error() == abi.FA_OK
+        grads.append([t.float().cpu().numpy() for t in outs])
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, scale, True)
+    for (name, r), g1, g4 in zip((("dQ", rq), ("dK", rk), ("dV", rv)), grads[0], grads[1]):
+        _check(name, g1, r)
+        _check(name, g4, r)
+        # the two differ only through the rounding of O and LSE
+        assert np.linalg.norm(g1 - g4) <= 5e-3 * np.linalg.norm(r), name
