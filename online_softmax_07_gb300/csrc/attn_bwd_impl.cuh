@@ -362,19 +362,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    for (int it = 0; it < nq; ++it) {
+    // The statistics of query tile it come in by TMA with its stage; the warps wait on the
+    // stage's own barrier to see them, for tile it+1 at the end of tile it (off the path
+    // from S^T to P^T; the stage is refilled only after these warps are done with it).
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->stage_full[0]), 0, abort, p.status));
+    for (int it = 0; ok && it < nq; ++it) {
       // S^T of this query tile: buffer it % 2 with two buffers (barrier phase it / 2).
       const uint32_t tSb = Cfg::kDouble && (it & 1) ? tbase + lane_off + Cfg::kColX : tS;
       ok = __all_sync(0xffffffffu,
                       Cfg::kDouble
                           ? mbar_wait(smem_u32(&bars->s_full[it & 1]), (it >> 1) & 1, abort, p.status)
                           : mbar_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
-      if (!ok) break;
-      // The statistics came in by TMA with the stage; wait on the stage's own barrier
-      // (complete already: S^T of this stage is done) to see them.
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]),
-                                (it / Cfg::kStages) & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
       const int i = i0 + it;
@@ -451,6 +449,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready[0]));
+      if (it + 1 < nq)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&bars->stage_full[(it + 1) % Cfg::kStages]),
+                                  ((it + 1) / Cfg::kStages) & 1, abort, p.status));
     }
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
