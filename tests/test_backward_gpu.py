@@ -91,10 +91,23 @@ def test_backward_single_key():
     assert np.abs(dq).max() < 1e-3 and np.abs(dk).max() < 1e-3
 
 
-def test_backward_f16():
-    q, k, v, do = _inputs(1, 2, 200, 128, seed=960, dtype="f16")
-    dq, dk, dv = _run_bwd(q, k, v, do, 1.0 / np.sqrt(128), True, dtype="f16")
-    rq, rk, rv = oracle.attention_backward(q, k, v, do, 1.0 / np.sqrt(128), True)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_f16(d, causal):
+    q, k, v, do = _inputs(1, 2, 200, d, seed=960 + d, dtype="f16")
+    dq, dk, dv = _run_bwd(q, k, v, do, 1.0 / np.sqrt(d), causal, dtype="f16")
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, 1.0 / np.sqrt(d), causal)
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        _check(name, g, r)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_large_logits(d):
+    """Q with standard deviation 4: peaky probability rows (few keys carry the weight)."""
+    q, k, v = synth.attention_inputs(1, 2, 700, d, seed=965 + d, q_std=4.0)
+    do = synth.attention_inputs(1, 2, 700, d, seed=966 + d)[0]
+    dq, dk, dv = _run_bwd(q, k, v, do, 1.0 / np.sqrt(d), True)
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, 1.0 / np.sqrt(d), True)
     for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
         _check(name, g, r)
 
