@@ -10,8 +10,14 @@ namespace osfa {
 
 struct AttnTcBarriers {
   uint64_t q_full;
-  uint64_t s_full[2];    // MMA -> softmax t: S_t of the current K/V tile is in TMEM
-  uint64_t p_ready[2];   // softmax t -> MMA: P_t stored in TMEM and O_t rescaled
+  // s_full and p_ready come in pairs per tile, used alternately: S_t(j) completes on
+  // s_full[2 t + (j & 1)] and is waited with parity (j >> 1) & 1, P_t(j) likewise on
+  // p_ready.  With three S buffers the MMA warp issues S_t(j+1) before it needs P_t(j),
+  // so two S_t completions can be pending at once; on a single barrier the second would
+  // hide the first from a parity wait if the softmax warps fell behind.  On alternating
+  // barriers neither side can get two phases ahead of the other.
+  uint64_t s_full[4];    // MMA -> softmax t: S_t of a K/V tile is in TMEM
+  uint64_t p_ready[4];   // softmax t -> MMA: P_t stored in TMEM and O_t rescaled
   uint64_t o_final[2];   // MMA -> softmax t: last P_t V product done
   uint64_t pv_done[2];   // MMA -> softmax t: P_t V of a K/V tile done (three-buffer mode)
   uint64_t mma_drain;    // MMA thread: all of its MMAs finished (before TMEM is freed)
@@ -118,8 +124,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->q_full), 1);
     for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&bars->s_full[t]), 1);
-      mbar_init(smem_u32(&bars->p_ready[t]), 4);  // one arrival per softmax warp
+      for (int u = 0; u < 2; ++u) {
+        mbar_init(smem_u32(&bars->s_full[2 * t + u]), 1);
+        mbar_init(smem_u32(&bars->p_ready[2 * t + u]), 4);  // one arrival per softmax warp
+      }
       mbar_init(smem_u32(&bars->o_final[t]), 1);
       mbar_init(smem_u32(&bars->pv_done[t]), 1);
     }
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mma_commit_elect(smem_u32(&bars->s_full[0]));
         }
         issue_s(colS(n0 > 0 ? 1 : 0), dQ1, 0);
-        mma_commit_elect(smem_u32(&bars->s_full[1]));
+        mma_commit_elect(smem_u32(&bars->s_full[2]));
         mma_commit_elect(smem_u32(&bars->slot_empty[0]));
       }
       for (int j = 0; ok && j < n1; ++j) {
@@ -261,9 +269,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             k_ready = true;
             tc_fence_after();
             issue_s(colS(2 * j + 2), dQ0, itK);
-            mma_commit_elect(smem_u32(&bars->s_full[0]));
+            mma_commit_elect(smem_u32(&bars->s_full[(j + 1) & 1]));
           }
-          if (!(ok = wait_bar(&bars->p_ready[0], j & 1))) break;
+          if (!(ok = wait_bar(&bars->p_ready[j & 1], (j >> 1) & 1))) break;
           issue_pv(tO0, colS(2 * j), itV, j > 0);
           mma_commit_elect(smem_u32(&bars->pv_done[0]));
           if (j + 1 == n0) mma_commit_elect(smem_u32(&bars->o_final[0]));
@@ -274,10 +282,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
           }
           issue_s(colS(min(j + 2, n0) + j + 1), dQ1, itK);
-          mma_commit_elect(smem_u32(&bars->s_full[1]));
+          mma_commit_elect(smem_u32(&bars->s_full[2 + ((j + 1) & 1)]));
           mma_commit_elect(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
         }
-        if (!(ok = wait_bar(&bars->p_ready[1], j & 1))) break;
+        if (!(ok = wait_bar(&bars->p_ready[2 + (j & 1)], (j >> 1) & 1))) break;
         issue_pv(tO1, colS(min(j + 1, n0) + j), itV, j > 0);
         mma_commit_elect(smem_u32(&bars->pv_done[1]));
         mma_commit_elect(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
@@ -291,7 +299,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mma_commit_elect(smem_u32(&bars->s_full[0]));
         }
         issue_s(tS1, dQ1, 0);
-        mma_commit_elect(smem_u32(&bars->s_full[1]));
+        mma_commit_elect(smem_u32(&bars->s_full[2]));
         mma_commit_elect(smem_u32(&bars->slot_empty[0]));
       }
       for (int j = 0; ok && j < n1; ++j) {
@@ -299,7 +307,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!(ok = __all_sync(0xffffffffu, wait_full(itV)))) break;
         if (j < n0) {
           if (!(ok = __all_sync(0xffffffffu,
-                                mbar_wait(smem_u32(&bars->p_ready[0]), j & 1, abort, p.status))))
+                                mbar_wait(smem_u32(&bars->p_ready[j & 1]), (j >> 1) & 1, abort,
+                                          p.status))))
             break;
           tc_fence_after();
           issue_pv(tO0, tS0, itV, j > 0);
@@ -307,13 +316,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
             tc_fence_after();
             issue_s(tS0, dQ0, itK);
-            mma_commit_elect(smem_u32(&bars->s_full[0]));
+            mma_commit_elect(smem_u32(&bars->s_full[(j + 1) & 1]));
           } else {
             mma_commit_elect(smem_u32(&bars->o_final[0]));
           }
         }
         if (!(ok = __all_sync(0xffffffffu,
-                              mbar_wait(smem_u32(&bars->p_ready[1]), j & 1, abort, p.status))))
+                              mbar_wait(smem_u32(&bars->p_ready[2 + (j & 1)]), (j >> 1) & 1,
+                                        abort, p.status))))
           break;
         tc_fence_after();
         issue_pv(tO1, tS1, itV, j > 0);
@@ -322,7 +332,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
           tc_fence_after();
           issue_s(tS1, dQ1, itK);
-          mma_commit_elect(smem_u32(&bars->s_full[1]));
+          mma_commit_elect(smem_u32(&bars->s_full[2 + ((j + 1) & 1)]));
           mma_commit_elect(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
         } else {
           mma_commit_elect(smem_u32(&bars->o_final[1]));
@@ -351,7 +361,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     const int nbt = t ? n1 : n0;
     for (int j = 0; j < nbt; ++j) {
-      ok = mbar_wait(smem_u32(&bars->s_full[t]), j & 1, abort, p.status);
+      ok = mbar_wait(smem_u32(&bars->s_full[2 * t + (j & 1)]), (j >> 1) & 1, abort, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -448,7 +458,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready[t]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready[2 * t + (j & 1)]));
     }
 
     if (ok && nbt > 0) {

@@ -110,6 +110,31 @@ def test_f32_path(d, causal):
     check_attention(o, lse, o_ref, lse_ref, dtype="f32")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N", [(2, 160, 300), (1, 48, 1000)])
+def test_bf16_more_blocks_than_sms(B, H, N, d, causal):
+    """More blocks (256-row query blocks x heads) than SMs, so the launch runs in
+    several waves and each SM runs blocks back to back; (1, 48, 1000) mixes block
+    lengths (causal) and ragged last blocks.  Q std 2 makes the O rescale run.  Every
+    element compared; two launches must agree bit for bit."""
+    q, k, v = synth.attention_inputs(B, H, N, d, seed=73000 + H + N + d + int(causal),
+                                     q_std=2.0)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_attention(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, scale, causal)
+    check_attention(o, lse, o_ref, lse_ref)
+    o2, lse2 = run_attention(q, k, v, scale, causal)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+def test_f16_more_blocks_than_sms():
+    q, k, v = synth.attention_inputs(1, 200, 256, 64, seed=73900, dtype="f16", q_std=2.0)
+    o, lse = run_attention(q, k, v, 0.125, False, dtype="f16")
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, 0.125, False)
+    check_attention(o, lse, o_ref, lse_ref, dtype="f16")
+
+
 def test_workload_f32_b1h1n128d64():
     """fp32, B1 H1 N128 d64, scale 1/8, no mask: every element against the oracle;
     also the same inputs rounded to bf16 through the tensor-core kernel."""

@@ -50,6 +50,18 @@ def test_splitkv_all_rows(N, splits, d, causal):
     check_attention(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_splitkv_more_blocks_than_sms(d, causal):
+    """64 heads x 2 query blocks x 3 splits = 384 blocks, more than the SMs; some
+    partials are empty (causal early blocks)."""
+    q, k, v = synth.attention_inputs(1, 64, 500, d, seed=90500 + d + int(causal), q_std=2.0)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_splitkv(q, k, v, scale, causal, 3)
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, scale, causal)
+    check_attention(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref)
+
+
 def test_splitkv_f16():
     q, k, v = synth.attention_inputs(1, 1, 1500, 128, seed=91000, dtype="f16")
     o, lse = run_splitkv(q, k, v, 1 / math.sqrt(128), True, 4, dtype="f16")
