@@ -615,17 +615,17 @@ def suite(args):
         if name == "attn_bf16_b2h16n8192d128_causal":
             qh, kh, vh = (synth.round_to_f16(t) for t in (q, k, v))
             attn_line(name, qh, kh, vh, True, "f16", label=name.replace("bf16", "f16"))
-    # split-KV where the grid is small: B=1 H=2 N=32768 d=128 causal (256 query blocks)
-    q, k, v = synth.attention_inputs(1, 2, 32768, 128, seed=96000)
-    label = "attn_bf16_b1h2n32768d128_causal"
+    # split-KV where the grid is small: B=1 H=1 N=32768 d=128 causal (128 query blocks)
+    q, k, v = synth.attention_inputs(1, 1, 32768, 128, seed=96000)
+    label = "attn_bf16_b1h1n32768d128_causal"
     attn_line(label, q, k, v, True, "bf16", label=label + " (no split)")
-    s_def = abi.fa_fwd_splitkv_default_splits(1, 2, 32768)
+    s_def = abi.fa_fwd_splitkv_default_splits(1, 1, 32768, True)
     attn_line(label, q, k, v, True, "bf16", splits=s_def, label=label + " (split-KV)")
     # and where the grid is smaller still: B=1 H=1 N=16384 (64 query blocks)
     q, k, v = synth.attention_inputs(1, 1, 16384, 128, seed=96100)
     label = "attn_bf16_b1h1n16384d128_causal"
     attn_line(label, q, k, v, True, "bf16", label=label + " (no split)")
-    s_def = abi.fa_fwd_splitkv_default_splits(1, 1, 16384)
+    s_def = abi.fa_fwd_splitkv_default_splits(1, 1, 16384, True)
     attn_line(label, q, k, v, True, "bf16", splits=s_def, label=label + " (split-KV)")
     # backward (fa_bwd) on the attention workloads with a seeded dO of the same shape
     for name in ("attn_bf16_b4h16n4096d64", "attn_bf16_b2h16n8192d128_causal",

@@ -116,9 +116,15 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
  * (0 for invalid arguments).  Host-only, no CUDA call. */
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
 
-/* A split count for fa_fwd_splitkv on the current device: enough thread blocks for two
- * waves of its SMs, at least two K/V tiles per split, at most 64 (1 when no split pays). */
-int fa_fwd_splitkv_default_splits(int B, int H, int N);
+/* A split count for fa_fwd_splitkv on the current device (SM count from the runtime).
+ * Causal: the last query block needs about 2 SMs / blocks times the average work per SM
+ * (blocks = B * H * ceil(N/256)); the split count is that ratio rounded down after
+ * adding 0.2, so the longest pieces no longer set the time.  Not causal: blocks are of
+ * equal length and a split pays only while every piece still runs in the first wave,
+ * so SMs / blocks rounded down.  Then at least two K/V tiles per split, at most 64; 1
+ * when no split pays or for invalid arguments (causal not 0 or 1).  Host-only apart
+ * from reading the SM count. */
+int fa_fwd_splitkv_default_splits(int B, int H, int N, int causal);
 
 /*
  * Split-KV forward for callers that cannot allocate device memory (memory pools or arenas

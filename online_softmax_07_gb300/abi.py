@@ -34,7 +34,7 @@ _SIGNATURES = {
     "fa_fwd_splitkv_static": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p]
                               + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                                       ctypes.c_int, ctypes.c_void_p]),
-    "fa_fwd_splitkv_default_splits": (ctypes.c_int, [ctypes.c_int] * 3),
+    "fa_fwd_splitkv_default_splits": (ctypes.c_int, [ctypes.c_int] * 4),
     "fa_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 4
                + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
                   ctypes.c_void_p]),
@@ -141,8 +141,8 @@ def fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits) -> int:
     return int(load().fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits))
 
 
-def fa_fwd_splitkv_default_splits(B, H, N) -> int:
-    return int(load().fa_fwd_splitkv_default_splits(B, H, N))
+def fa_fwd_splitkv_default_splits(B, H, N, causal) -> int:
+    return int(load().fa_fwd_splitkv_default_splits(B, H, N, int(causal)))
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,

@@ -119,6 +119,21 @@ def test_splitkv_workspace_size(lib):
     assert abi.fa_fwd_splitkv_workspace_bytes(1, 1, 100, 64, 0) == 0      # no splits
 
 
+def test_splitkv_default_splits(lib):
+    """The split-count rule (the same answer with 148 or 152 SMs; without a GPU the
+    library assumes 148).  Query blocks = B * H * ceil(N / 256)."""
+    f = abi.fa_fwd_splitkv_default_splits
+    assert f(1, 1, 16384, True) == 4        # causal, 64 blocks: floor(2 * SMs / 64 + 0.2)
+    assert f(1, 1, 32768, True) == 2        # causal, 128 blocks
+    assert f(1, 5, 8192, True) == 2         # causal, 160 blocks
+    assert f(1, 2, 32768, True) == 1        # causal, 256 blocks: no split
+    assert f(1, 1, 8192, False) == 4        # not causal, 32 blocks: 128 pieces, one wave
+    assert f(1, 2, 16384, False) == 1       # not causal, 128 blocks
+    assert f(1, 1, 512, True) == 2          # 2 blocks, but 4 K/V tiles: two per split
+    assert f(1, 1, 100, False) == 1         # a single K/V tile
+    assert f(1, 1, 100000, True) <= 64
+    assert f(0, 1, 1024, True) == 1 and f(1, 1, 1024, 2) == 1
+
 @pytest.mark.parametrize("splits,ws,ws_bytes,expect", [
     (0, FAKE, 1 << 30, abi.FA_ERR_INVALID),
     (65, FAKE, 1 << 30, abi.FA_ERR_INVALID),

@@ -70,11 +70,12 @@ def test_splitkv_f16():
 
 
 def test_splitkv_long_sequence_default_splits():
-    """B=1 H=2 N=32768 d=128 causal, Q std 4: few query blocks per SM without splits."""
+    """B=1 H=1 N=32768 d=128 causal, Q std 4: 128 query blocks, fewer than the SMs, and
+    the last one is 256 K/V tiles long; the default splits it."""
     import torch
-    B, H, N, d = 1, 2, 32768, 128
+    B, H, N, d = 1, 1, 32768, 128
     q, k, v = synth.attention_inputs(B, H, N, d, seed=92000, q_std=4.0)
-    splits = abi.fa_fwd_splitkv_default_splits(B, H, N)
+    splits = abi.fa_fwd_splitkv_default_splits(B, H, N, True)
     assert splits >= 2
     o, lse = run_splitkv(q, k, v, 1 / math.sqrt(d), True, splits)
     for h in range(H):
