@@ -21,7 +21,7 @@ __all__ = ["attention_forward", "attention_backward", "row_state", "softmax", "a
 
 
 def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=True,
-                      out=None, lse_out=None):
+                      out=None, lse_out=None, splits=None):
     """O = softmax(scale * Q K^T) V and LSE for [B, H, N, d] tensors (bf16, fp16 or fp32).
 
     Returns (O, LSE) with O of q's dtype and LSE fp32 [B, H, N] (None without
@@ -30,12 +30,17 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
     are pinned first), and the results land in ``out`` / ``lse_out`` when given
     (pinned host tensors of the right shape), else in new pinned tensors.  Everything
     is ordered on ``stream`` (a torch.cuda.Stream; default: torch's current stream).
+
+    ``splits``: split-KV count for bf16 / fp16 with d in {64, 128} (fa_fwd_splitkv, its
+    workspace allocated here): None takes the library's default for the shape
+    (fa_fwd_splitkv_default_splits; 1 when a split does not pay), 1 never splits.
     """
     import torch
 
     if stream is not None:
         with torch.cuda.stream(stream):
-            return attention_forward(q, k, v, scale, causal, None, with_lse, out, lse_out)
+            return attention_forward(q, k, v, scale, causal, None, with_lse, out, lse_out,
+                                     splits)
     if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must be [B, H, N, d] of one shape")
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float16,
@@ -46,13 +51,34 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
         scale = 1.0 / math.sqrt(d)
     dtype = {torch.bfloat16: abi.FA_BF16, torch.float16: abi.FA_F16,
              torch.float32: abi.FA_F32}[q.dtype]
+    if splits is not None and int(splits) < 1:
+        raise ValueError("splits must be None or >= 1")
+    # One split count for the whole problem (the host path's chunks use it too, so that
+    # both paths compute the same arithmetic).
+    s = 1
+    if dtype in (abi.FA_BF16, abi.FA_F16) and d in (64, 128) and B * H * N > 0:
+        s = int(splits) if splits is not None else \
+            abi.fa_fwd_splitkv_default_splits(B, H, N, int(bool(causal)))
     if q.is_cuda:
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if with_lse else None
-        fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), dtype)
+        _forward_on_device(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, s)
         return o, lse
-    return _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype)
+    return _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype, s)
+
+
+def _forward_on_device(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, s):
+    """fa_fwd_dt, or with s > 1 split-KV fa_fwd_splitkv with a torch-allocated workspace."""
+    import torch
+
+    if s <= 1:
+        fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), dtype)
+        return
+    nbytes = abi.fa_fwd_splitkv_workspace_bytes(B, H, N, d, s)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    abi.fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), s, ws, nbytes,
+                       dtype)
 
 
 _COPY_STREAMS = {}
@@ -67,7 +93,7 @@ def _copy_streams(dev):
     return _COPY_STREAMS[dev.index]
 
 
-def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype):
+def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype, s):
     """Host tensors in, host tensors out, with the copies overlapped with the kernels:
     the (batch, head) slabs are split into chunks; chunk c is copied in on one stream,
     computed on the caller's stream and copied out on a third, so the copy of chunk c+1
@@ -108,9 +134,9 @@ def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtyp
             for dst, src in ((qd, qh), (kd, kh), (vd, vh)):
                 dst[h0:h1].copy_(src[h0:h1], non_blocking=True)
         compute.wait_stream(s_in)
-        fa_fwd_dt(qd[h0:h1], kd[h0:h1], vd[h0:h1], od[h0:h1],
-                  lsed[h0:h1] if lsed is not None else None, 1, h1 - h0, N, d, scale,
-                  int(bool(causal)), dtype)
+        _forward_on_device(qd[h0:h1], kd[h0:h1], vd[h0:h1], od[h0:h1],
+                           lsed[h0:h1] if lsed is not None else None, 1, h1 - h0, N, d,
+                           scale, causal, dtype, s)
         s_out.wait_stream(compute)
         with torch.cuda.stream(s_out):
             o_hv[h0:h1].copy_(od[h0:h1], non_blocking=True)

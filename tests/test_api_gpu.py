@@ -47,6 +47,41 @@ def test_host_path_into_given_buffers_and_without_lse():
     assert torch.equal(o1, o_d.cpu())
 
 
+@pytest.mark.parametrize("B,H,N,d,causal", [
+    (1, 1, 4096, 128, True),     # 16 query blocks: the default splits
+    (1, 2, 2048, 64, False),     # 16 blocks, not causal: the default splits
+])
+def test_forward_api_splits(B, H, N, d, causal):
+    """attention_forward takes the library's default split count for small grids: the
+    result is within the gates of the oracle on sampled rows, splits=1 is exactly the
+    plain kernel, and the host path gives exactly what the device path gives."""
+    import oracle
+    from online_softmax_07_gb300 import abi
+
+    from gpu_helpers import check_attention, sample_rows
+
+    assert abi.fa_fwd_splitkv_default_splits(B, H, N, causal) > 1
+    qn, kn, vn = synth.attention_inputs(B, H, N, d, seed=998 + N, q_std=2.0)
+    q, k, v = (torch.from_numpy(t).to("cuda", torch.bfloat16) for t in (qn, kn, vn))
+    o, lse = osf.attention_forward(q, k, v, causal=causal)
+    scale = 1.0 / np.sqrt(d)
+    for h in range(H):
+        rows = sample_rows(N, 96, seed=999 + h)
+        o_ref, lse_ref = oracle.attention_forward(qn[:, h:h + 1], kn[:, h:h + 1], vn[:, h:h + 1],
+                                                  scale, causal, rows=rows)
+        idx = torch.from_numpy(rows).cuda()
+        check_attention(o[0, h].index_select(0, idx).float().cpu().numpy()[None, None],
+                        lse[0, h].index_select(0, idx).cpu().numpy()[None, None], o_ref, lse_ref)
+    o1, lse1 = osf.attention_forward(q, k, v, causal=causal, splits=1)
+    o_plain = torch.empty_like(q)
+    lse_plain = torch.empty_like(lse)
+    abi.fa_fwd(q, k, v, o_plain, lse_plain, B, H, N, d, scale, int(causal))
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o_plain) and torch.equal(lse1, lse_plain)
+    o_h, lse_h = osf.attention_forward(q.cpu(), k.cpu(), v.cpu(), causal=causal)
+    assert torch.equal(o_h, o.cpu()) and torch.equal(lse_h, lse.cpu())
+
+
 def test_backward_api_matches_abi():
     B, H, N, d = 1, 2, 300, 128
     q, k, v = (torch.from_numpy(t).to("cuda", torch.bfloat16)
