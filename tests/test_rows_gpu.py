@@ -52,6 +52,16 @@ def test_lengths(length):
     check_rows(x, m, l)
 
 
+@pytest.mark.parametrize("rows,length,sigma", [(2, 4_000_003, 3.0), (1, 16_000_001, 3.0),
+                                               (1, 16_000_001, 0.01)])
+def test_very_long_rows(rows, length, sigma):
+    """Rows of 4 M and 16 M floats (each thread folds hundreds of batches into its l);
+    sigma 0.01 makes every term of l close to 1, so l is a sum of 16 M similar terms."""
+    x = synth.row_inputs(rows, length, seed=84000 + int(sigma * 100), std=sigma)
+    m, l = run_rows(x)
+    check_rows(x, m, l)
+
+
 @pytest.mark.parametrize("offset", [1, 2, 3])
 def test_unaligned_base_pointer(offset):
     """The array itself starts 4, 8 or 12 bytes past a 16-byte boundary."""
