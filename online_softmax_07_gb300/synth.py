@@ -66,6 +66,21 @@ def attention_inputs(B, H, N, d, seed, dtype="bf16", q_std=1.0, kv_std=1.0):
     return q, k, v
 
 
+def device_normal(shape, seed: int, std: float = 1.0, dtype=None, device="cuda"):
+    """i.i.d. N(0, std^2) drawn on a CUDA device by torch's seeded generator, for inputs
+    too large to draw on the host (tensors of several GB); cast to ``dtype`` (a torch
+    dtype; default fp32).  Tests copy the rows they check back to the host, so the
+    oracle sees exactly the values the kernels saw."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x if dtype is None else x.to(dtype)
+
+
 def workload_attention_inputs(name: str):
     w = WORKLOADS[name]
     return attention_inputs(w["B"], w["H"], w["N"], w["d"], w["seed"], w["dtype"],

@@ -1,0 +1,57 @@
+"""Tensors of more than 2^31 elements: B=1 H=4100 N=4096 d=128 bf16, 4.3 GB per tensor.
+Heads 4096..4099 start at or beyond element 2^31, so every index into Q, K, V, O, LSE,
+dO and the gradients must be 64-bit.  Sampled rows of heads on both sides of that
+boundary, forward and backward, against the fp64 oracle."""
+
+import numpy as np
+import pytest
+
+import oracle
+from online_softmax_07_gb300 import abi, synth
+from online_softmax_07_gb300.build import build_library
+
+from gpu_helpers import check_attention, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build_library()
+    abi.load()
+
+
+def test_forward_and_backward_beyond_2_31_elements():
+    import torch
+
+    B, H, N, d = 1, 4100, 4096, 128
+    assert B * H * N * d > 2 ** 31 and 4096 * N * d == 2 ** 31
+    scale = 1.0 / np.sqrt(d)
+    q, k, v, do = (synth.device_normal((B, H, N, d), seed=5_000_000 + i, dtype=torch.bfloat16)
+                   for i in range(4))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device="cuda")
+    abi.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, 1)
+    assert abi.fa_last_device_error() == abi.FA_OK
+    nbytes = abi.fa_bwd_workspace_bytes(B, H, N)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    abi.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, 1, ws, nbytes, abi.FA_BF16)
+    assert abi.fa_last_device_error() == abi.FA_OK
+    torch.cuda.synchronize()
+
+    def head(t, h):
+        return t[0, h].float().cpu().numpy()[None, None]
+
+    for h in (0, 4095, 4096, H - 1):
+        rows = sample_rows(N, 24, seed=h)
+        qh, kh, vh, doh = (head(t, h) for t in (q, k, v, do))
+        o_ref, lse_ref = oracle.attention_forward(qh, kh, vh, scale, True, rows=rows)
+        check_attention(head(o, h)[:, :, rows], lse[0, h].cpu().numpy()[None, None, rows],
+                        o_ref, lse_ref)
+        refs = oracle.attention_backward_rows(qh, kh, vh, doh, scale, True, (0, 0), rows, rows)
+        for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), refs):
+            got = head(g, h)[0, 0, rows]
+            rel = np.linalg.norm(got - r) / np.linalg.norm(r)
+            assert rel <= 1e-2, f"{name} head {h}: rel RMS {rel:.3e}"
+            assert np.abs(got - r).max() <= 2e-2 * np.abs(r).max(), f"{name} head {h}"
