@@ -55,3 +55,31 @@ def test_forward_and_backward_beyond_2_31_elements():
             rel = np.linalg.norm(got - r) / np.linalg.norm(r)
             assert rel <= 1e-2, f"{name} head {h}: rel RMS {rel:.3e}"
             assert np.abs(got - r).max() <= 2e-2 * np.abs(r).max(), f"{name} head {h}"
+
+
+@pytest.mark.parametrize("d,q_std", [(128, 1.0), (64, 4.0)])
+def test_forward_sequence_of_131072(d, q_std):
+    """One head of N = 131072, causal: the last query block runs over 1024 K/V tiles
+    (with Q std 4 the row maximum keeps moving).  Sampled rows, including the last,
+    against the oracle; the API's default split count agrees as well."""
+    import torch
+
+    import online_softmax_07_gb300 as osf
+
+    B, H, N = 1, 1, 131072
+    scale = 1.0 / np.sqrt(d)
+    q = synth.device_normal((B, H, N, d), seed=6_000_000 + d, std=q_std, dtype=torch.bfloat16)
+    k, v = (synth.device_normal((B, H, N, d), seed=6_000_010 + d + i, dtype=torch.bfloat16)
+            for i in range(2))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device="cuda")
+    abi.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, 1)
+    assert abi.fa_last_device_error() == abi.FA_OK
+    o2, lse2 = osf.attention_forward(q, k, v, causal=True, splits=4)
+    torch.cuda.synchronize()
+    rows = sample_rows(N, 32, seed=7 + d)
+    qh, kh, vh = (t[0, 0].float().cpu().numpy()[None, None] for t in (q, k, v))
+    o_ref, lse_ref = oracle.attention_forward(qh, kh, vh, scale, True, rows=rows)
+    for oo, ll in ((o, lse), (o2, lse2)):
+        check_attention(oo[0, 0].float().cpu().numpy()[None, None, rows],
+                        ll[0, 0].cpu().numpy()[None, None, rows], o_ref, lse_ref)
