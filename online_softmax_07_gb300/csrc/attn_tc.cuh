@@ -1,4 +1,4 @@
-// attn_tc.cuh -- bf16 attention forward on the 5th-generation tensor cores (sm_103a).
+// attn_tc.cuh -- bf16 / fp16 attention forward on the 5th-generation tensor cores (sm_103a).
 //
 // Computes, for every (batch, head) and query row i,
 //   O_i = sum_j softmax_j(scale * q_i . k_j) v_j  and  LSE_i = ln sum_j exp(scale q_i.k_j)
@@ -13,8 +13,8 @@
 //  * one CTA per SM holds TWO 128-row Q tiles that share one stream of K/V tiles;
 //    the tensor pipe alternates between them, so the softmax of one tile overlaps
 //    the two MMAs of the other ("ping-pong");
-//  * S = Q K^T and O += P V are tcgen05.mma kind::f16 (bf16 in, fp32 accumulate), one
-//    thread issues them; S, P and O live in tensor memory (TMEM), never in HBM;
+//  * S = Q K^T and O += P V are tcgen05.mma kind::f16 (bf16 or fp16 in, fp32
+//    accumulate), issued by one elected thread of the MMA warp; S, P and O live in tensor memory (TMEM), never in HBM;
 //  * Q, K, V tiles arrive by TMA into 128-byte-swizzled shared memory through a ring of
 //    slots guarded by mbarriers; O leaves through shared memory and a TMA store;
 //  * each softmax thread owns one query row of its tile (TMEM lane = row), so row max
