@@ -48,6 +48,20 @@ METRIC = "attn fwd TFLOP/s and % of GB300 bf16 dense peak (1 GPU); row-softmax H
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
 
+def run_config(world):
+    """The workload both arms report (the bench line's ``config``)."""
+    return {
+        "workload": f"{ATTN['name']} + {ROWS['name']}",
+        "attention": {"B": ATTN["B"], "H": ATTN["H"], "N": ATTN["N"], "d": ATTN["d"],
+                      "causal": ATTN["causal"], "scale": 1.0 / math.sqrt(ATTN["d"]),
+                      "inputs": "Q, K, V i.i.d. N(0,1) rounded to bf16"},
+        "rows": {"rows": ROWS["rows"], "len": ROWS["length"],
+                 "inputs": "N(0,9) fp32 with all-equal, +1000 and -1e4 special rows"},
+        "l2": "inputs larger than L2 (201 MB attention, 537 MB rows); no flush",
+        "parallelism": f"replicas x{world} (each GPU runs the full workload)",
+    }
+
+
 def attn_flops(B, H, N, d, causal):
     f = 4.0 * B * H * N * N * d
     return f / 2 if causal else f
@@ -353,7 +367,7 @@ def reference_arm(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": ATTN["name"] + " + " + ROWS["name"], "sample": sample},
+        "config": run_config(world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": workers, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -463,15 +477,7 @@ def our_arm(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": f"{ATTN['name']} + {ROWS['name']}",
-            "attention": {"B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": scale,
-                          "inputs": "Q, K, V i.i.d. N(0,1) rounded to bf16"},
-            "rows": {"rows": rows, "len": length,
-                     "inputs": "N(0,9) fp32 with all-equal, +1000 and -1e4 special rows"},
-            "l2": "inputs larger than L2 (201 MB attention, 537 MB rows); no flush",
-            "parallelism": f"replicas x{world} (each GPU runs the full workload)",
-        },
+        "config": run_config(world),
         "pct_of_peak": per_gpu_tflops / peaks["bf16_tflops"] * 100.0,
         "ms_attention": attn_ms,
         "ms_rows": rows_ms,
