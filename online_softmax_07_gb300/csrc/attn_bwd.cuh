@@ -57,6 +57,15 @@ struct AttnBwdCfg {
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
   static constexpr uint32_t kColX = 384;
   static constexpr uint32_t kTmemCols = 512;
+  // Query-outer pass: K and V stream through separate rings, since K_j is held until
+  // dQ += dS K_j (its last use) and V_j only until dP = dO V_j^T.  K gets the deeper
+  // ring; at d = 128 three K slots and two V slots fit beside the resident Q_i, dO_i.
+  static constexpr int kDqSlotsK = (D == 128) ? 3 : 4;
+  static constexpr int kDqSlotsV = (D == 128) ? 2 : 4;
+  static constexpr int kDqSmemK = kSmemStages;
+  static constexpr int kDqSmemV = kDqSmemK + kDqSlotsK * kTileBytes;
+  static constexpr int kDqSmemBars = kDqSmemV + kDqSlotsV * kTileBytes;
+  static constexpr int kDqSmemBytes = kDqSmemBars + 512 + 1024;
 };
 
 struct AttnBwdParams {

@@ -19,8 +19,10 @@ struct AttnBwdBarriers {
   uint64_t ds_ready[2];  // element-wise -> MMA: dS (or dS^T) stored in TMEM
   uint64_t acc_final;    // MMA -> element-wise: the last accumulation finished
   uint64_t mma_drain;    // MMA warp: all of its MMAs finished (before TMEM is freed)
-  uint64_t stage_full[4];
+  uint64_t stage_full[4];   // key-outer: Q_i, dO_i stages; query-outer: the K ring
   uint64_t stage_empty[4];
+  uint64_t v_full[4];       // query-outer: the V ring
+  uint64_t v_empty[4];
   uint32_t tmem_base;
   int abort;
 };
@@ -495,7 +497,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  AttnBwdBarriers* bars = reinterpret_cast<AttnBwdBarriers*>(smem + Cfg::kSmemBars);
+  AttnBwdBarriers* bars = reinterpret_cast<AttnBwdBarriers*>(smem + Cfg::kDqSmemBars);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -514,9 +516,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(smem_u32(&bars->acc_final), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
-    for (int s = 0; s < Cfg::kStages; ++s) {
+    for (int s = 0; s < Cfg::kDqSlotsK; ++s) {
       mbar_init(smem_u32(&bars->stage_full[s]), 1);
       mbar_init(smem_u32(&bars->stage_empty[s]), 1);
+    }
+    for (int s = 0; s < Cfg::kDqSlotsV; ++s) {
+      mbar_init(smem_u32(&bars->v_full[s]), 1);
+      mbar_init(smem_u32(&bars->v_empty[s]), 1);
     }
     bars->abort = 0;
     mbar_init_fence();
@@ -530,7 +536,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
   volatile int* abort = &bars->abort;
-  auto stage_addr = [&](int s) { return sbase + Cfg::kSmemStages + s * Cfg::kStageBytes; };
+  auto k_addr = [&](int it) { return sbase + Cfg::kDqSmemK + (it % Cfg::kDqSlotsK) * Cfg::kTileBytes; };
+  auto v_addr = [&](int it) { return sbase + Cfg::kDqSmemV + (it % Cfg::kDqSlotsV) * Cfg::kTileBytes; };
 
   if (warp >= 10) {
     // idle
@@ -547,26 +554,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sbase + Cfg::kSmemFixed0 + b * kBoxBytes, &tm_q, fbar, b * kBoxCols, i * kBlockM, bh);
         tma_load_3d(sbase + Cfg::kSmemFixed1 + b * kBoxBytes, &tm_do, fbar, b * kBoxCols, i * kBlockM, bh);
       }
-      int issued = 0;
+      // K_it and V_it in turn (V_it's slot frees before K_it+1's: dP is done before dQ).
+      int issued_k = 0, issued_v = 0;
       for (int it = 0; it < nk; ++it) {
-        const int s = it % Cfg::kStages;
-        if (!mbar_wait(smem_u32(&bars->stage_empty[s]), ((it / Cfg::kStages) & 1) ^ 1, abort,
+        const int sk = it % Cfg::kDqSlotsK, sv = it % Cfg::kDqSlotsV;
+        if (!mbar_wait(smem_u32(&bars->stage_empty[sk]), ((it / Cfg::kDqSlotsK) & 1) ^ 1, abort,
                        p.status))
           break;
-        const uint32_t full = smem_u32(&bars->stage_full[s]);
-        const uint32_t dst = stage_addr(s);
-        mbar_arrive_expect_tx(full, 2 * Cfg::kTileBytes);
+        const uint32_t kfull = smem_u32(&bars->stage_full[sk]);
+        mbar_arrive_expect_tx(kfull, Cfg::kTileBytes);
 #pragma unroll
-        for (int b = 0; b < Cfg::kBoxes; ++b) {
-          tma_load_3d(dst + b * kBoxBytes, &tm_k, full, b * kBoxCols, it * kBlockM, bh);
-          tma_load_3d(dst + Cfg::kTileBytes + b * kBoxBytes, &tm_v, full, b * kBoxCols, it * kBlockM, bh);
-        }
-        issued = it + 1;
+        for (int b = 0; b < Cfg::kBoxes; ++b)
+          tma_load_3d(k_addr(it) + b * kBoxBytes, &tm_k, kfull, b * kBoxCols, it * kBlockM, bh);
+        issued_k = it + 1;
+        if (!mbar_wait(smem_u32(&bars->v_empty[sv]), ((it / Cfg::kDqSlotsV) & 1) ^ 1, abort,
+                       p.status))
+          break;
+        const uint32_t vfull = smem_u32(&bars->v_full[sv]);
+        mbar_arrive_expect_tx(vfull, Cfg::kTileBytes);
+#pragma unroll
+        for (int b = 0; b < Cfg::kBoxes; ++b)
+          tma_load_3d(v_addr(it) + b * kBoxBytes, &tm_v, vfull, b * kBoxCols, it * kBlockM, bh);
+        issued_v = it + 1;
       }
       int no_abort = 0;
       mbar_wait(fbar, 0, &no_abort, p.status);
-      for (int it = max(0, issued - Cfg::kStages); it < issued; ++it)
-        mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]), (it / Cfg::kStages) & 1,
+      for (int it = max(0, issued_k - Cfg::kDqSlotsK); it < issued_k; ++it)
+        mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kDqSlotsK]), (it / Cfg::kDqSlotsK) & 1,
+                  &no_abort, p.status);
+      for (int it = max(0, issued_v - Cfg::kDqSlotsV); it < issued_v; ++it)
+        mbar_wait(smem_u32(&bars->v_full[it % Cfg::kDqSlotsV]), (it / Cfg::kDqSlotsV) & 1,
                   &no_abort, p.status);
     }
   } else if (warp == kBwdWarpMma) {
@@ -580,8 +597,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (r) tc_fence_after();
       return r;
     };
-    auto stage_desc = [&](int it, int tile, uint32_t lbo) {
-      return desc_sw128(stage_addr(it % Cfg::kStages) + tile * Cfg::kTileBytes, lbo, 1024);
+    auto k_desc = [&](int it, uint32_t lbo) { return desc_sw128(k_addr(it), lbo, 1024); };
+    auto v_desc = [&](int it) { return desc_sw128(v_addr(it), 16, 1024); };
+    auto wait_k = [&](int it) {
+      return wait_bar(&bars->stage_full[it % Cfg::kDqSlotsK], (it / Cfg::kDqSlotsK) & 1);
+    };
+    auto wait_v = [&](int it) {
+      return wait_bar(&bars->v_full[it % Cfg::kDqSlotsV], (it / Cfg::kDqSlotsV) & 1);
     };
     // S = Q_i K_j^T into tS, or dP = dO_i V_j^T into tDP: queries on lanes, keys on
     // columns; the streamed tile is the K-major B operand.
@@ -596,7 +618,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //   S(it+1) (once the element-wise warps hold S(it) in registers)  |
     //   dQ += dS(it) K_it (dS stored over dP(it))  |  dP(it+1)
     // so the next S is computed while dS(it) is being formed.
-    bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0);
+    bool ok = wait_bar(&bars->fixed_full, 0) && wait_k(0) && wait_v(0);
     if constexpr (Cfg::kDouble) {
       // Two dP buffers (d = 64): dP(it) and dS(it) in buffer it % 2, so dP(it+1) is issued
       // together with S(it+1) instead of after dQ(it).  Order per key tile it:
@@ -605,62 +627,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // before this warp has taken dS(it).
       auto colDP = [&](int i) { return tbase + ((i & 1) ? Cfg::kColX : Cfg::kColDP); };
       if (ok) {
-        issue_n(tS, dQ, stage_desc(0, 0, 16));
+        issue_n(tS, dQ, k_desc(0, 16));
         mma_commit_elect(smem_u32(&bars->s_full[0]));
-        issue_n(colDP(0), dDO, stage_desc(0, 1, 16));
+        issue_n(colDP(0), dDO, v_desc(0));
         mma_commit_elect(smem_u32(&bars->dp_full[0]));
+        mma_commit_elect(smem_u32(&bars->v_empty[0]));
       }
       for (int it = 0; ok && it < nk; ++it) {
         if (it + 1 < nk) {
           if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
-          if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
-                              ((it + 1) / Cfg::kStages) & 1)))
-            break;
-          issue_n(tS, dQ, stage_desc(it + 1, 0, 16));
+          if (!(ok = wait_k(it + 1) && wait_v(it + 1))) break;
+          issue_n(tS, dQ, k_desc(it + 1, 16));
           mma_commit_elect(smem_u32(&bars->s_full[0]));
-          issue_n(colDP(it + 1), dDO, stage_desc(it + 1, 1, 16));
+          issue_n(colDP(it + 1), dDO, v_desc(it + 1));
           mma_commit_elect(smem_u32(&bars->dp_full[(it + 1) & 1]));
+          mma_commit_elect(smem_u32(&bars->v_empty[(it + 1) % Cfg::kDqSlotsV]));
         }
         if (!(ok = wait_bar(&bars->ds_ready[it & 1], (it >> 1) & 1))) break;
-        const uint64_t dKmn = stage_desc(it, 0, kBoxBytes);
+        const uint64_t dKmn = k_desc(it, kBoxBytes);
 #pragma unroll
         for (int kk = 0; kk < kBlockM / 16; ++kk) {
           const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
           mma_bf16_ts_elect(tDQ, colDP(it) + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
                             (it > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
+        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kDqSlotsK]));
       }
     } else {
       if (ok) {
-        issue_n(tS, dQ, stage_desc(0, 0, 16));
+        issue_n(tS, dQ, k_desc(0, 16));
         mma_commit_elect(smem_u32(&bars->s_full[0]));
-        issue_n(tDP, dDO, stage_desc(0, 1, 16));
+        issue_n(tDP, dDO, v_desc(0));
         mma_commit_elect(smem_u32(&bars->dp_full[0]));
+        mma_commit_elect(smem_u32(&bars->v_empty[0]));
       }
       for (int it = 0; ok && it < nk; ++it) {
         const bool more = it + 1 < nk;
         if (more) {
           if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
-          if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
-                              ((it + 1) / Cfg::kStages) & 1)))
-            break;
-          issue_n(tS, dQ, stage_desc(it + 1, 0, 16));
+          if (!(ok = wait_k(it + 1))) break;
+          issue_n(tS, dQ, k_desc(it + 1, 16));
           mma_commit_elect(smem_u32(&bars->s_full[0]));
         }
         if (!(ok = wait_bar(&bars->ds_ready[0], it & 1))) break;
         // dQ += dS K_j: dS (16 keys = 8 packed columns per step) from the dP columns.
-        const uint64_t dKmn = stage_desc(it, 0, kBoxBytes);
-  #pragma unroll
+        const uint64_t dKmn = k_desc(it, kBoxBytes);
+#pragma unroll
         for (int kk = 0; kk < kBlockM / 16; ++kk) {
           const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
           mma_bf16_ts_elect(tDQ, tDP + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
                             (it > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
+        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kDqSlotsK]));
         if (more) {
-          issue_n(tDP, dDO, stage_desc(it + 1, 1, 16));
+          if (!(ok = wait_v(it + 1))) break;
+          issue_n(tDP, dDO, v_desc(it + 1));
           mma_commit_elect(smem_u32(&bars->dp_full[0]));
+          mma_commit_elect(smem_u32(&bars->v_empty[(it + 1) % Cfg::kDqSlotsV]));
         }
       }
     }
@@ -781,6 +804,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             cudaStream_t stream) {
   using Cfg = AttnBwdCfg<D>;
   static_assert(sizeof(AttnBwdBarriers) <= 512, "barrier block");
+  static_assert(Cfg::kSmemBytes <= 227 * 1024 && Cfg::kDqSmemBytes <= 227 * 1024, "shared memory");
   AttnBwdParams p = p0;
   float* lse2 = ws;
   float* dd = ws + static_cast<long long>(p.BH) * p.n_pad;
@@ -797,13 +821,13 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
       cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, F16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes)) !=
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kDqSmemBytes)) !=
       cudaSuccess)
     return e;
   const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.BH) * p.nblk);
   attn_bwd_dkdv_kernel<D, F16><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
