@@ -57,13 +57,16 @@ struct AttnBwdCfg {
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
   static constexpr uint32_t kColX = 384;
   static constexpr uint32_t kTmemCols = 512;
-  // Query-outer pass: K and V stream through separate rings, since K_j is held until
-  // dQ += dS K_j (its last use) and V_j only until dP = dO V_j^T.  K gets the deeper
-  // ring; at d = 128 three K slots and two V slots fit beside the resident Q_i, dO_i.
-  static constexpr int kDqSlotsK = (D == 128) ? 3 : 4;
-  static constexpr int kDqSlotsV = (D == 128) ? 2 : 4;
+  // Query-outer pass at d = 128: K and V stream through separate rings, since K_j is
+  // held until dQ += dS K_j (its last use) and V_j only until dP = dO V_j^T; K gets the
+  // deeper ring, three slots, and V two, beside the resident Q_i, dO_i.  At d = 64 a
+  // single ring of four K|V pairs (one barrier per pair) measured faster.
+  static constexpr bool kDqSplitKV = (D == 128);
+  static constexpr int kDqSlotsK = kDqSplitKV ? 3 : 4;  // K slots, or K|V pairs
+  static constexpr int kDqSlotsV = kDqSplitKV ? 2 : 0;
+  static constexpr int kDqSlotBytes = kDqSplitKV ? kTileBytes : 2 * kTileBytes;
   static constexpr int kDqSmemK = kSmemStages;
-  static constexpr int kDqSmemV = kDqSmemK + kDqSlotsK * kTileBytes;
+  static constexpr int kDqSmemV = kDqSmemK + kDqSlotsK * kDqSlotBytes;
   static constexpr int kDqSmemBars = kDqSmemV + kDqSlotsV * kTileBytes;
   static constexpr int kDqSmemBytes = kDqSmemBars + 512 + 1024;
 };

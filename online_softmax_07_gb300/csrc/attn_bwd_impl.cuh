@@ -536,8 +536,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
   volatile int* abort = &bars->abort;
-  auto k_addr = [&](int it) { return sbase + Cfg::kDqSmemK + (it % Cfg::kDqSlotsK) * Cfg::kTileBytes; };
-  auto v_addr = [&](int it) { return sbase + Cfg::kDqSmemV + (it % Cfg::kDqSlotsV) * Cfg::kTileBytes; };
+  auto k_addr = [&](int it) {
+    return sbase + Cfg::kDqSmemK + (it % Cfg::kDqSlotsK) * Cfg::kDqSlotBytes;
+  };
+  auto v_addr = [&](int it) {
+    if constexpr (Cfg::kDqSplitKV)
+      return sbase + Cfg::kDqSmemV + (it % Cfg::kDqSlotsV) * Cfg::kTileBytes;
+    else
+      return k_addr(it) + Cfg::kTileBytes;  // the second tile of the pair
+  };
 
   if (warp >= 10) {
     // idle
@@ -554,37 +561,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sbase + Cfg::kSmemFixed0 + b * kBoxBytes, &tm_q, fbar, b * kBoxCols, i * kBlockM, bh);
         tma_load_3d(sbase + Cfg::kSmemFixed1 + b * kBoxBytes, &tm_do, fbar, b * kBoxCols, i * kBlockM, bh);
       }
-      // K_it and V_it in turn (V_it's slot frees before K_it+1's: dP is done before dQ).
+      // K_it and V_it in turn (with split rings V_it's slot frees before K_it+1's: dP is
+      // done before dQ).  With pairs, one barrier covers both tiles.
       int issued_k = 0, issued_v = 0;
       for (int it = 0; it < nk; ++it) {
-        const int sk = it % Cfg::kDqSlotsK, sv = it % Cfg::kDqSlotsV;
+        const int sk = it % Cfg::kDqSlotsK;
         if (!mbar_wait(smem_u32(&bars->stage_empty[sk]), ((it / Cfg::kDqSlotsK) & 1) ^ 1, abort,
                        p.status))
           break;
         const uint32_t kfull = smem_u32(&bars->stage_full[sk]);
-        mbar_arrive_expect_tx(kfull, Cfg::kTileBytes);
+        mbar_arrive_expect_tx(kfull, Cfg::kDqSplitKV ? Cfg::kTileBytes : 2 * Cfg::kTileBytes);
 #pragma unroll
         for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_load_3d(k_addr(it) + b * kBoxBytes, &tm_k, kfull, b * kBoxCols, it * kBlockM, bh);
         issued_k = it + 1;
-        if (!mbar_wait(smem_u32(&bars->v_empty[sv]), ((it / Cfg::kDqSlotsV) & 1) ^ 1, abort,
-                       p.status))
-          break;
-        const uint32_t vfull = smem_u32(&bars->v_full[sv]);
-        mbar_arrive_expect_tx(vfull, Cfg::kTileBytes);
+        uint32_t vfull = kfull;
+        if constexpr (Cfg::kDqSplitKV) {
+          const int sv = it % Cfg::kDqSlotsV;
+          if (!mbar_wait(smem_u32(&bars->v_empty[sv]), ((it / Cfg::kDqSlotsV) & 1) ^ 1, abort,
+                         p.status))
+            break;
+          vfull = smem_u32(&bars->v_full[sv]);
+          mbar_arrive_expect_tx(vfull, Cfg::kTileBytes);
+          issued_v = it + 1;
+        }
 #pragma unroll
         for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_load_3d(v_addr(it) + b * kBoxBytes, &tm_v, vfull, b * kBoxCols, it * kBlockM, bh);
-        issued_v = it + 1;
       }
       int no_abort = 0;
       mbar_wait(fbar, 0, &no_abort, p.status);
       for (int it = max(0, issued_k - Cfg::kDqSlotsK); it < issued_k; ++it)
         mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kDqSlotsK]), (it / Cfg::kDqSlotsK) & 1,
                   &no_abort, p.status);
-      for (int it = max(0, issued_v - Cfg::kDqSlotsV); it < issued_v; ++it)
-        mbar_wait(smem_u32(&bars->v_full[it % Cfg::kDqSlotsV]), (it / Cfg::kDqSlotsV) & 1,
-                  &no_abort, p.status);
+      if constexpr (Cfg::kDqSplitKV) {
+        for (int it = max(0, issued_v - Cfg::kDqSlotsV); it < issued_v; ++it)
+          mbar_wait(smem_u32(&bars->v_full[it % Cfg::kDqSlotsV]), (it / Cfg::kDqSlotsV) & 1,
+                    &no_abort, p.status);
+      }
     }
   } else if (warp == kBwdWarpMma) {
     constexpr uint32_t kIdescS = idesc_f16kind(kBlockM, kBlockM, false, F16);
@@ -602,8 +616,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto wait_k = [&](int it) {
       return wait_bar(&bars->stage_full[it % Cfg::kDqSlotsK], (it / Cfg::kDqSlotsK) & 1);
     };
+    // With pairs V_it came with K_it: nothing more to wait for, nothing to release early.
     auto wait_v = [&](int it) {
-      return wait_bar(&bars->v_full[it % Cfg::kDqSlotsV], (it / Cfg::kDqSlotsV) & 1);
+      if constexpr (Cfg::kDqSplitKV)
+        return wait_bar(&bars->v_full[it % Cfg::kDqSlotsV], (it / Cfg::kDqSlotsV) & 1);
+      else
+        return true;
+    };
+    auto release_v = [&](int it) {
+      if constexpr (Cfg::kDqSplitKV)
+        mma_commit_elect(smem_u32(&bars->v_empty[it % Cfg::kDqSlotsV]));
     };
     // S = Q_i K_j^T into tS, or dP = dO_i V_j^T into tDP: queries on lanes, keys on
     // columns; the streamed tile is the K-major B operand.
@@ -631,7 +653,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit_elect(smem_u32(&bars->s_full[0]));
         issue_n(colDP(0), dDO, v_desc(0));
         mma_commit_elect(smem_u32(&bars->dp_full[0]));
-        mma_commit_elect(smem_u32(&bars->v_empty[0]));
+        release_v(0);
       }
       for (int it = 0; ok && it < nk; ++it) {
         if (it + 1 < nk) {
@@ -641,7 +663,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit_elect(smem_u32(&bars->s_full[0]));
           issue_n(colDP(it + 1), dDO, v_desc(it + 1));
           mma_commit_elect(smem_u32(&bars->dp_full[(it + 1) & 1]));
-          mma_commit_elect(smem_u32(&bars->v_empty[(it + 1) % Cfg::kDqSlotsV]));
+          release_v(it + 1);
         }
         if (!(ok = wait_bar(&bars->ds_ready[it & 1], (it >> 1) & 1))) break;
         const uint64_t dKmn = k_desc(it, kBoxBytes);
@@ -659,7 +681,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit_elect(smem_u32(&bars->s_full[0]));
         issue_n(tDP, dDO, v_desc(0));
         mma_commit_elect(smem_u32(&bars->dp_full[0]));
-        mma_commit_elect(smem_u32(&bars->v_empty[0]));
+        release_v(0);
       }
       for (int it = 0; ok && it < nk; ++it) {
         const bool more = it + 1 < nk;
@@ -683,7 +705,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = wait_v(it + 1))) break;
           issue_n(tDP, dDO, v_desc(it + 1));
           mma_commit_elect(smem_u32(&bars->dp_full[0]));
-          mma_commit_elect(smem_u32(&bars->v_empty[(it + 1) % Cfg::kDqSlotsV]));
+          release_v(it + 1);
         }
       }
     }
