@@ -148,6 +148,37 @@ fa_status fa_fwd_splitkv_static(const void* q, const void* k, const void* v, voi
                                 cudaStream_t stream);
 
 /*
+ * Attention forward on host-resident tensors (the end-to-end path): q, k, v, o and lse
+ * as in fa_fwd_dt but in host memory.  The B * H (batch, head) slabs are processed in
+ * `chunks` consecutive groups; for each group the library copies Q, K, V in on an
+ * internal copy stream, runs fa_fwd_dt on `stream`, and copies O (and LSE) out on a
+ * second internal copy stream, so the copies of one group overlap the kernels of its
+ * neighbours.  Up to three groups' device buffers are in use at a time, in `workspace`.
+ *
+ * q, k, v, o: host [B, H, N, d] (bf16/fp16: d in {64, 128}; fp32: any d <= 128);
+ *             should be page-locked (cudaHostAlloc / cudaHostRegister): pageable memory
+ *             gives the same results but the copies then do not overlap.
+ * lse:        host fp32 [B, H, N], or NULL.
+ * chunks:     >= 1 (more than B * H acts as B * H).
+ * workspace:  device memory owned by the caller, at least
+ *             fa_fwd_host_workspace_bytes(B, H, N, d, dtype, chunks) bytes, 256-byte
+ *             aligned; its contents are overwritten.
+ * Ordering: the copies in start after work enqueued on `stream` before the call, and
+ * work enqueued on `stream` after the call starts after the last copy out; the call
+ * returns once everything is enqueued (synchronise `stream` before reading o / lse).
+ * Calls from several threads are enqueued one at a time.
+ * Errors: as fa_fwd_dt; FA_ERR_INVALID for chunks < 1, a NULL or too small workspace;
+ * FA_ERR_ALIGN for a misaligned workspace; FA_ERR_CUDA if a copy or an enqueue fails
+ * (o and lse are then undefined).
+ */
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int N, int d, float scale, int causal, fa_dtype dtype, int chunks,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Device workspace bytes fa_fwd_host needs (0 for invalid arguments).  Host-only. */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d, fa_dtype dtype, int chunks);
+
+/*
  * Row online-softmax state.
  *
  * x:      device fp32 [rows, len], contiguous row-major; any 4-byte alignment (a row

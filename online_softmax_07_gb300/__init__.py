@@ -93,11 +93,20 @@ def _copy_streams(dev):
     return _COPY_STREAMS[dev.index]
 
 
+# Groups of (batch, head) slabs of the host path: the copies of one group overlap the
+# kernels of its neighbours, so more groups shorten the exposed first copy in and last
+# copy out, until a group's kernel is held up by its longest query block.  Measured on
+# B2 H16 N8192 d128 causal (fa_fwd_host): 2 groups 1.405 ms, 4 1.272, 8 1.281, 16 1.689.
+_HOST_CHUNKS = 4
+
+
 def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype, s):
     """Host tensors in, host tensors out, with the copies overlapped with the kernels:
     the (batch, head) slabs are split into chunks; chunk c is copied in on one stream,
     computed on the caller's stream and copied out on a third, so the copy of chunk c+1
-    runs while chunk c computes and the copy out of chunk c overlaps both."""
+    runs while chunk c computes and the copy out of chunk c overlaps both.  Without
+    split-KV the library does this itself (fa_fwd_host); with it, the chunks are
+    enqueued from here."""
     import torch
 
     B, H, N, d = q.shape
@@ -108,12 +117,22 @@ def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtyp
         t = t.contiguous()
         return t if t.is_pinned() else t.pin_memory()
 
-    qh, kh, vh = (pinned(t).view(BH, N, d) for t in (q, k, v))
     o_h = out if out is not None else torch.empty((B, H, N, d), dtype=q.dtype, pin_memory=True)
     lse_h = None
     if with_lse:
         lse_h = lse_out if lse_out is not None else torch.empty((B, H, N), dtype=torch.float32,
                                                                 pin_memory=True)
+    if s <= 1:
+        qp, kp, vp = (pinned(t) for t in (q, k, v))
+        nbytes = abi.fa_fwd_host_workspace_bytes(B, H, N, d, dtype, _HOST_CHUNKS)
+        ws = torch.empty(max(1, nbytes), dtype=torch.uint8, device=dev)
+        abi.fa_fwd_host(qp, kp, vp, o_h, lse_h, B, H, N, d, scale, int(bool(causal)), dtype,
+                        _HOST_CHUNKS, ws, nbytes)
+        # The caller's stream waits for the last copy out: after this, the results are in
+        # o_h / lse_h and the workspace is no longer in use.
+        torch.cuda.current_stream().synchronize()
+        return o_h, lse_h
+    qh, kh, vh = (pinned(t).view(BH, N, d) for t in (q, k, v))
     o_hv = o_h.view(BH, N, d)
     lse_hv = lse_h.view(BH, N) if lse_h is not None else None
     qd, kd, vd = (torch.empty((BH, N, d), dtype=q.dtype, device=dev) for _ in range(3))

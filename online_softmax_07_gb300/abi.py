@@ -2,6 +2,7 @@
 
 The functions here carry the C names and signatures: ``fa_fwd``, ``fa_fwd_dt``,
 ``fa_fwd_splitkv``, ``fa_fwd_splitkv_workspace_bytes``, ``fa_fwd_splitkv_default_splits``,
+``fa_fwd_host``, ``fa_fwd_host_workspace_bytes``,
 ``online_softmax_rows``, ``online_softmax_forward``, ``fa_status_str``,
 ``fa_last_device_error`` and ``fa_selftest_wait_timeout``.  Pointer arguments accept a CUDA ``torch.Tensor``
 (its data pointer is passed), an ``int`` address, or ``None`` (NULL).  A non-OK
@@ -35,6 +36,10 @@ _SIGNATURES = {
                               + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                                       ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_splitkv_default_splits": (ctypes.c_int, [ctypes.c_int] * 4),
+    "fa_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 4
+                    + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                       ctypes.c_size_t, ctypes.c_void_p]),
+    "fa_fwd_host_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
     "fa_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 4
                + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
                   ctypes.c_void_p]),
@@ -89,6 +94,17 @@ def _ptr(x):
     raise TypeError(f"cannot pass {type(x).__name__} as a pointer")
 
 
+def _host_ptr(x):
+    """Address of a host buffer: a contiguous CPU torch.Tensor, an int, or None."""
+    if x is None or isinstance(x, int):
+        return x
+    if x.is_cuda:
+        raise ValueError("host pointer expected: pass a CPU tensor")
+    if not x.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return x.data_ptr()
+
+
 def _stream(s):
     if s is None:
         import torch
@@ -139,6 +155,20 @@ def fa_fwd_splitkv_static(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits
 
 def fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits) -> int:
     return int(load().fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits))
+
+
+def fa_fwd_host(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, chunks, workspace,
+                workspace_bytes, stream=None) -> None:
+    """q, k, v, o, lse are host tensors (page-locked for overlapped copies); workspace is a
+    device buffer of fa_fwd_host_workspace_bytes bytes."""
+    _check(load().fa_fwd_host(_host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(o),
+                              _host_ptr(lse), B, H, N, d, float(scale), int(causal), int(dtype),
+                              int(chunks), _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "fa_fwd_host")
+
+
+def fa_fwd_host_workspace_bytes(B, H, N, d, dtype, chunks) -> int:
+    return int(load().fa_fwd_host_workspace_bytes(B, H, N, d, int(dtype), int(chunks)))
 
 
 def fa_fwd_splitkv_default_splits(B, H, N, causal) -> int:

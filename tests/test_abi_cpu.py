@@ -188,3 +188,37 @@ def test_fa_bwd_argument_checks(lib, args, expect):
                     a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], a["ws"], a["ws_bytes"],
                     a["dtype"], None)
     assert st == expect, abi.status_str(st)
+
+def test_fwd_host_workspace_size(lib):
+    """Three groups' Q, K, V, O (256-byte aligned) and LSE at most; heads per group =
+    ceil(B * H / chunks)."""
+    f = abi.fa_fwd_host_workspace_bytes
+    # B*H = 8 in 3 groups of 3 heads: 3 slots of 4 * 115200 + 3840 bytes
+    assert f(2, 4, 300, 64, abi.FA_BF16, 3) == 3 * (4 * 115200 + 3840)
+    # one head, fp32 d = 64: one slot; 100 * 4 LSE bytes rounded up to 512
+    assert f(1, 1, 100, 64, abi.FA_F32, 5) == 4 * 25600 + 512
+    # 16 heads in 8 groups of 2: still three slots
+    assert f(1, 16, 128, 128, abi.FA_F16, 8) == 3 * (4 * 65536 + 1024)
+    assert f(1, 1, 100, 64, abi.FA_BF16, 0) == 0          # no chunks
+    assert f(1, 1, 100, 96, abi.FA_BF16, 2) == 0          # unsupported d
+    assert f(0, 4, 100, 64, abi.FA_BF16, 2) == 0          # empty
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(chunks=0), abi.FA_ERR_INVALID),
+    (dict(d=96), abi.FA_ERR_UNSUPPORTED),
+    (dict(causal=2), abi.FA_ERR_INVALID),
+    (dict(ws=None), abi.FA_ERR_INVALID),
+    (dict(ws_bytes=16), abi.FA_ERR_INVALID),
+    (dict(ws=8), abi.FA_ERR_ALIGN),
+    (dict(q=None), abi.FA_ERR_INVALID),
+    (dict(B=0), abi.FA_OK),                               # empty: nothing to do
+])
+def test_fwd_host_argument_checks(lib, args, expect):
+    """Rejected (or, for an empty problem, accepted) before any CUDA call."""
+    a = dict(q=4096, B=1, H=2, N=100, d=64, causal=0, chunks=2, ws=1 << 20, ws_bytes=1 << 30)
+    a.update(args)
+    st = lib.fa_fwd_host(a["q"], 8192, 12288, 16384, None, a["B"], a["H"], a["N"], a["d"],
+                         0.125, a["causal"], abi.FA_BF16, a["chunks"], a["ws"], a["ws_bytes"],
+                         None)
+    assert st == expect

@@ -82,6 +82,43 @@ def test_forward_api_splits(B, H, N, d, causal):
     assert torch.equal(o_h, o.cpu()) and torch.equal(lse_h, lse.cpu())
 
 
+@pytest.mark.parametrize("dtype,d,causal,chunks", [
+    ("bf16", 128, True, 1), ("bf16", 64, False, 3), ("f16", 128, True, 7),
+    ("bf16", 128, False, 100),   # more chunks than heads
+    ("f32", 40, True, 4),        # the fp32 kernel, d not a multiple of 16
+])
+@pytest.mark.parametrize("with_lse,pin", [(True, True), (False, False)])
+def test_fwd_host_equals_device(dtype, d, causal, chunks, with_lse, pin):
+    """fa_fwd_host (host tensors, copies and kernels overlapped in groups of heads) gives
+    exactly what fa_fwd_dt gives on device copies of the same tensors; from pageable
+    memory as well (the copies are then synchronous)."""
+    from online_softmax_07_gb300 import abi
+
+    B, H, N = 2, 5, 333
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
+    code = {"bf16": abi.FA_BF16, "f16": abi.FA_F16, "f32": abi.FA_F32}[dtype]
+    q, k, v = (torch.from_numpy(t).to(tdt)
+               for t in synth.attention_inputs(B, H, N, d, seed=1200 + d + chunks, dtype="f32"))
+    if pin:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    scale = 1.0 / np.sqrt(d)
+    o_h = torch.full((B, H, N, d), float("nan"), dtype=tdt, pin_memory=pin)
+    lse_h = torch.full((B, H, N), float("nan"), pin_memory=pin) if with_lse else None
+    nbytes = abi.fa_fwd_host_workspace_bytes(B, H, N, d, code, chunks)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    abi.fa_fwd_host(q, k, v, o_h, lse_h, B, H, N, d, scale, int(causal), code, chunks, ws, nbytes)
+    torch.cuda.current_stream().synchronize()
+    assert abi.fa_last_device_error() == abi.FA_OK
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o_d = torch.empty_like(qd)
+    lse_d = torch.empty((B, H, N), device="cuda")
+    abi.fa_fwd_dt(qd, kd, vd, o_d, lse_d, B, H, N, d, scale, int(causal), code)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    if with_lse:
+        assert torch.equal(lse_h, lse_d.cpu())
+
+
 def test_backward_api_matches_abi():
     B, H, N, d = 1, 2, 300, 128
     q, k, v = (torch.from_numpy(t).to("cuda", torch.bfloat16)
