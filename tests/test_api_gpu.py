@@ -119,6 +119,51 @@ def test_fwd_host_equals_device(dtype, d, causal, chunks, with_lse, pin):
         assert torch.equal(lse_h, lse_d.cpu())
 
 
+def test_fwd_host_concurrent_threads():
+    """Four host threads, each on its own stream with its own inputs, workspace and group
+    count, call fa_fwd_host repeatedly at the same time: the library's copy streams and
+    slot events are shared, and every result must still equal the device path's."""
+    import threading
+
+    from online_softmax_07_gb300 import abi
+
+    B, H, N, d = 1, 6, 400, 64
+    scale = 1.0 / np.sqrt(d)
+    jobs = []
+    for t in range(4):
+        q, k, v = (torch.from_numpy(x).to(torch.bfloat16).pin_memory()
+                   for x in synth.attention_inputs(B, H, N, d, seed=1300 + t))
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        o_ref = torch.empty_like(qd)
+        lse_ref = torch.empty((B, H, N), device="cuda")
+        abi.fa_fwd_dt(qd, kd, vd, o_ref, lse_ref, B, H, N, d, scale, t % 2, abi.FA_BF16)
+        chunks = 1 + t
+        nbytes = abi.fa_fwd_host_workspace_bytes(B, H, N, d, abi.FA_BF16, chunks)
+        jobs.append(dict(q=q, k=k, v=v, causal=t % 2, chunks=chunks, nbytes=nbytes,
+                         ws=torch.empty(nbytes, dtype=torch.uint8, device="cuda"),
+                         stream=torch.cuda.Stream(), o_ref=o_ref, lse_ref=lse_ref,
+                         ok=True))
+    torch.cuda.synchronize()
+
+    def worker(j):
+        for _ in range(10):
+            o = torch.full((B, H, N, d), float("nan"), dtype=torch.bfloat16, pin_memory=True)
+            lse = torch.full((B, H, N), float("nan"), pin_memory=True)
+            abi.fa_fwd_host(j["q"], j["k"], j["v"], o, lse, B, H, N, d, scale, j["causal"],
+                            abi.FA_BF16, j["chunks"], j["ws"], j["nbytes"], j["stream"])
+            j["stream"].synchronize()
+            if not (torch.equal(o, j["o_ref"].cpu()) and torch.equal(lse, j["lse_ref"].cpu())):
+                j["ok"] = False
+
+    threads = [threading.Thread(target=worker, args=(j,)) for j in jobs]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert abi.fa_last_device_error() == abi.FA_OK
+    assert all(j["ok"] for j in jobs)
+
+
 def test_backward_api_matches_abi():
     B, H, N, d = 1, 2, 300, 128
     q, k, v = (torch.from_numpy(t).to("cuda", torch.bfloat16)
