@@ -82,8 +82,11 @@ __device__ __forceinline__ void bwd_work(const AttnBwdParams& p, bool low_first,
   *bh = base + r % hg;
 }
 
-// D_i = sum_c dO_ic O_ic and LSE_i * log2(e), one warp per query row; rows N .. n_pad-1
-// of each head get D = 0 and +inf.
+// D_i = sum_c dO_ic O_ic and LSE_i * log2(e); rows N .. n_pad-1 of each head get D = 0 and
+// +inf.  A warp takes kPrepRows query rows and issues all their loads before reducing any,
+// so that enough bytes are in flight to stream O and dO at HBM speed.
+constexpr int kPrepRows = 4;
+
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __restrict__ o,
                                                             const uint16_t* __restrict__ dout,
@@ -91,47 +94,62 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __re
                                                             float* __restrict__ lse2,
                                                             float* __restrict__ dd, int BH, int N,
                                                             int n_pad) {
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  constexpr int kPer = D / 32;  // 16-bit elements per lane and row: 2 or 4
+  const long long total = static_cast<long long>(BH) * n_pad;
+  const long long row0 =
+      (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kPrepRows;
   const int lane = threadIdx.x & 31;
-  if (row >= static_cast<long long>(BH) * n_pad) return;
-  const long long bh = row / n_pad;
-  const int q = static_cast<int>(row - bh * n_pad);
-  if (q >= N) {
-    if (lane == 0) {
-      dd[row] = 0.f;
-      lse2[row] = INFINITY;
-    }
-    return;
-  }
-  const long long off = (bh * N + q) * D;
-  constexpr int kPer = D / 32;  // 16-bit elements per lane: 2 or 4
-  float acc = 0.f;
-  if constexpr (kPer == 4) {
-    const uint2 a = *reinterpret_cast<const uint2*>(o + off + lane * 4);
-    const uint2 b = *reinterpret_cast<const uint2*>(dout + off + lane * 4);
-    const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
+  uint32_t av[kPrepRows][kPer / 2], bv[kPrepRows][kPer / 2];
+  bool real[kPrepRows];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+  for (int r = 0; r < kPrepRows; ++r) {
+    const long long row = row0 + r;
+    const long long bh = row / n_pad;
+    const int q = static_cast<int>(row - bh * n_pad);
+    real[r] = row < total && q < N;
+#pragma unroll
+    for (int i = 0; i < kPer / 2; ++i) av[r][i] = bv[r][i] = 0u;
+    if (real[r]) {
+      const long long off = (bh * N + q) * D + lane * kPer;
+      if constexpr (kPer == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+        const uint2 b = *reinterpret_cast<const uint2*>(dout + off);
+        av[r][0] = a.x; av[r][1] = a.y;
+        bv[r][0] = b.x; bv[r][1] = b.y;
+      } else {
+        av[r][0] = *reinterpret_cast<const uint32_t*>(o + off);
+        bv[r][0] = *reinterpret_cast<const uint32_t*>(dout + off);
+      }
+    }
+  }
+  float acc[kPrepRows];
+#pragma unroll
+  for (int r = 0; r < kPrepRows; ++r) {
+    acc[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer / 2; ++i) {
       float a0, a1, b0, b1;
-      unpack_elem2<F16>(av[i], a0, a1);
-      unpack_elem2<F16>(bv[i], b0, b1);
-      acc = fmaf(a0, b0, acc);
-      acc = fmaf(a1, b1, acc);
+      unpack_elem2<F16>(av[r][i], a0, a1);
+      unpack_elem2<F16>(bv[r][i], b0, b1);
+      acc[r] = fmaf(a0, b0, acc[r]);
+      acc[r] = fmaf(a1, b1, acc[r]);
     }
-  } else {
-    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + off + lane * 2);
-    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + off + lane * 2);
-    float a0, a1, b0, b1;
-    unpack_elem2<F16>(a, a0, a1);
-    unpack_elem2<F16>(b, b0, b1);
-    acc = fmaf(a0, b0, acc);
-    acc = fmaf(a1, b1, acc);
   }
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    dd[row] = acc;
-    lse2[row] = lse[bh * N + q] * 1.4426950408889634f;
+  for (int sh = 16; sh > 0; sh >>= 1)
+#pragma unroll
+    for (int r = 0; r < kPrepRows; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], sh);
+  if (lane < kPrepRows) {
+    float mine = acc[0];
+#pragma unroll
+    for (int r = 1; r < kPrepRows; ++r) mine = (lane == r) ? acc[r] : mine;
+    const long long row = row0 + lane;
+    if (row < total) {
+      const long long bh = row / n_pad;
+      const int q = static_cast<int>(row - bh * n_pad);
+      dd[row] = q < N ? mine : 0.f;
+      lse2[row] = q < N ? lse[bh * N + q] * 1.4426950408889634f : INFINITY;
+    }
   }
 }
 
@@ -833,7 +851,8 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   p.lse2 = lse2;
   p.dd = dd;
   const long long rows = static_cast<long long>(p.BH) * p.n_pad;
-  attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+  attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((rows + 8 * kPrepRows - 1) / (8 * kPrepRows)),
+                                 256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dd, p.BH,
       p.N, p.n_pad);
   cudaError_t e = cudaGetLastError();
