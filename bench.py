@@ -19,7 +19,9 @@ Printed JSON (one line, rank 0):
              (inside row_softmax) against the measured HBM copy bandwidth;
   cpu_baseline  the fp64 oracle timed on a bounded sample of the same workload on the
              host cores (rank 0, one GPU only).
-``--impl reference`` times the oracle alone (see ``reference_arm``).
+``--impl reference`` times the oracle alone (see ``reference_arm``); ``--suite``,
+``--backward`` and ``--forward B,H,N,d,causal`` print per-workload lines instead (the
+commands the committed profiles were taken with).
 """
 
 from __future__ import annotations
@@ -712,6 +714,50 @@ def backward_run(args):
                       "warmup": args.warmup, "ms": ms, "TFLOP/s": tf}), flush=True)
 
 
+def forward_run(args):
+    """The attention forward alone on one shape, --forward B,H,N,d,causal (bf16; Q, K, V
+    i.i.d. N(0,1) drawn on the device from fixed seeds): --warmup and --steps fa_fwd_dt
+    calls timed with CUDA events.  One JSON line; this is the command that single-shape
+    launch lists and ncu captures of the forward are taken with."""
+    import torch
+
+    from online_softmax_07_gb300 import abi, synth
+    from online_softmax_07_gb300.build import build_library
+
+    try:
+        B, H, N, d, causal = (int(x) for x in args.forward.split(","))
+    except ValueError:
+        raise SystemExit("--forward wants B,H,N,d,causal (five integers)")
+    build_library()
+    abi.load()
+    stream = torch.cuda.current_stream()
+    q, k, v = (synth.device_normal((B, H, N, d), seed=98000 + i, dtype=torch.bfloat16)
+               for i in range(3))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=q.device)
+    scale = 1.0 / math.sqrt(d)
+
+    def call():
+        abi.fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, abi.FA_BF16, stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if abi.fa_last_device_error() != abi.FA_OK:
+        raise RuntimeError("device-side error")
+    ms = e0.elapsed_time(e1) / args.steps
+    name = f"attn_bf16_b{B}h{H}n{N}d{d}" + ("_causal" if causal else "")
+    print(json.dumps({"workload": name, "steps": args.steps, "warmup": args.warmup, "ms": ms,
+                      "TFLOP/s": attn_flops(B, H, N, d, bool(causal)) / (ms * 1e-3) / 1e12}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -724,6 +770,8 @@ def main():
                     help="one line per workload instead of the bench line (1 GPU)")
     ap.add_argument("--backward", action="store_true",
                     help="time fa_bwd alone on B2 H16 N8192 d128 causal (1 GPU)")
+    ap.add_argument("--forward", metavar="B,H,N,d,causal",
+                    help="time the bf16 forward alone on one shape (1 GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -734,6 +782,9 @@ def main():
         return
     if args.backward:
         backward_run(args)
+        return
+    if args.forward:
+        forward_run(args)
         return
     if world > 1 and args.impl == "ours":
         import torch
