@@ -176,10 +176,12 @@ fa_status run_tc(const void* q, const void* k, const void* v, void* o, float* ls
   p.N = N;
   p.BH = bh;
   p.nqb = static_cast<int>(nqb);
-  // Heads scheduled together: as many as keep their K and V within about 64 MB of L2.
+  // Heads scheduled together: as many as keep their K and V within about 32 MB of the
+  // 129 MB L2 (a sweep of 8-128 MB on GB300: 32 MB as fast as or faster than 64 MB on
+  // every shape measured; 16 MB and below lengthen the causal tail).
   const long long kv_head_bytes = 2LL * N * d * 2;
   p.head_group = static_cast<int>(
-      std::max(1LL, std::min(BH, (64LL << 20) / std::max(1LL, kv_head_bytes))));
+      std::max(1LL, std::min(BH, (32LL << 20) / std::max(1LL, kv_head_bytes))));
   p.causal = causal;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.splits = splits;
