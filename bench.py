@@ -666,10 +666,12 @@ def suite(args):
 
 
 def backward_run(args):
-    """The backward alone, on the B=2 H=16 N=8192 d=128 causal workload with the suite's
-    seeded dO: fa_fwd once for O and LSE, then --warmup and --steps fa_bwd calls (each a
-    prep, a dK/dV and a dQ launch) timed with CUDA events.  One JSON line; this is the
-    command the backward's launch list and ncu captures are taken with."""
+    """The backward alone: by default on the B=2 H=16 N=8192 d=128 causal workload with the
+    suite's seeded dO, or on the shape --backward B,H,N,d,causal gives (bf16, Q, K, V, dO
+    i.i.d. N(0,1) drawn on the device from fixed seeds): fa_fwd once for O and LSE, then
+    --warmup and --steps fa_bwd calls (each a prep, a dK/dV and a dQ launch) timed with
+    CUDA events.  One JSON line; this is the command the backward's launch lists and ncu
+    captures are taken with."""
     import torch
 
     from online_softmax_07_gb300 import abi, synth
@@ -679,23 +681,32 @@ def backward_run(args):
     abi.load()
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
-    name = "attn_bf16_b2h16n8192d128_causal"
-    w = synth.WORKLOADS[name]
-    q, k, v = synth.workload_attention_inputs(name)
-    B, H, N, d = q.shape
-    do = synth.attention_inputs(B, H, N, d, seed=97000 + d)[0]
-    tq, tk, tv, tdo = (torch.from_numpy(t).to(dev, torch.bfloat16) for t in (q, k, v, do))
+    if args.backward == "default":
+        name = "attn_bf16_b2h16n8192d128_causal"
+        causal = int(synth.WORKLOADS[name]["causal"])
+        q, k, v = synth.workload_attention_inputs(name)
+        B, H, N, d = q.shape
+        do = synth.attention_inputs(B, H, N, d, seed=97000 + d)[0]
+        tq, tk, tv, tdo = (torch.from_numpy(t).to(dev, torch.bfloat16) for t in (q, k, v, do))
+    else:
+        try:
+            B, H, N, d, causal = (int(x) for x in args.backward.split(","))
+        except ValueError:
+            raise SystemExit("--backward wants B,H,N,d,causal (five integers)")
+        name = f"attn_bf16_b{B}h{H}n{N}d{d}" + ("_causal" if causal else "")
+        tq, tk, tv, tdo = (synth.device_normal((B, H, N, d), seed=98000 + i, dtype=torch.bfloat16)
+                           for i in range(4))
     o = torch.empty_like(tq)
     lse = torch.empty((B, H, N), device=dev)
     scale = 1.0 / math.sqrt(d)
-    abi.fa_fwd_dt(tq, tk, tv, o, lse, B, H, N, d, scale, int(w["causal"]), abi.FA_BF16, stream)
+    abi.fa_fwd_dt(tq, tk, tv, o, lse, B, H, N, d, scale, causal, abi.FA_BF16, stream)
     nbytes = abi.fa_bwd_workspace_bytes(B, H, N)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     gq, gk, gv = torch.empty_like(tq), torch.empty_like(tq), torch.empty_like(tq)
 
     def call():
-        abi.fa_bwd(tq, tk, tv, o, lse, tdo, gq, gk, gv, B, H, N, d, scale, int(w["causal"]), ws,
-                   nbytes, abi.FA_BF16, stream)
+        abi.fa_bwd(tq, tk, tv, o, lse, tdo, gq, gk, gv, B, H, N, d, scale, causal, ws, nbytes,
+                   abi.FA_BF16, stream)
 
     for _ in range(args.warmup):
         call()
@@ -709,7 +720,7 @@ def backward_run(args):
     if abi.fa_last_device_error() != abi.FA_OK:
         raise RuntimeError("device-side error")
     ms = e0.elapsed_time(e1) / args.steps
-    tf = 2.5 * attn_flops(B, H, N, d, True) / (ms * 1e-3) / 1e12
+    tf = 2.5 * attn_flops(B, H, N, d, bool(causal)) / (ms * 1e-3) / 1e12
     print(json.dumps({"workload": name.replace("attn_", "attn_bwd_"), "steps": args.steps,
                       "warmup": args.warmup, "ms": ms, "TFLOP/s": tf}), flush=True)
 
@@ -768,8 +779,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--suite", action="store_true",
                     help="one line per workload instead of the bench line (1 GPU)")
-    ap.add_argument("--backward", action="store_true",
-                    help="time fa_bwd alone on B2 H16 N8192 d128 causal (1 GPU)")
+    ap.add_argument("--backward", nargs="?", const="default", metavar="B,H,N,d,causal",
+                    help="time fa_bwd alone, on B2 H16 N8192 d128 causal or the shape given "
+                         "(1 GPU)")
     ap.add_argument("--forward", metavar="B,H,N,d,causal",
                     help="time the bf16 forward alone on one shape (1 GPU)")
     args = ap.parse_args()
