@@ -20,6 +20,21 @@ __all__ = ["attention_forward", "attention_backward", "row_state", "softmax", "a
            "fa_last_device_error"]
 
 
+def _one_device(ts, what):
+    """Raises unless every tensor in ts lives on the same device."""
+    if any(t.device != ts[0].device for t in ts):
+        raise ValueError(f"{what} must all be on one device")
+
+
+def _check_host_out(t, shape, dtype, name):
+    """A caller-supplied host result buffer must match exactly: the copies out write
+    shape's bytes into it."""
+    if (t.is_cuda or tuple(t.shape) != tuple(shape) or t.dtype != dtype
+            or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous host tensor of shape {tuple(shape)} "
+                         f"and dtype {dtype}")
+
+
 def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=True,
                       out=None, lse_out=None, splits=None):
     """O = softmax(scale * Q K^T) V and LSE for [B, H, N, d] tensors (bf16, fp16 or fp32).
@@ -46,6 +61,7 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float16,
                                                                torch.float32):
         raise ValueError("q, k, v must all be bf16, all fp16 or all fp32")
+    _one_device((q, k, v), "q, k, v")
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -63,8 +79,13 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None, with_lse=T
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if with_lse else None
-        _forward_on_device(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, s)
+        with torch.cuda.device(q.device):
+            _forward_on_device(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, s)
         return o, lse
+    if out is not None:
+        _check_host_out(out, (B, H, N, d), q.dtype, "out")
+    if with_lse and lse_out is not None:
+        _check_host_out(lse_out, (B, H, N), torch.float32, "lse_out")
     return _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype, s)
 
 
@@ -141,9 +162,7 @@ def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtyp
     compute = torch.cuda.current_stream()
     s_in, s_out = _copy_streams(dev)
     s_in.wait_stream(compute)      # device buffers are ordered after earlier work
-    # Four chunks: measured on B2 H16 N8192 d128 as fast as eight (1.30 ms against
-    # 1.73 ms unchunked); sixteen and more are held back by the per-call host overhead.
-    n_chunks = max(1, min(BH, 4))
+    n_chunks = max(1, min(BH, _HOST_CHUNKS))
     bounds = [BH * c // n_chunks for c in range(n_chunks + 1)]
     for c in range(n_chunks):
         h0, h1 = bounds[c], bounds[c + 1]
@@ -184,9 +203,12 @@ def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, stream=N
         raise ValueError("q, k, v, o, dout must be [B, H, N, d] of one shape")
     if any(t.dtype != q.dtype for t in ts) or q.dtype not in (torch.bfloat16, torch.float16):
         raise ValueError("q, k, v, o, dout must all be bf16 or all fp16")
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be fp32 [B, H, N]")
     if not all(t.is_cuda for t in ts) or not lse.is_cuda:
         raise ValueError("attention_backward takes CUDA tensors")
-    B, H, N, d = q.shape
+    _one_device(ts + (lse,), "q, k, v, o, lse, dout")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     q, k, v, o, dout = (t.contiguous() for t in ts)
@@ -195,8 +217,9 @@ def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, stream=N
     ws_bytes = abi.fa_bwd_workspace_bytes(B, H, N)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     dtype = abi.FA_BF16 if q.dtype == torch.bfloat16 else abi.FA_F16
-    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, int(bool(causal)), ws, ws_bytes,
-           dtype)
+    with torch.cuda.device(q.device):
+        fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, int(bool(causal)), ws,
+               ws_bytes, dtype)
     return dq, dk, dv
 
 
@@ -220,7 +243,8 @@ def row_state(x, stream=None):
     rows, length = x.shape
     m = torch.empty(rows, dtype=torch.float32, device=x.device)
     l = torch.empty(rows, dtype=torch.float32, device=x.device)
-    online_softmax_rows(x, m, l, rows, length)
+    with torch.cuda.device(x.device):
+        online_softmax_rows(x, m, l, rows, length)
     if host:
         return m.cpu(), l.cpu()
     return m, l
@@ -240,5 +264,6 @@ def softmax(x, stream=None):
     y = torch.empty_like(x)
     m = torch.empty(rows, dtype=torch.float32, device=x.device)
     l = torch.empty(rows, dtype=torch.float32, device=x.device)
-    online_softmax_forward(x, y, m, l, rows, length)
+    with torch.cuda.device(x.device):
+        online_softmax_forward(x, y, m, l, rows, length)
     return y, m, l
