@@ -225,7 +225,11 @@ fa_status online_softmax_forward(const float* x, float* y, float* m_out, float* 
  * Alignment: bf16/fp16: every pointer but lse 16 bytes, lse 4; fp32: 4 bytes, the
  * workspace 16.  B*H*N == 0 is a no-op (FA_OK).
  * Every output element is written exactly once by one block (no atomics), so results
- * are deterministic.  Errors: FA_ERR_INVALID (null pointer, lse missing, negative size,
+ * are deterministic.  Stream order: the call is ordered on `stream` like a single launch;
+ * inside it (bf16/fp16), the dQ pass runs on an internal stream of the library that forks
+ * from `stream` after the statistics pass and joins it after the dQ pass, so that it can
+ * overlap the dK/dV pass (stream capture sees the fork and the join).  Enqueueing is
+ * serialised across host threads.  Errors: FA_ERR_INVALID (null pointer, lse missing, negative size,
  * scale not finite and > 0, causal not 0/1, workspace too small), FA_ERR_UNSUPPORTED
  * (d or dtype), FA_ERR_ALIGN, FA_ERR_CUDA.
  */

@@ -7,6 +7,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "attn_bwd.cuh"
 #include "fa.h"
@@ -20,6 +21,31 @@ long long bwd_n_pad(int N) { return (static_cast<long long>(N) + kBlockM - 1) / 
 
 // fp32 LSE * log2(e) and fp32 D per (head, padded query row).
 long long bwd_ws_bytes(long long BH, int N) { return 2 * BH * bwd_n_pad(N) * 4; }
+
+// The query-outer pass's stream and its fork / join events, created once per device.
+// Enqueueing is serialised by the mutex, so that each event's latest record is the one
+// the following wait refers to.  Backward calls on different caller streams share the
+// side stream, so their dQ passes run in call order.
+constexpr int kMaxDevices = 64;
+std::mutex g_fork_mu;
+BwdFork g_fork[kMaxDevices];
+bool g_fork_ready[kMaxDevices] = {};
+
+cudaError_t fork_of_current_device(BwdFork** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  BwdFork& f = g_fork[dev];
+  if (!g_fork_ready[dev]) {
+    if ((e = cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    g_fork_ready[dev] = true;
+  }
+  *out = &f;
+  return cudaSuccess;
+}
 
 }  // namespace
 }  // namespace osfa
@@ -98,12 +124,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   float* ws = static_cast<float*>(workspace);
+  std::lock_guard<std::mutex> lock(g_fork_mu);
+  BwdFork* fk = nullptr;
+  if ((e = fork_of_current_device(&fk)) != cudaSuccess) return FA_ERR_CUDA;
   if (d == 64)
-    e = f16 ? launch_attn_bwd<64, true>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream)
-            : launch_attn_bwd<64, false>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream);
+    e = f16 ? launch_attn_bwd<64, true>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream, fk)
+            : launch_attn_bwd<64, false>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream, fk);
   else
-    e = f16 ? launch_attn_bwd<128, true>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream)
-            : launch_attn_bwd<128, false>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream);
+    e = f16 ? launch_attn_bwd<128, true>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream, fk)
+            : launch_attn_bwd<128, false>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream, fk);
   return from_cuda(e);
 }
 

@@ -88,10 +88,19 @@ struct AttnBwdParams {
   float scale_log2;    // scale * log2(e)
 };
 
+// A second stream for the query-outer pass: it forks from the caller's stream after the
+// prep launch and joins it again after the dQ pass, so that dQ blocks take the SMs the
+// key-outer pass's causal tail leaves idle (both passes only read the prep's output and
+// write disjoint gradients).  nullptr: all three launches on the caller's stream.
+struct BwdFork {
+  cudaStream_t side;
+  cudaEvent_t fork, join;
+};
+
 template <int D, bool F16>
 cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const void* o, const void* dout,
                             const float* lse, float* ws, const AttnBwdParams& p,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const BwdFork* fork);
 
 }  // namespace osfa

@@ -841,7 +841,7 @@ template <int D, bool F16>
 cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const void* o, const void* dout,
                             const float* lse, float* ws, const AttnBwdParams& p0,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const BwdFork* fork) {
   using Cfg = AttnBwdCfg<D>;
   static_assert(sizeof(AttnBwdBarriers) <= 512, "barrier block");
   static_assert(Cfg::kSmemBytes <= 227 * 1024 && Cfg::kDqSmemBytes <= 227 * 1024, "shared memory");
@@ -866,10 +866,20 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
       cudaSuccess)
     return e;
   const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.BH) * p.nblk);
+  // The fork point is the prep's completion, recorded before the key-outer launch.
+  if (fork != nullptr && (e = cudaEventRecord(fork->fork, stream)) != cudaSuccess) return e;
   attn_bwd_dkdv_kernel<D, F16><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, stream>>>(tq, tk, tv, tdo, p);
-  return cudaGetLastError();
+  if (fork == nullptr) {
+    attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+    return cudaGetLastError();
+  }
+  if ((e = cudaStreamWaitEvent(fork->side, fork->fork, 0)) != cudaSuccess) return e;
+  attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, fork->side>>>(tq, tk, tv, tdo,
+                                                                                    p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaEventRecord(fork->join, fork->side)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(stream, fork->join, 0);
 }
 
 }  // namespace osfa
