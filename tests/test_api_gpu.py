@@ -186,3 +186,45 @@ def test_row_state_and_softmax_host_and_device():
     assert torch.equal(m.cpu(), m_h)
     rows_sum = y.double().sum(dim=1).cpu().numpy()
     assert np.abs(rows_sum - 1).max() < 1e-5
+
+
+def test_forward_paths_in_cuda_graph():
+    """The forward (plain and split-KV with its combine) and the row kernels captured in
+    one CUDA graph replay to the eager results, bitwise: every launch of the library is
+    stream-ordered and capturable (the first calls, which look up the library's device
+    addresses, are made eagerly before the capture)."""
+    from online_softmax_07_gb300 import abi
+
+    B, H, N, d = 1, 2, 3000, 128
+    q, k, v = (torch.from_numpy(t).to(torch.bfloat16).cuda()
+               for t in synth.attention_inputs(B, H, N, d, seed=2500))
+    x = torch.from_numpy(synth.row_inputs(64, 5000, 2501, 3.0)).cuda()
+    scale = 1.0 / np.sqrt(d)
+    splits = 3
+    nb = abi.fa_fwd_splitkv_workspace_bytes(B, H, N, d, splits)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    outs = dict(o=torch.empty_like(q), lse=torch.empty((B, H, N), device="cuda"),
+                o_s=torch.empty_like(q), lse_s=torch.empty((B, H, N), device="cuda"),
+                m=torch.empty(64, device="cuda"), l=torch.empty(64, device="cuda"))
+
+    def calls(s):
+        abi.fa_fwd_dt(q, k, v, outs["o"], outs["lse"], B, H, N, d, scale, 1, abi.FA_BF16, s)
+        abi.fa_fwd_splitkv(q, k, v, outs["o_s"], outs["lse_s"], B, H, N, d, scale, 1, splits,
+                           ws, nb, abi.FA_BF16, s)
+        abi.online_softmax_rows(x, outs["m"], outs["l"], 64, 5000, s)
+
+    calls(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ref = {key: t.clone() for key, t in outs.items()}
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(graph, stream=s):
+        calls(s)
+    for _ in range(3):
+        for t in outs.values():
+            t.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        for key, t in outs.items():
+            assert torch.equal(t, ref[key]), key
+    assert abi.fa_last_device_error() == abi.FA_OK

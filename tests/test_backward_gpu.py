@@ -212,3 +212,81 @@ def test_backward_from_splitkv_forward():
         _check(name, g4, r)
         # the two differ only through the rounding of O and LSE
         assert np.linalg.norm(g1 - g4) <= 5e-3 * np.linalg.norm(r), name
+
+
+def _bwd_job(B, H, N, d, causal, seed):
+    """Device inputs, forward outputs, workspace and NaN-filled gradient buffers."""
+    import torch
+    q, k, v, do = (to_device(x, torch.bfloat16) for x in _inputs(B, H, N, d, seed))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    abi.fa_fwd_dt(q, k, v, o, lse, B, H, N, d, 1 / np.sqrt(d), int(causal), abi.FA_BF16)
+    nb = abi.fa_bwd_workspace_bytes(B, H, N)
+    return dict(q=q, k=k, v=v, do=do, o=o, lse=lse, B=B, H=H, N=N, d=d, causal=int(causal),
+                nb=nb, ws=torch.empty(nb, dtype=torch.uint8, device="cuda"),
+                g=[torch.full_like(q, float("nan")) for _ in range(3)])
+
+
+def _bwd_call(j, stream):
+    abi.fa_bwd(j["q"], j["k"], j["v"], j["o"], j["lse"], j["do"], *j["g"], j["B"], j["H"], j["N"],
+               j["d"], 1 / np.sqrt(j["d"]), j["causal"], j["ws"], j["nb"], abi.FA_BF16, stream)
+
+
+def test_backward_concurrent_threads():
+    """Three host threads, each with its own stream and inputs, call fa_bwd at the same
+    time: the dQ pass runs on a stream of the library that all calls share, forked from
+    and joined to each caller's stream; every result must equal the sequential one."""
+    import threading
+
+    import torch
+    jobs = [_bwd_job(1, 3, 700 + 130 * t, (64, 128, 64)[t], t % 2, 2300 + t) for t in range(3)]
+    refs = []
+    for j in jobs:
+        _bwd_call(j, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        refs.append([g.clone() for g in j["g"]])
+    ok = [True] * len(jobs)
+
+    def worker(t):
+        j = jobs[t]
+        s = torch.cuda.Stream()
+        for _ in range(8):
+            for g in j["g"]:
+                with torch.cuda.stream(s):
+                    g.fill_(float("nan"))
+            _bwd_call(j, s)
+            s.synchronize()
+            if not all(torch.equal(g, r) for g, r in zip(j["g"], refs[t])):
+                ok[t] = False
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(len(jobs))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert abi.fa_last_device_error() == abi.FA_OK
+    assert all(ok)
+
+
+def test_backward_in_cuda_graph():
+    """A captured fa_bwd (the fork to the library's dQ stream and the join back are part
+    of the capture) replays to the same gradients as the eager call."""
+    import torch
+    j = _bwd_job(2, 2, 900, 128, True, 2400)
+    _bwd_call(j, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ref = [g.clone() for g in j["g"]]
+    for g in j["g"]:
+        g.fill_(float("nan"))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(graph, stream=s):
+        _bwd_call(j, s)
+    for _ in range(3):
+        for g in j["g"]:
+            g.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert all(torch.equal(g, r) for g, r in zip(j["g"], ref))
+    assert abi.fa_last_device_error() == abi.FA_OK
