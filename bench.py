@@ -20,8 +20,8 @@ Printed JSON (one line, rank 0):
   cpu_baseline  the fp64 oracle timed on a bounded sample of the same workload on the
              host cores (rank 0, one GPU only).
 ``--impl reference`` times the oracle alone (see ``reference_arm``); ``--suite``,
-``--backward`` and ``--forward B,H,N,d,causal`` print per-workload lines instead (the
-commands the committed profiles were taken with).
+``--backward [B,H,N,d,causal]``, ``--forward B,H,N,d,causal`` and ``--rows state|softmax``
+print per-workload lines instead (the commands the committed profiles were taken with).
 """
 
 from __future__ import annotations
@@ -769,6 +769,50 @@ def forward_run(args):
           flush=True)
 
 
+def rows_run(args):
+    """The row kernels alone on the 4096 x 32768 fp32 workload (N(0, 9) with the special
+    rows): --rows state times online_softmax_rows, --rows softmax online_softmax_forward
+    (the normalised output), --warmup and --steps calls with CUDA events.  One JSON line;
+    this is the command the row kernels' ncu captures are taken with."""
+    import torch
+
+    from online_softmax_07_gb300 import abi, synth
+    from online_softmax_07_gb300.build import build_library
+
+    if args.rows not in ("state", "softmax"):
+        raise SystemExit("--rows wants state or softmax")
+    build_library()
+    abi.load()
+    stream = torch.cuda.current_stream()
+    x = torch.from_numpy(synth.workload_row_inputs()[0]).cuda()
+    rows, length = x.shape
+    m = torch.empty(rows, device=x.device)
+    l = torch.empty(rows, device=x.device)
+    y = torch.empty_like(x) if args.rows == "softmax" else None
+
+    def call():
+        if y is None:
+            abi.online_softmax_rows(x, m, l, rows, length, stream)
+        else:
+            abi.online_softmax_forward(x, y, m, l, rows, length, stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    # Algorithmic bytes: x read once (+ y written once for the softmax) and m, l.
+    nbytes = rows * length * 4 * (2 if y is not None else 1) + rows * 8
+    print(json.dumps({"workload": f"rows_{rows}x{length} {args.rows}", "steps": args.steps,
+                      "warmup": args.warmup, "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -784,6 +828,8 @@ def main():
                          "(1 GPU)")
     ap.add_argument("--forward", metavar="B,H,N,d,causal",
                     help="time the bf16 forward alone on one shape (1 GPU)")
+    ap.add_argument("--rows", metavar="state|softmax",
+                    help="time a row kernel alone on the 4096 x 32768 workload (1 GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -797,6 +843,9 @@ def main():
         return
     if args.forward:
         forward_run(args)
+        return
+    if args.rows:
+        rows_run(args)
         return
     if world > 1 and args.impl == "ours":
         import torch
