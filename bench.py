@@ -20,7 +20,8 @@ Printed JSON (one line, rank 0):
   cpu_baseline  the fp64 oracle timed on a bounded sample of the same workload on the
              host cores (rank 0, one GPU only).
 ``--impl reference`` times the oracle alone (see ``reference_arm``); ``--suite``,
-``--backward [B,H,N,d,causal]``, ``--forward B,H,N,d,causal`` and ``--rows state|softmax``
+``--backward [B,H,N,d,causal]``, ``--forward B,H,N,d,causal[,splits]`` and
+``--rows state|softmax``
 print per-workload lines instead (the commands the committed profiles were taken with).
 """
 
@@ -726,19 +727,24 @@ def backward_run(args):
 
 
 def forward_run(args):
-    """The attention forward alone on one shape, --forward B,H,N,d,causal (bf16; Q, K, V
-    i.i.d. N(0,1) drawn on the device from fixed seeds): --warmup and --steps fa_fwd_dt
-    calls timed with CUDA events.  One JSON line; this is the command that single-shape
-    launch lists and ncu captures of the forward are taken with."""
+    """The attention forward alone on one shape, --forward B,H,N,d,causal[,splits] (bf16;
+    Q, K, V i.i.d. N(0,1) drawn on the device from fixed seeds): --warmup and --steps
+    fa_fwd_dt calls (fa_fwd_splitkv with a workspace when splits > 1; splits 0 takes
+    fa_fwd_splitkv_default_splits) timed with CUDA events.  One JSON line; this is the
+    command that single-shape launch lists and ncu captures of the forward are taken with."""
     import torch
 
     from online_softmax_07_gb300 import abi, synth
     from online_softmax_07_gb300.build import build_library
 
     try:
-        B, H, N, d, causal = (int(x) for x in args.forward.split(","))
+        vals = [int(x) for x in args.forward.split(",")]
+        B, H, N, d, causal = vals[:5]
+        splits = vals[5] if len(vals) == 6 else 1
+        if len(vals) not in (5, 6) or splits < 0:
+            raise ValueError
     except ValueError:
-        raise SystemExit("--forward wants B,H,N,d,causal (five integers)")
+        raise SystemExit("--forward wants B,H,N,d,causal[,splits] (integers)")
     build_library()
     abi.load()
     stream = torch.cuda.current_stream()
@@ -747,9 +753,17 @@ def forward_run(args):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=q.device)
     scale = 1.0 / math.sqrt(d)
+    if splits == 0:
+        splits = abi.fa_fwd_splitkv_default_splits(B, H, N, causal)
+    nbytes = abi.fa_fwd_splitkv_workspace_bytes(B, H, N, d, splits) if splits > 1 else 0
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
 
     def call():
-        abi.fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, abi.FA_BF16, stream)
+        if splits > 1:
+            abi.fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, splits, ws, nbytes,
+                               abi.FA_BF16, stream)
+        else:
+            abi.fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, abi.FA_BF16, stream)
 
     for _ in range(args.warmup):
         call()
@@ -764,7 +778,8 @@ def forward_run(args):
         raise RuntimeError("device-side error")
     ms = e0.elapsed_time(e1) / args.steps
     name = f"attn_bf16_b{B}h{H}n{N}d{d}" + ("_causal" if causal else "")
-    print(json.dumps({"workload": name, "steps": args.steps, "warmup": args.warmup, "ms": ms,
+    print(json.dumps({"workload": name, "splits": splits, "steps": args.steps,
+                      "warmup": args.warmup, "ms": ms,
                       "TFLOP/s": attn_flops(B, H, N, d, bool(causal)) / (ms * 1e-3) / 1e12}),
           flush=True)
 
@@ -826,8 +841,9 @@ def main():
     ap.add_argument("--backward", nargs="?", const="default", metavar="B,H,N,d,causal",
                     help="time fa_bwd alone, on B2 H16 N8192 d128 causal or the shape given "
                          "(1 GPU)")
-    ap.add_argument("--forward", metavar="B,H,N,d,causal",
-                    help="time the bf16 forward alone on one shape (1 GPU)")
+    ap.add_argument("--forward", metavar="B,H,N,d,causal[,splits]",
+                    help="time the bf16 forward alone on one shape, split-KV with splits > 1 "
+                         "(0: the library's default count) (1 GPU)")
     ap.add_argument("--rows", metavar="state|softmax",
                     help="time a row kernel alone on the 4096 x 32768 workload (1 GPU)")
     args = ap.parse_args()
