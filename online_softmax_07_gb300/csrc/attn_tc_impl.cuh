@@ -106,6 +106,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int n1 = max(0, min(nb1, jlo + chunk) - jlo);
   const int n0 = max(0, min(nb0, jlo + chunk) - jlo);
   const bool split_mode = p.splits > 1;
+  // Split mode: the combine kernel that follows may be scheduled once every block of this
+  // grid has started (it waits for the grid's completion before reading the partials).
+  if (split_mode) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   auto part_row = [&](int r) {  // index of query row r of this head in the partials
     return (static_cast<int64_t>(split) * p.BH + bh) * p.n_pad + r;
   };

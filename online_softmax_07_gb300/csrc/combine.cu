@@ -9,6 +9,11 @@
 //
 // One warp per query row; lane t holds output columns [t * D/32, (t+1) * D/32).  The
 // partials are read once (HBM-bound: splits * (D + 1) * 4 bytes per row).
+//
+// The kernel is a programmatic dependent of the split-mode attention launch: its blocks
+// may be scheduled as the attention blocks drain (the attention kernel signals
+// griddepcontrol.launch_dependents when it starts), and griddepcontrol.wait holds them
+// until the whole attention grid has completed and its partials are visible.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -24,6 +29,7 @@ __global__ void __launch_bounds__(256)
                            void* __restrict__ o, float* __restrict__ lse, int BH, int N,
                            int n_pad, int splits) {
   constexpr int kPer = D / 32;  // columns per lane: 2 or 4
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<int64_t>(BH) * N) return;
@@ -84,19 +90,21 @@ cudaError_t launch_splitkv_combine(const float* ws_o, const float* ws_lse, void*
                                    int BH, int N, int n_pad, int d, int splits, bool f16,
                                    cudaStream_t stream) {
   const long long rows = static_cast<long long>(BH) * N;
-  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
-  if (d == 64) {
-    if (f16)
-      splitkv_combine_kernel<64, true><<<grid, 256, 0, stream>>>(ws_o, ws_lse, o, lse, BH, N, n_pad, splits);
-    else
-      splitkv_combine_kernel<64, false><<<grid, 256, 0, stream>>>(ws_o, ws_lse, o, lse, BH, N, n_pad, splits);
-  } else {
-    if (f16)
-      splitkv_combine_kernel<128, true><<<grid, 256, 0, stream>>>(ws_o, ws_lse, o, lse, BH, N, n_pad, splits);
-    else
-      splitkv_combine_kernel<128, false><<<grid, 256, 0, stream>>>(ws_o, ws_lse, o, lse, BH, N, n_pad, splits);
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (d == 64)
+    return f16 ? cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<64, true>, ws_o, ws_lse, o, lse, BH, N, n_pad, splits)
+               : cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<64, false>, ws_o, ws_lse, o, lse, BH, N, n_pad, splits);
+  return f16 ? cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<128, true>, ws_o, ws_lse, o, lse, BH, N, n_pad, splits)
+             : cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<128, false>, ws_o, ws_lse, o, lse, BH, N, n_pad, splits);
 }
 
 }  // namespace osfa
