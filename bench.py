@@ -678,11 +678,19 @@ def backward_run(args):
     from online_softmax_07_gb300 import abi, synth
     from online_softmax_07_gb300.build import build_library
 
+    shape = None
+    if args.backward != "default":
+        try:
+            shape = tuple(int(x) for x in args.backward.split(","))
+            if len(shape) != 5:
+                raise ValueError
+        except ValueError:
+            raise SystemExit("--backward wants B,H,N,d,causal (five integers)")
     build_library()
     abi.load()
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
-    if args.backward == "default":
+    if shape is None:
         name = "attn_bf16_b2h16n8192d128_causal"
         causal = int(synth.WORKLOADS[name]["causal"])
         q, k, v = synth.workload_attention_inputs(name)
@@ -690,10 +698,7 @@ def backward_run(args):
         do = synth.attention_inputs(B, H, N, d, seed=97000 + d)[0]
         tq, tk, tv, tdo = (torch.from_numpy(t).to(dev, torch.bfloat16) for t in (q, k, v, do))
     else:
-        try:
-            B, H, N, d, causal = (int(x) for x in args.backward.split(","))
-        except ValueError:
-            raise SystemExit("--backward wants B,H,N,d,causal (five integers)")
+        B, H, N, d, causal = shape
         name = f"attn_bf16_b{B}h{H}n{N}d{d}" + ("_causal" if causal else "")
         tq, tk, tv, tdo = (synth.device_normal((B, H, N, d), seed=98000 + i, dtype=torch.bfloat16)
                            for i in range(4))
