@@ -96,7 +96,9 @@ fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float*
  * contiguous chunks processed by separate thread blocks, which raises the parallelism
  * when B * H * ceil(N / 256) is small next to the number of SMs.  Each chunk's result
  * (O normalised by its own denominator, and its LSE) goes to `workspace`; a second
- * kernel merges them by bringing them to a common maximum, as the lihaoran.work
+ * kernel (launched as a programmatic dependent of the first on the same stream, so that
+ * its blocks are placed while the first drains; it reads nothing before the first has
+ * completed) merges them by bringing them to a common maximum, as the lihaoran.work
  * FlashAttention note ("为什么不能平均各块的softmax") and the merge rule of "Softmax
  * 数值稳定性与 IO-Aware Attention" §4.1 prescribe (partial results are not averaged).
  *
