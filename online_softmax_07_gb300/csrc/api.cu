@@ -177,8 +177,9 @@ fa_status run_tc(const void* q, const void* k, const void* v, void* o, float* ls
   p.BH = bh;
   p.nqb = static_cast<int>(nqb);
   // Heads scheduled together: as many as keep their K and V within about 32 MB of the
-  // 129 MB L2 (a sweep of 8-128 MB on GB300: 32 MB as fast as or faster than 64 MB on
-  // every shape measured; 16 MB and below lengthen the causal tail).
+  // 129 MB L2 (a sweep of 8-128 MB on GB300: 32 MB within 1 % of the best budget on every
+  // shape measured, and the one at which B2 H16 N8192 causal reads Q, K and V from DRAM
+  // only once; 16 MB and below lengthen the causal tail).
   const long long kv_head_bytes = 2LL * N * d * 2;
   p.head_group = static_cast<int>(
       std::max(1LL, std::min(BH, (32LL << 20) / std::max(1LL, kv_head_bytes))));
