@@ -118,14 +118,17 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
  * (0 for invalid arguments).  Host-only, no CUDA call. */
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
 
-/* A split count for fa_fwd_splitkv on the current device (SM count from the runtime).
- * Causal: the last query block needs about 2 SMs / blocks times the average work per SM
- * (blocks = B * H * ceil(N/256)); the split count is that ratio rounded down after
- * adding 0.2, so the longest pieces no longer set the time.  Not causal: blocks are of
- * equal length and a split pays only while every piece still runs in the first wave,
- * so SMs / blocks rounded down.  Then at least two K/V tiles per split, at most 64; 1
- * when no split pays or for invalid arguments (causal not 0 or 1).  Host-only apart
- * from reading the SM count. */
+/* A split count for fa_fwd_splitkv on a GPU with `sms` SMs.  Causal: the last query
+ * block needs about 2 SMs / blocks times the average work per SM (blocks = B * H *
+ * ceil(N/256)); the split count is that ratio rounded down after adding 0.2, so the
+ * longest pieces no longer set the time.  Not causal: blocks are of equal length and a
+ * split pays only while every piece still runs in the first wave, so SMs / blocks rounded
+ * down.  Then at least two K/V tiles per split, at most 64; 1 when no split pays or for
+ * invalid arguments (causal not 0 or 1, sms < 1).  Host-only, no CUDA call. */
+int fa_fwd_splitkv_splits_for(int B, int H, int N, int causal, int sms);
+
+/* fa_fwd_splitkv_splits_for with the current device's SM count (read from the runtime);
+ * 1 when the device or its SM count cannot be queried. */
 int fa_fwd_splitkv_default_splits(int B, int H, int N, int causal);
 
 /*

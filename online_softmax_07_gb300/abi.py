@@ -2,6 +2,7 @@
 
 The functions here carry the C names and signatures: ``fa_fwd``, ``fa_fwd_dt``,
 ``fa_fwd_splitkv``, ``fa_fwd_splitkv_workspace_bytes``, ``fa_fwd_splitkv_default_splits``,
+``fa_fwd_splitkv_splits_for``, ``fa_fwd_splitkv_static``, ``fa_bwd``, ``fa_bwd_workspace_bytes``,
 ``fa_fwd_host``, ``fa_fwd_host_workspace_bytes``,
 ``online_softmax_rows``, ``online_softmax_forward``, ``fa_status_str``,
 ``fa_last_device_error`` and ``fa_selftest_wait_timeout``.  Pointer arguments accept a CUDA ``torch.Tensor``
@@ -36,6 +37,7 @@ _SIGNATURES = {
                               + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                                       ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_splitkv_default_splits": (ctypes.c_int, [ctypes.c_int] * 4),
+    "fa_fwd_splitkv_splits_for": (ctypes.c_int, [ctypes.c_int] * 5),
     "fa_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 4
                     + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                        ctypes.c_size_t, ctypes.c_void_p]),
@@ -173,6 +175,10 @@ def fa_fwd_host_workspace_bytes(B, H, N, d, dtype, chunks) -> int:
 
 def fa_fwd_splitkv_default_splits(B, H, N, causal) -> int:
     return int(load().fa_fwd_splitkv_default_splits(B, H, N, int(causal)))
+
+
+def fa_fwd_splitkv_splits_for(B, H, N, causal, sms) -> int:
+    return int(load().fa_fwd_splitkv_splits_for(B, H, N, int(causal), int(sms)))
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,

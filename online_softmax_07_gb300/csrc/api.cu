@@ -130,7 +130,6 @@ const char* fa_status_str(fa_status s) {
 }  // extern "C"
 
 namespace osfa {
-namespace {
 
 // Checks shared by the tensor-core entry points (bf16/fp16, d in {64, 128}).
 fa_status check_tc_args(const void* q, const void* k, const void* v, const void* o,
@@ -148,6 +147,8 @@ fa_status check_tc_args(const void* q, const void* k, const void* v, const void*
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return FA_ERR_ALIGN;
   return FA_OK;
 }
+
+namespace {
 
 long long nqb_of(int N) { return (static_cast<long long>(N) + 2 * kBlockM - 1) / (2 * kBlockM); }
 
@@ -240,11 +241,8 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits
   return static_cast<size_t>(splitkv_ws_bytes(static_cast<long long>(B) * H, N, d, num_splits));
 }
 
-int fa_fwd_splitkv_default_splits(int B, int H, int N, int causal) {
-  if (B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1)) return 1;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+int fa_fwd_splitkv_splits_for(int B, int H, int N, int causal, int sms) {
+  if (B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1) || sms <= 0) return 1;
   const long long blocks = nqb_of(N) * B * H;
   const long long kv_tiles = (static_cast<long long>(N) + kBlockN - 1) / kBlockN;
   // Causal: floor(2 sms / blocks + 0.2), the longest block over the average work per SM;
@@ -254,6 +252,15 @@ int fa_fwd_splitkv_default_splits(int B, int H, int N, int causal) {
   long long s = causal ? (20LL * sms + 2 * blocks) / (10 * blocks) : sms / blocks;
   s = std::min<long long>(s, std::max<long long>(1, kv_tiles / 2));
   return static_cast<int>(std::max<long long>(1, std::min<long long>(s, kMaxSplits)));
+}
+
+int fa_fwd_splitkv_default_splits(int B, int H, int N, int causal) {
+  int dev = 0, sms = 0;
+  // Without the device's SM count no split can be shown to pay: one split.
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return 1;
+  return fa_fwd_splitkv_splits_for(B, H, N, causal, sms);
 }
 
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -38,9 +38,17 @@ cudaError_t fork_of_current_device(BwdFork** out) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   BwdFork& f = g_fork[dev];
   if (!g_fork_ready[dev]) {
-    if ((e = cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    e = cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      // Release what was created, so that a later call starts afresh.
+      if (f.side != nullptr) cudaStreamDestroy(f.side);
+      if (f.fork != nullptr) cudaEventDestroy(f.fork);
+      if (f.join != nullptr) cudaEventDestroy(f.join);
+      f = BwdFork();
+      return e;
+    }
     g_fork_ready[dev] = true;
   }
   *out = &f;

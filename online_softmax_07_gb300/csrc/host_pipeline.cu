@@ -39,6 +39,17 @@ struct HostPipe {
 std::mutex g_mu;
 HostPipe g_pipes[kMaxDevices];
 
+// Destroys whatever streams and events of `p` exist and clears it.
+void release_pipe(HostPipe& p) {
+  if (p.s_in != nullptr) cudaStreamDestroy(p.s_in);
+  if (p.s_out != nullptr) cudaStreamDestroy(p.s_out);
+  if (p.start != nullptr) cudaEventDestroy(p.start);
+  for (int i = 0; i < kSlots; ++i)
+    for (cudaEvent_t ev : {p.in_done[i], p.comp_done[i], p.out_done[i]})
+      if (ev != nullptr) cudaEventDestroy(ev);
+  p = HostPipe();
+}
+
 cudaError_t pipe_of_current_device(HostPipe** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -46,12 +57,16 @@ cudaError_t pipe_of_current_device(HostPipe** out) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   HostPipe& p = g_pipes[dev];
   if (!p.ready) {
-    if ((e = cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming)) != cudaSuccess) return e;
-    for (int i = 0; i < kSlots; ++i)
+    e = cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming);
+    for (int i = 0; i < kSlots && e == cudaSuccess; ++i)
       for (cudaEvent_t* ev : {&p.in_done[i], &p.comp_done[i], &p.out_done[i]})
-        if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      release_pipe(p);  // nothing half-built stays behind; the next call starts afresh
+      return e;
+    }
     p.ready = true;
   }
   *out = &p;

@@ -20,11 +20,13 @@
 #include <mutex>
 
 #include "fa.h"
+#include "host_util.h"
 
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB per device
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 64;  // fa_fwd_splitkv's limit
 
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kStaticScratchBytes];
 
@@ -56,15 +58,17 @@ extern "C" fa_status fa_fwd_splitkv_static(const void* q, const void* k, const v
                                            float* lse, int B, int H, int N, int d, float scale,
                                            int causal, int num_splits, fa_dtype dtype,
                                            cudaStream_t stream) {
-  if (num_splits > 1) {
-    const size_t need = fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits);
-    // 0 means an empty problem or invalid arguments: fa_fwd_splitkv reports which,
-    // without touching the device.
-    if (need == 0)
-      return fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, nullptr, 0,
-                            dtype, stream);
-    if (need > kStaticScratchBytes) return FA_ERR_TOO_LARGE;
-  }
+  // Arguments are checked before anything touches the device.
+  if (num_splits < 1 || num_splits > kMaxSplits) return FA_ERR_INVALID;
+  const fa_status st = osfa::check_tc_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype);
+  if (st != FA_OK) return st;
+  if (static_cast<long long>(B) * H == 0 || N == 0) return FA_OK;  // empty: nothing launched
+  // One split needs no partials, hence no scratch.
+  if (num_splits == 1)
+    return fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, 0, dtype,
+                          stream);
+  if (fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits) > kStaticScratchBytes)
+    return FA_ERR_TOO_LARGE;
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return FA_ERR_CUDA;
   return fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, scratch,

@@ -33,8 +33,8 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
-        assert abi.status_str(code)
+    for code in range(7):
+        assert abi.status_str(code) != "unknown status"
     assert abi.status_str(99) == "unknown status"
 
 
@@ -119,10 +119,11 @@ def test_splitkv_workspace_size(lib):
     assert abi.fa_fwd_splitkv_workspace_bytes(1, 1, 100, 64, 0) == 0      # no splits
 
 
-def test_splitkv_default_splits(lib):
-    """The split-count rule (the same answer with 148 or 152 SMs; without a GPU the
-    library assumes 148).  Query blocks = B * H * ceil(N / 256)."""
-    f = abi.fa_fwd_splitkv_default_splits
+@pytest.mark.parametrize("sms", [148, 152])
+def test_splitkv_split_rule(lib, sms):
+    """The split-count rule (the same answers with 148 or 152 SMs).  Query blocks =
+    B * H * ceil(N / 256)."""
+    f = lambda B, H, N, c: abi.fa_fwd_splitkv_splits_for(B, H, N, c, sms)
     assert f(1, 1, 16384, True) == 4        # causal, 64 blocks: floor(2 * SMs / 64 + 0.2)
     assert f(1, 1, 32768, True) == 2        # causal, 128 blocks
     assert f(1, 5, 8192, True) == 2         # causal, 160 blocks
@@ -133,6 +134,16 @@ def test_splitkv_default_splits(lib):
     assert f(1, 1, 100, False) == 1         # a single K/V tile
     assert f(1, 1, 100000, True) <= 64
     assert f(0, 1, 1024, True) == 1 and f(1, 1, 1024, 2) == 1
+    assert abi.fa_fwd_splitkv_splits_for(1, 1, 16384, 1, 0) == 1     # no SMs: no split
+
+
+def test_splitkv_default_splits_without_a_device(lib):
+    """With no device to read the SM count from, the default is one split."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert abi.fa_fwd_splitkv_default_splits(1, 1, 16384, True) == 1
+
 
 @pytest.mark.parametrize("splits,ws,ws_bytes,expect", [
     (0, FAKE, 1 << 30, abi.FA_ERR_INVALID),
@@ -144,6 +155,29 @@ def test_splitkv_default_splits(lib):
 def test_splitkv_argument_checks(lib, splits, ws, ws_bytes, expect):
     st = lib.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 1000, 128, 0.1, 1, splits, ws,
                             ws_bytes, abi.FA_BF16, None)
+    assert st == expect, abi.status_str(st)
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(splits=0), abi.FA_ERR_INVALID),          # out of range: rejected before any CUDA call
+    (dict(splits=65), abi.FA_ERR_INVALID),
+    (dict(splits=65, B=1, H=64, N=32768), abi.FA_ERR_INVALID),   # not "too large"
+    (dict(d=96), abi.FA_ERR_UNSUPPORTED),          # no workspace size: fa_fwd_splitkv decides
+    (dict(scale=-1.0), abi.FA_ERR_INVALID),
+    (dict(B=0), abi.FA_OK),                        # empty problem: nothing launched
+    (dict(N=0), abi.FA_OK),
+    (dict(H=64, N=32768), abi.FA_ERR_TOO_LARGE),   # 2 splits need ~1.1 GB of partials
+    (dict(H=64, N=32768, scale=float("nan")), abi.FA_ERR_INVALID),   # argument errors first
+    (dict(H=64, N=32768, q=None), abi.FA_ERR_INVALID),
+    (dict(H=64, N=32768, k=FAKE + 8), abi.FA_ERR_ALIGN),
+])
+def test_splitkv_static_argument_checks(lib, args, expect):
+    """The scratch-memory split-KV entry checks its arguments on the host; none of these
+    cases touches the device."""
+    a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, H=1, N=1000, d=128, scale=0.1, splits=2)
+    a.update(args)
+    st = lib.fa_fwd_splitkv_static(a["q"], a["k"], a["v"], FAKE, None, a["B"], a["H"], a["N"],
+                                   a["d"], a["scale"], 1, a["splits"], abi.FA_BF16, None)
     assert st == expect, abi.status_str(st)
 
 
