@@ -373,11 +373,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           Cfg::kTripleS
               ? tbase + lane_off + static_cast<uint32_t>(((t ? min(j + 1, n0) + j : 2 * j) % 3) * 128)
               : tS_fixed;
+      // S_t(j) and its row maximum: the TMEM load reduces the 128 values it brings in.
       uint32_t sr[128];
-      tmem_ld128_wait(tS, sr);
+      float rowmax;
+      tmem_ld128_max_wait(tS, sr, rowmax);
       float* s = reinterpret_cast<float*>(sr);
 
-      // Mask: keys >= N (ragged last tile) and, on the diagonal tile, keys > row.
+      // Mask: keys >= N (ragged last tile) and, on the diagonal tile, keys > row.  (The
+      // condition is the same for the whole warp.)  The loaded maximum counted the masked
+      // keys, so it is taken again over the kept ones: four chains of three-input max.
       const int key0 = (jlo + j) * kBlockN;
       const bool diag = p.causal && (key0 + kBlockN - 1 > r0);
       if (diag || key0 + kBlockN > p.N) {
@@ -385,13 +389,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (p.causal) lim = min(lim, r0 + rr - key0);
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
-      }
-
-      // Row max: four independent chains of three-input max.
-      float mx[4] = {s[0], s[1], s[2], s[3]};
+        float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int c = 4; c < 128; c += 2) mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], s[c], s[c + 1]);
-      const float rowmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+        for (int c = 4; c < 128; c += 2)
+          mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], s[c], s[c + 1]);
+        rowmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      }
       const float m2_new = fmaxf(m2, rowmax * sl2);
       const float m2_use = (m2_new > m2 + kRescaleLog2) ? m2_new : m2;
       const float alpha = ex2_approx(m2 - m2_use);  // 1 if unchanged, 0 on the first tile
