@@ -53,6 +53,7 @@ struct AttnTcCfg {
   static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D bf16
   static constexpr int kSlots = (D == 128) ? 5 : 8;       // K/V ring depth
+  static constexpr bool kPairWait = (D == 64);  // one landing barrier per K/V pair
   static constexpr int kSmemQ0 = 0;
   static constexpr int kSmemQ1 = kTileBytes;
   static constexpr int kSmemSlots = 2 * kTileBytes;

@@ -8,6 +8,9 @@
 
 namespace osfa {
 
+// K/V pairs tracked at once (kv_full barriers); more than the ring holds.
+constexpr int kKvBars = 8;
+
 struct AttnTcBarriers {
   uint64_t q_full;
   // s_full and p_ready come in pairs per tile, used alternately: S_t(j) completes on
@@ -21,7 +24,12 @@ struct AttnTcBarriers {
   uint64_t o_final[2];   // MMA -> softmax t: last P_t V product done
   uint64_t pv_done[2];   // MMA -> softmax t: P_t V of a K/V tile done (three-buffer mode)
   uint64_t mma_drain;    // MMA thread: all of its MMAs finished (before TMEM is freed)
-  uint64_t slot_full[8];
+  // Landing of the K/V loads.  d = 64 (kPairWait): K_j and V_j both land on
+  // kv_full[j % 8], so one wait covers the pair.  d = 128: each ring slot has its own
+  // full barrier (kv_full[slot]): the MMA warp waits for K_{j+1} without waiting for
+  // V_{j+1}, which the 5-slot ring may load a tile later.  Each ring slot is released on
+  // its own (slot_empty) when the products reading it are done.
+  uint64_t kv_full[8];
   uint64_t slot_empty[8];
   uint32_t tmem_base;
   int abort;
@@ -135,10 +143,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(smem_u32(&bars->pv_done[t]), 1);
     }
     mbar_init(smem_u32(&bars->mma_drain), 1);
-    for (int s = 0; s < Cfg::kSlots; ++s) {
-      mbar_init(smem_u32(&bars->slot_full[s]), 1);
-      mbar_init(smem_u32(&bars->slot_empty[s]), 1);
-    }
+    for (int u = 0; u < kKvBars; ++u) mbar_init(smem_u32(&bars->kv_full[u]), 1);
+    for (int s = 0; s < Cfg::kSlots; ++s) mbar_init(smem_u32(&bars->slot_empty[s]), 1);
     bars->abort = 0;
     mbar_init_fence();
   }
@@ -173,28 +179,51 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_load_3d(sbase + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0) + b * kBoxBytes, &tm_q, qbar,
                       b * kBoxCols, qb * 2 * kBlockM + t * kBlockM, bh);
+      // Load it: K_j at it = 2j, V_j at 2j + 1, into ring slot it % kSlots once the slot's
+      // previous load has been consumed.  kPairWait: both tiles of pair j complete
+      // kv_full[j % kKvBars] (armed for both when K_j is issued); else load it completes
+      // kv_full[slot].
       int issued = 0;
       const int nload = 2 * n1;  // K_j, V_j for j < n1 (tile 1 needs the most)
       for (int it = 0; it < nload; ++it) {
         const int slot = it % Cfg::kSlots;
         const int phase = (it / Cfg::kSlots) & 1;
         if (!mbar_wait(smem_u32(&bars->slot_empty[slot]), phase ^ 1, abort, p.status)) break;
-        const uint32_t full = smem_u32(&bars->slot_full[slot]);
-        mbar_arrive_expect_tx(full, Cfg::kTileBytes);
+        const int j = it >> 1;
+        uint32_t full;
+        if constexpr (Cfg::kPairWait) {
+          full = smem_u32(&bars->kv_full[j % kKvBars]);
+          if ((it & 1) == 0) mbar_arrive_expect_tx(full, 2 * Cfg::kTileBytes);
+        } else {
+          full = smem_u32(&bars->kv_full[slot]);
+          mbar_arrive_expect_tx(full, Cfg::kTileBytes);
+        }
         const CUtensorMap* tm = (it & 1) ? &tm_v : &tm_k;
         const uint32_t dst = sbase + Cfg::kSmemSlots + slot * Cfg::kTileBytes;
 #pragma unroll
         for (int b = 0; b < Cfg::kBoxes; ++b)
-          tma_load_3d(dst + b * kBoxBytes, tm, full, b * kBoxCols, (jlo + (it >> 1)) * kBlockN, bh);
+          tma_load_3d(dst + b * kBoxBytes, tm, full, b * kBoxCols, (jlo + j) * kBlockN, bh);
         issued = it + 1;
       }
-      // Every issued copy must land before the block's shared memory goes away: wait
-      // for the last load issued into each slot.
+      // Every issued copy must land before the block's shared memory goes away.
       int no_abort = 0;
       mbar_wait(qbar, 0, &no_abort, p.status);
-      for (int it = max(0, issued - Cfg::kSlots); it < issued; ++it)
-        mbar_wait(smem_u32(&bars->slot_full[it % Cfg::kSlots]), (it / Cfg::kSlots) & 1, &no_abort,
-                  p.status);
+      if constexpr (Cfg::kPairWait) {
+        // If the loop gave up between K_j and V_j, V_j's bytes are counted as arrived so
+        // that pair j's phase completes once K_j has landed; then wait for the pairs whose
+        // copies may still be in flight (the ring holds fewer than kKvBars pairs, so older
+        // ones have been consumed).
+        if (issued & 1)
+          mbar_complete_tx(smem_u32(&bars->kv_full[(issued >> 1) % kKvBars]), Cfg::kTileBytes);
+        const int pairs = (issued + 1) >> 1;
+        for (int j = max(0, pairs - kKvBars); j < pairs; ++j)
+          mbar_wait(smem_u32(&bars->kv_full[j % kKvBars]), (j / kKvBars) & 1, &no_abort, p.status);
+      } else {
+        // The last load issued into each slot.
+        for (int it = max(0, issued - Cfg::kSlots); it < issued; ++it)
+          mbar_wait(smem_u32(&bars->kv_full[it % Cfg::kSlots]), (it / Cfg::kSlots) & 1, &no_abort,
+                    p.status);
+      }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -214,31 +243,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     auto slot_off16 = [](int it) {
       return static_cast<uint64_t>(((it % Cfg::kSlots) * Cfg::kTileBytes) >> 4);
     };
-    auto wait_full = [&](int it) {
-      return mbar_wait(smem_u32(&bars->slot_full[it % Cfg::kSlots]), (it / Cfg::kSlots) & 1,
-                       abort, p.status);
+    // K_j and V_j have landed (kPairWait).
+    auto wait_kv = [&](int j) {
+      return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->kv_full[j % kKvBars]),
+                                               (j / kKvBars) & 1, abort, p.status));
     };
-    // S_t = Q_t K^T: K-major A and B, 16 columns (32 bytes) of d per instruction.
+    // Load `it` of the ring has landed (per-slot barriers).
+    auto wait_full = [&](int it) {
+      return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->kv_full[it % Cfg::kSlots]),
+                                               (it / Cfg::kSlots) & 1, abort, p.status));
+    };
+    // S_t = Q_t K^T: K-major A and B, 16 columns (32 bytes) of d per instruction, all
+    // issued under one elect.
     auto issue_s = [&](uint32_t tS, uint64_t dQ, int itK) {
       const uint64_t dK = dSlot0K + slot_off16(itK);
+      uint64_t a[D / 16], b[D / 16];
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_elect(tS, dQ + off16, dK + off16, kIdescS, kk > 0 ? 1u : 0u);
+        a[kk] = dQ + off16;
+        b[kk] = dK + off16;
       }
+      if constexpr (D == 64) mma_ss4_elect(tS, a, b, kIdescS, 0u);
+      else mma_ss8_elect(tS, a, b, kIdescS, 0u);
     };
     // O_t += P_t V: P from TMEM (bf16 packed two per column), V MN-major in shared
-    // memory; 16 keys (2 KB of the V tile) per instruction.
+    // memory; 16 keys (2 KB of the V tile) per instruction, all under one elect.
     auto issue_pv = [&](uint32_t tO, uint32_t tP, int itV, bool acc) {
+      static_assert(kBlockN == 128, "eight 16-key products per P V");
       const uint64_t dV = dSlot0V + slot_off16(itV);
+      uint32_t a[8];
+      uint64_t b[8];
 #pragma unroll
-      for (int kk = 0; kk < kBlockN / 16; ++kk)
-        mma_bf16_ts_elect(tO, tP + kk * 8, dV + ((kk * 2048) >> 4), kIdescPV,
-                          (acc || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < 8; ++kk) {
+        a[kk] = tP + kk * 8;
+        b[kk] = dV + ((kk * 2048) >> 4);
+      }
+      mma_ts8_elect(tO, a, b, kIdescPV, acc ? 1u : 0u);
     };
 
-    bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort, p.status) && wait_full(0);
-    ok = __all_sync(0xffffffffu, ok);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->q_full), 0, abort, p.status));
+    if constexpr (Cfg::kPairWait) ok = ok && wait_kv(0);
+    else ok = ok && wait_full(0);
     if constexpr (Cfg::kTripleS) {
       // Three S/P buffers in rotation: the S issued at position pos of the sequence
       // S_0(0), S_1(0), S_0(1), S_1(1), ... (S_0(j) at 2j, S_1(j) at min(j+1, n0) + j once
@@ -264,13 +310,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       for (int j = 0; ok && j < n1; ++j) {
         const int itV = 2 * j + 1, itK = 2 * j + 2;
-        if (!(ok = __all_sync(0xffffffffu, wait_full(itV)))) break;
-        bool k_ready = false;
+        // K_{j+1} (and V_{j+1}); V_j landed with K_j.
+        if (j + 1 < n1) {
+          if (!(ok = wait_kv(j + 1))) break;
+          tc_fence_after();
+        }
         if (j < n0) {
           if (j + 1 < n0) {
-            if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
-            k_ready = true;
-            tc_fence_after();
             issue_s(colS(2 * j + 2), dQ0, itK);
             mma_commit_elect(smem_u32(&bars->s_full[(j + 1) & 1]));
           }
@@ -280,10 +326,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (j + 1 == n0) mma_commit_elect(smem_u32(&bars->o_final[0]));
         }
         if (j + 1 < n1) {
-          if (!k_ready) {
-            if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
-            tc_fence_after();
-          }
           issue_s(colS(min(j + 2, n0) + j + 1), dQ1, itK);
           mma_commit_elect(smem_u32(&bars->s_full[2 + ((j + 1) & 1)]));
           mma_commit_elect(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
@@ -307,7 +349,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       for (int j = 0; ok && j < n1; ++j) {
         const int itV = 2 * j + 1, itK = 2 * j + 2;
-        if (!(ok = __all_sync(0xffffffffu, wait_full(itV)))) break;
+        if (!(ok = wait_full(itV))) break;
+        bool k_ready = false;
         if (j < n0) {
           if (!(ok = __all_sync(0xffffffffu,
                                 mbar_wait(smem_u32(&bars->p_ready[j & 1]), (j >> 1) & 1, abort,
@@ -316,7 +359,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tc_fence_after();
           issue_pv(tO0, tS0, itV, j > 0);
           if (j + 1 < n0) {
-            if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
+            if (!(ok = wait_full(itK))) break;
+            k_ready = true;
             tc_fence_after();
             issue_s(tS0, dQ0, itK);
             mma_commit_elect(smem_u32(&bars->s_full[(j + 1) & 1]));
@@ -332,8 +376,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         issue_pv(tO1, tS1, itV, j > 0);
         mma_commit_elect(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
         if (j + 1 < n1) {
-          if (!(ok = __all_sync(0xffffffffu, wait_full(itK)))) break;
-          tc_fence_after();
+          if (!k_ready) {
+            if (!(ok = wait_full(itK))) break;
+            tc_fence_after();
+          }
           issue_s(tS1, dQ1, itK);
           mma_commit_elect(smem_u32(&bars->s_full[2 + ((j + 1) & 1)]));
           mma_commit_elect(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));

@@ -47,6 +47,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Counts `bytes` of the barrier's expected transaction bytes as arrived without a copy
+// (used when an expected copy is not issued after all).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -197,6 +203,71 @@ __device__ __forceinline__ void mma_bf16_ts_elect(uint32_t d_tmem, uint32_t a_tm
       "setp.ne.b32 q, %4, 0;\n\t"
       "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+
+// 4 tcgen05.mma (A and B from shared memory) into one accumulator under a single
+// elect.sync: a[k], b[k] are the k-th operand descriptors; the first product accumulates
+// when `acc` is non-zero, the others always.
+__device__ __forceinline__ void mma_ss4_elect(uint32_t d_tmem, const uint64_t* a, const uint64_t* b,
+                                                uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %2, 0;\n\t"
+      "setp.eq.b32 t, %2, %2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %1, f;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %1, t;\n\t"
+      "}"
+      :: "r"(d_tmem), "r"(idesc), "r"(acc), "l"(a[0]), "l"(b[0]), "l"(a[1]), "l"(b[1]), "l"(a[2]), "l"(b[2]), "l"(a[3]), "l"(b[3])
+      : "memory");
+}
+
+// 8 tcgen05.mma (A and B from shared memory) into one accumulator under a single
+// elect.sync: a[k], b[k] are the k-th operand descriptors; the first product accumulates
+// when `acc` is non-zero, the others always.
+__device__ __forceinline__ void mma_ss8_elect(uint32_t d_tmem, const uint64_t* a, const uint64_t* b,
+                                                uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %2, 0;\n\t"
+      "setp.eq.b32 t, %2, %2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %1, f;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %11, %12, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %13, %14, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %15, %16, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %17, %18, %1, t;\n\t"
+      "}"
+      :: "r"(d_tmem), "r"(idesc), "r"(acc), "l"(a[0]), "l"(b[0]), "l"(a[1]), "l"(b[1]), "l"(a[2]), "l"(b[2]), "l"(a[3]), "l"(b[3]), "l"(a[4]), "l"(b[4]), "l"(a[5]), "l"(b[5]), "l"(a[6]), "l"(b[6]), "l"(a[7]), "l"(b[7])
+      : "memory");
+}
+
+// 8 tcgen05.mma (A from TMEM, B from shared memory) into one accumulator under a single
+// elect.sync; a[k]: TMEM address of the k-th A operand, b[k]: descriptor of the k-th B.
+__device__ __forceinline__ void mma_ts8_elect(uint32_t d_tmem, const uint32_t* a, const uint64_t* b,
+                                                uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %2, 0;\n\t"
+      "setp.eq.b32 t, %2, %2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %1, f;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], %12, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%13], %14, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%15], %16, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%17], %18, %1, t;\n\t"
+      "}"
+      :: "r"(d_tmem), "r"(idesc), "r"(acc), "r"(a[0]), "l"(b[0]), "r"(a[1]), "l"(b[1]), "r"(a[2]), "l"(b[2]), "r"(a[3]), "l"(b[3]), "r"(a[4]), "l"(b[4]), "r"(a[5]), "l"(b[5]), "r"(a[6]), "l"(b[6]), "r"(a[7]), "l"(b[7])
       : "memory");
 }
 
