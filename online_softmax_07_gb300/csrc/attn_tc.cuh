@@ -20,10 +20,11 @@
 //  * each softmax thread owns one query row of its tile (TMEM lane = row), so row max
 //    and row sum need no shuffles;
 //  * the rescale reference m is moved only when a row's maximum grows by more than
-//    2^8 (kRescaleLog2); between moves alpha = 1 and the O rescale is skipped.  The
-//    identity behind the merge rule holds for any common reference, so O and LSE are
-//    the same in exact arithmetic; P then lies in [0, 2^8] instead of [0, 1], which
-//    bf16 and fp32 represent with the same relative precision.
+//    a factor 2^64 for bf16 (2^8 for fp16; kRescaleLog2); between moves alpha = 1 and
+//    the O rescale is skipped.  The identity behind the merge rule holds for any common
+//    reference, so O and LSE are the same in exact arithmetic; P then lies in
+//    [0, 2^64] instead of [0, 1], which bf16 and fp32 represent with the same relative
+//    precision.
 #pragma once
 
 #include <cstdint>
@@ -45,7 +46,12 @@ constexpr int kRegsSoftmax = 208;  // per thread, softmax warpgroups
 constexpr int kRegsIssue = 88;     // per thread, MMA / TMA warpgroup (384 x 168 = 256 x 208 + 128 x 88)
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
-constexpr float kRescaleLog2 = 8.0f;
+// Lazy rescale threshold in log2 units: P = 2^(s' - m) stays below 2^kRescaleLog2.  bf16
+// holds any such P to the same relative precision (its range reaches 2^127), so the
+// reference moves only for growth beyond 2^64 (sums of up to 2^17 such terms times |v|
+// stay far inside fp32); fp16 P must stay below 65504, so 2^8 there.
+template <bool F16>
+constexpr float kRescaleLog2 = F16 ? 8.0f : 64.0f;
 
 template <int D>
 struct AttnTcCfg {

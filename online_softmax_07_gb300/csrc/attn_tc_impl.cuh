@@ -28,9 +28,12 @@ struct AttnTcBarriers {
   // kv_full[j % 8], so one wait covers the pair.  d = 128: each ring slot has its own
   // full barrier (kv_full[slot]): the MMA warp waits for K_{j+1} without waiting for
   // V_{j+1}, which the 5-slot ring may load a tile later.  Each ring slot is released on
-  // its own (slot_empty) when the products reading it are done.
+  // its own (slot_empty) when the products reading it are done, except with kPairWait,
+  // where the ring is deep enough to release both slots of pair j once, after the last
+  // product reading the pair (kv_empty[j % 8]).
   uint64_t kv_full[8];
   uint64_t slot_empty[8];
+  uint64_t kv_empty[8];  // kPairWait: both slots of pair j released at once
   uint32_t tmem_base;
   int abort;
 };
@@ -143,7 +146,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(smem_u32(&bars->pv_done[t]), 1);
     }
     mbar_init(smem_u32(&bars->mma_drain), 1);
-    for (int u = 0; u < kKvBars; ++u) mbar_init(smem_u32(&bars->kv_full[u]), 1);
+    for (int u = 0; u < kKvBars; ++u) {
+      mbar_init(smem_u32(&bars->kv_full[u]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[u]), 1);
+    }
     for (int s = 0; s < Cfg::kSlots; ++s) mbar_init(smem_u32(&bars->slot_empty[s]), 1);
     bars->abort = 0;
     mbar_init_fence();
@@ -179,47 +185,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_load_3d(sbase + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0) + b * kBoxBytes, &tm_q, qbar,
                       b * kBoxCols, qb * 2 * kBlockM + t * kBlockM, bh);
-      // Load it: K_j at it = 2j, V_j at 2j + 1, into ring slot it % kSlots once the slot's
-      // previous load has been consumed.  kPairWait: both tiles of pair j complete
-      // kv_full[j % kKvBars] (armed for both when K_j is issued); else load it completes
-      // kv_full[slot].
-      int issued = 0;
-      const int nload = 2 * n1;  // K_j, V_j for j < n1 (tile 1 needs the most)
-      for (int it = 0; it < nload; ++it) {
-        const int slot = it % Cfg::kSlots;
-        const int phase = (it / Cfg::kSlots) & 1;
-        if (!mbar_wait(smem_u32(&bars->slot_empty[slot]), phase ^ 1, abort, p.status)) break;
-        const int j = it >> 1;
-        uint32_t full;
-        if constexpr (Cfg::kPairWait) {
-          full = smem_u32(&bars->kv_full[j % kKvBars]);
-          if ((it & 1) == 0) mbar_arrive_expect_tx(full, 2 * Cfg::kTileBytes);
-        } else {
-          full = smem_u32(&bars->kv_full[slot]);
-          mbar_arrive_expect_tx(full, Cfg::kTileBytes);
-        }
-        const CUtensorMap* tm = (it & 1) ? &tm_v : &tm_k;
-        const uint32_t dst = sbase + Cfg::kSmemSlots + slot * Cfg::kTileBytes;
-#pragma unroll
-        for (int b = 0; b < Cfg::kBoxes; ++b)
-          tma_load_3d(dst + b * kBoxBytes, tm, full, b * kBoxCols, (jlo + j) * kBlockN, bh);
-        issued = it + 1;
-      }
-      // Every issued copy must land before the block's shared memory goes away.
       int no_abort = 0;
-      mbar_wait(qbar, 0, &no_abort, p.status);
       if constexpr (Cfg::kPairWait) {
-        // If the loop gave up between K_j and V_j, V_j's bytes are counted as arrived so
-        // that pair j's phase completes once K_j has landed; then wait for the pairs whose
-        // copies may still be in flight (the ring holds fewer than kKvBars pairs, so older
-        // ones have been consumed).
-        if (issued & 1)
-          mbar_complete_tx(smem_u32(&bars->kv_full[(issued >> 1) % kKvBars]), Cfg::kTileBytes);
-        const int pairs = (issued + 1) >> 1;
-        for (int j = max(0, pairs - kKvBars); j < pairs; ++j)
+        // Pair j: K_j into ring slot 2j % kSlots and V_j into the next slot, both landing
+        // on kv_full[j % kKvBars], once pair j - kSlots / 2 (the previous occupant of both
+        // slots) has been released.
+        static_assert(Cfg::kSlots % 2 == 0, "pairs of slots");
+        int issued = 0;
+        for (int j = 0; j < n1; ++j) {
+          const int jp = j - Cfg::kSlots / 2;
+          if (jp >= 0 && !mbar_wait(smem_u32(&bars->kv_empty[jp % kKvBars]), (jp / kKvBars) & 1,
+                                    abort, p.status))
+            break;
+          const uint32_t full = smem_u32(&bars->kv_full[j % kKvBars]);
+          mbar_arrive_expect_tx(full, 2 * Cfg::kTileBytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t dst =
+                sbase + Cfg::kSmemSlots + ((2 * j + h) % Cfg::kSlots) * Cfg::kTileBytes;
+#pragma unroll
+            for (int b = 0; b < Cfg::kBoxes; ++b)
+              tma_load_3d(dst + b * kBoxBytes, h ? &tm_v : &tm_k, full, b * kBoxCols,
+                          (jlo + j) * kBlockN, bh);
+          }
+          issued = j + 1;
+        }
+        // Every issued copy must land before the block's shared memory goes away: the
+        // pairs not yet known to be released (the ring holds fewer than kKvBars pairs).
+        mbar_wait(qbar, 0, &no_abort, p.status);
+        for (int j = max(0, issued - kKvBars); j < issued; ++j)
           mbar_wait(smem_u32(&bars->kv_full[j % kKvBars]), (j / kKvBars) & 1, &no_abort, p.status);
       } else {
-        // The last load issued into each slot.
+        // Load it: K_j at it = 2j, V_j at 2j + 1, into ring slot it % kSlots once the
+        // slot's previous load has been consumed; load it completes kv_full[slot].
+        int issued = 0;
+        const int nload = 2 * n1;  // K_j, V_j for j < n1 (tile 1 needs the most)
+        for (int it = 0; it < nload; ++it) {
+          const int slot = it % Cfg::kSlots;
+          const int phase = (it / Cfg::kSlots) & 1;
+          if (!mbar_wait(smem_u32(&bars->slot_empty[slot]), phase ^ 1, abort, p.status)) break;
+          const uint32_t full = smem_u32(&bars->kv_full[slot]);
+          mbar_arrive_expect_tx(full, Cfg::kTileBytes);
+          const CUtensorMap* tm = (it & 1) ? &tm_v : &tm_k;
+          const uint32_t dst = sbase + Cfg::kSmemSlots + slot * Cfg::kTileBytes;
+#pragma unroll
+          for (int b = 0; b < Cfg::kBoxes; ++b)
+            tma_load_3d(dst + b * kBoxBytes, tm, full, b * kBoxCols, (jlo + (it >> 1)) * kBlockN, bh);
+          issued = it + 1;
+        }
+        // Every issued copy must land before the block's shared memory goes away: the
+        // last load issued into each slot.
+        mbar_wait(qbar, 0, &no_abort, p.status);
         for (int it = max(0, issued - Cfg::kSlots); it < issued; ++it)
           mbar_wait(smem_u32(&bars->kv_full[it % Cfg::kSlots]), (it / Cfg::kSlots) & 1, &no_abort,
                     p.status);
@@ -306,7 +322,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         issue_s(colS(n0 > 0 ? 1 : 0), dQ1, 0);
         mma_commit_elect(smem_u32(&bars->s_full[2]));
-        mma_commit_elect(smem_u32(&bars->slot_empty[0]));
       }
       for (int j = 0; ok && j < n1; ++j) {
         const int itV = 2 * j + 1, itK = 2 * j + 2;
@@ -328,12 +343,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (j + 1 < n1) {
           issue_s(colS(min(j + 2, n0) + j + 1), dQ1, itK);
           mma_commit_elect(smem_u32(&bars->s_full[2 + ((j + 1) & 1)]));
-          mma_commit_elect(smem_u32(&bars->slot_empty[itK % Cfg::kSlots]));
         }
         if (!(ok = wait_bar(&bars->p_ready[2 + (j & 1)], (j >> 1) & 1))) break;
         issue_pv(tO1, colS(min(j + 1, n0) + j), itV, j > 0);
         mma_commit_elect(smem_u32(&bars->pv_done[1]));
-        mma_commit_elect(smem_u32(&bars->slot_empty[itV % Cfg::kSlots]));
+        // P_1(j) V is the last product reading K_j or V_j.
+        mma_commit_elect(smem_u32(&bars->kv_empty[j % kKvBars]));
         if (j + 1 == n1) mma_commit_elect(smem_u32(&bars->o_final[1]));
       }
     } else {
@@ -442,7 +457,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         rowmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       }
       const float m2_new = fmaxf(m2, rowmax * sl2);
-      const float m2_use = (m2_new > m2 + kRescaleLog2) ? m2_new : m2;
+      const float m2_use = (m2_new > m2 + kRescaleLog2<F16>) ? m2_new : m2;
       const float alpha = ex2_approx(m2 - m2_use);  // 1 if unchanged, 0 on the first tile
 
       // Rescale O_t by alpha.  S_t(j) complete implies P_t(j-1) V done (one issuing

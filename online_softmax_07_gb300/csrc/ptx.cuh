@@ -47,12 +47,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Counts `bytes` of the barrier's expected transaction bytes as arrived without a copy
-// (used when an expected copy is not issued after all).
-__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -47,19 +47,34 @@ def test_bf16_large_logits_rescales(d, causal):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_bf16_growing_logits_force_every_rescale(d):
-    """Keys whose scores grow along the sequence: every tile raises the row max by
-    more than the lazy-rescale threshold, so the O rescale runs on every tile."""
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_growing_logits_force_every_rescale(d, dtype):
+    """Keys whose scores grow along the sequence: every 128-key tile raises the row max
+    by 48 (natural log units), more than the kernel's lazy-rescale thresholds (64 log2
+    units = 44.4 for bf16, 8 for fp16), so the O rescale runs on every tile."""
     N = 1024
-    q, k, v = synth.attention_inputs(1, 1, N, d, seed=72000 + d)
-    q[...] = synth.round_to_bf16(np.abs(q) * 0 + 1.0)             # q = (1, ..., 1)
-    ramp = (np.arange(N, dtype=np.float32) / 128.0) * 2.0        # +2 per 128 keys
-    k = synth.round_to_bf16(k * 0.1 + ramp[None, None, :, None] / math.sqrt(d))
+    rnd = synth.round_to_bf16 if dtype == "bf16" else synth.round_to_f16
+    q, k, v = synth.attention_inputs(1, 1, N, d, seed=72000 + d, dtype=dtype)
+    q[...] = rnd(np.abs(q) * 0 + 1.0)                            # q = (1, ..., 1)
+    ramp = (np.arange(N, dtype=np.float32) / 128.0) * 6.0        # +6 per 128 keys
+    k = rnd(k * 0.1 + ramp[None, None, :, None] / math.sqrt(d))
     scale = 1.0 / math.sqrt(d) * 8.0
     for causal in (False, True):
-        o, lse = run_attention(q, k, v, scale, causal)
+        o, lse = run_attention(q, k, v, scale, causal, dtype=dtype)
         o_ref, lse_ref = oracle.attention_forward(q, k, v, scale, causal)
-        check_attention(o, lse, o_ref, lse_ref)
+        check_attention(o, lse, o_ref, lse_ref, dtype=dtype)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_f16_large_logits_rescales(d):
+    """fp16 with Q standard deviation 4 (its lazy-rescale threshold is 2^8, so the
+    reference moves often) against the oracle."""
+    q, k, v = synth.attention_inputs(1, 2, 900, d, seed=71500 + d, dtype="f16", q_std=4.0)
+    scale = 1.0 / math.sqrt(d)
+    for causal in (False, True):
+        o, lse = run_attention(q, k, v, scale, causal, dtype="f16")
+        o_ref, lse_ref = oracle.attention_forward(q, k, v, scale, causal)
+        check_attention(o, lse, o_ref, lse_ref, dtype="f16")
 
 
 def test_bf16_scale_and_batch_layout():
