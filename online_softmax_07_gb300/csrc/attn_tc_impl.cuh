@@ -22,7 +22,7 @@ struct AttnTcBarriers {
   uint64_t s_full[4];    // MMA -> softmax t: S_t of a K/V tile is in TMEM
   uint64_t p_ready[4];   // softmax t -> MMA: P_t stored in TMEM and O_t rescaled
   uint64_t o_final[2];   // MMA -> softmax t: last P_t V product done
-  uint64_t pv_done[2];   // MMA -> softmax t: P_t V of a K/V tile done (three-buffer mode)
+  uint64_t pv_done[2];   // MMA -> softmax 1: P_1(n1 - 2) V done (three-buffer mode, once)
   uint64_t mma_drain;    // MMA thread: all of its MMAs finished (before TMEM is freed)
   // Landing of the K/V loads.  d = 64 (kPairWait): K_j and V_j both land on
   // kv_full[j % 8], so one wait covers the pair.  d = 128: each ring slot has its own
@@ -337,7 +337,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           if (!(ok = wait_bar(&bars->p_ready[j & 1], (j >> 1) & 1))) break;
           issue_pv(tO0, colS(2 * j), itV, j > 0);
-          mma_commit_elect(smem_u32(&bars->pv_done[0]));
           if (j + 1 == n0) mma_commit_elect(smem_u32(&bars->o_final[0]));
         }
         if (j + 1 < n1) {
@@ -346,7 +345,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (!(ok = wait_bar(&bars->p_ready[2 + (j & 1)], (j >> 1) & 1))) break;
         issue_pv(tO1, colS(min(j + 1, n0) + j), itV, j > 0);
-        mma_commit_elect(smem_u32(&bars->pv_done[1]));
+        // The one P_1 V that no later product of this thread follows before tile 1's next
+        // step (see the softmax's rescale wait).
+        if (j + 2 == n1 && j + 1 >= n0) mma_commit_elect(smem_u32(&bars->pv_done[1]));
         // P_1(j) V is the last product reading K_j or V_j.
         mma_commit_elect(smem_u32(&bars->kv_empty[j % kKvBars]));
         if (j + 1 == n1) mma_commit_elect(smem_u32(&bars->o_final[1]));
@@ -505,11 +506,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       l = l * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
       if constexpr (Cfg::kTripleS) {
         if (rescale) {
-          // S_t(j) may have finished before P_t(j-1) V: wait for that product (the
-          // barrier has completed j-1 or j phases here, so the parity wait is
-          // unambiguous), then rescale O_t before P_t(j) V is issued.
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[t]), (j - 1) & 1,
-                                                 abort, p.status));
+          // S_t(j) may have finished before P_t(j-1) V.  The MMA thread's products
+          // complete in issue order, so wait for the first product it issues after
+          // P_t(j-1) V (none of which depends on this step): S_1(j) for tile 0; for tile 1
+          // S_0(j+1), else P_0(j) V (tile 0's last, o_final), else S_1(j+1), else the
+          // one-off pv_done[1] commit.  None of these barriers can have run two phases
+          // ahead: their next phases need this tile's next step.  Then rescale O_t before
+          // P_t(j) V is issued.
+          uint32_t bar;
+          int parity;
+          if (t == 0) {
+            bar = smem_u32(&bars->s_full[2 + (j & 1)]);
+            parity = (j >> 1) & 1;
+          } else if (j + 1 < n0) {
+            bar = smem_u32(&bars->s_full[(j + 1) & 1]);
+            parity = ((j + 1) >> 1) & 1;
+          } else if (j < n0) {
+            bar = smem_u32(&bars->o_final[0]);
+            parity = 0;
+          } else if (j + 1 < n1) {
+            bar = smem_u32(&bars->s_full[2 + ((j + 1) & 1)]);
+            parity = ((j + 1) >> 1) & 1;
+          } else {
+            bar = smem_u32(&bars->pv_done[1]);
+            parity = 0;
+          }
+          ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, p.status));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
