@@ -10,8 +10,15 @@ larger than the 129 MB L2 (Q, K, V: 201 MB; x: 537 MB), so no L2 flush is needed
 
 Printed JSON (one line, rank 0):
   value      attention TFLOP/s = 4*B*H*N^2*d/2 / mean attention kernel time (CUDA events
-             on the launching stream, max over ranks);
+             on the launching stream, max over ranks); ms_attention_median beside it;
+  errors     O max / mean abs and LSE max abs error of the bench step's output against
+             the fp64 oracle on seeded rows of four heads (the stated gates alongside);
   row_softmax  the row kernel's GB/s = (rows*len*4 + rows*8) / mean kernel time;
+  clocks     nvidia-smi samples from a loaded window: the same steps run untimed for
+             --load-seconds right before the timed ones, then the timed steps;
+  workloads  the other attention configurations (B4 H16 N4096 d64; B1 H8 N32768 d128
+             causal, Q std 4), each timed alone on this GPU: mean / median ms, TFLOP/s,
+             roofline fraction and oracle errors (not part of the step);
   e2e        the same attention metric through the public Python API with pinned host
              buffers: host->device copy of Q, K, V, the kernel and device->host read of
              O and LSE inside the timed region;
@@ -145,6 +152,9 @@ def rank_env():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
+    """nvidia-smi sampled every `period_ms` while the workload runs; each line is kept with
+    its arrival time, so that the summary can be restricted to the window in which the
+    GPU was loaded."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -153,7 +163,7 @@ class ClockSampler:
         self.index = index
         self.period_ms = period_ms
         self.proc = None
-        self.lines = []
+        self.lines = []   # (arrival time, line)
         self.thread = None
 
     def start(self):
@@ -170,37 +180,44 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, window=None):
+        """Summary of the samples; with `window` = (t0, t1) (host time) the clock median,
+        power and reasons come from the samples that arrived inside it (the loaded
+        period), and `samples_under_load` counts them."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
-                    "samples": 0}
+                    "samples": 0, "samples_under_load": 0}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
-        sm, smax, power, reasons = [], [], [], set()
+        sm, smax, power, reasons, total = [], [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for t, line in self.lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                vals = float(parts[1]), float(parts[2]), float(parts[3])
             except ValueError:
                 continue
+            total += 1
+            if window is not None and not (window[0] <= t <= window[1]):
+                continue
+            sm.append(vals[0])
+            smax.append(vals[1])
+            power.append(vals[2])
             for n, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": total, "samples_under_load": len(sm)}
 
 
 # ------------------------------------------------------------------ oracle sample (CPU)
@@ -378,6 +395,78 @@ def reference_arm(args, rank, world):
     }
 
 
+# ------------------------------------------------------------------ errors against the oracle
+def attention_errors(q, k, v, o, lse, scale, causal, n_heads=4, n_rows=32, seed=7):
+    """Max and mean abs error of O and max abs error of LSE against the fp64 oracle on
+    the first and last row and `n_rows` seeded rows of `n_heads` heads spread over the
+    batch (q, k, v: host arrays holding the values the kernel read; o, lse: device
+    results)."""
+    import torch
+
+    import oracle
+    B, H, N, d = q.shape
+    all_heads = [(b, h) for b in range(B) for h in range(H)]
+    step = max(1, len(all_heads) // n_heads)
+    heads = all_heads[::step][:n_heads]
+    errs, lerrs = [], []
+    for i, (b, h) in enumerate(heads):
+        g = np.random.Generator(np.random.PCG64(seed + i))
+        rows = np.unique(np.concatenate([[0, N - 1], g.choice(N, min(n_rows, N), False)]))
+        o_ref, lse_ref = oracle.attention_forward(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                                  v[b:b + 1, h:h + 1], scale, causal, rows=rows)
+        idx = torch.from_numpy(rows).to(o.device)
+        errs.append(np.abs(o[b, h].index_select(0, idx).float().cpu().numpy() - o_ref[0, 0]))
+        lerrs.append(np.abs(lse[b, h].index_select(0, idx).cpu().numpy() - lse_ref[0, 0]))
+    e = np.concatenate([x.ravel() for x in errs])
+    le = np.concatenate([x.ravel() for x in lerrs])
+    return {"o_max_abs_err": float(e.max()), "o_mean_abs_err": float(e.mean()),
+            "lse_max_abs_err": float(le.max()), "rows_checked": int(le.size),
+            "gates": {"o_max_abs": 2e-2, "o_mean_abs": 2e-3, "lse_max_abs": 1e-3}}
+
+
+def extra_workload(name, peaks, stream, reps=20):
+    """One more attention workload of the configuration list, measured like the bench
+    workload (CUDA events around each of `reps` launches after 3 warm-ups): mean and
+    median time, TFLOP/s, fraction of the measured bf16 peak, and oracle errors."""
+    import torch
+
+    from online_softmax_07_gb300 import abi, synth
+    w = synth.WORKLOADS[name]
+    q, k, v = synth.workload_attention_inputs(name)
+    B, H, N, d = q.shape
+    dev = torch.device("cuda", torch.cuda.current_device())
+    tq, tk, tv = (torch.from_numpy(t).to(dev, torch.bfloat16) for t in (q, k, v))
+    o = torch.empty_like(tq)
+    lse = torch.empty((B, H, N), device=dev)
+    scale = 1.0 / math.sqrt(d)
+    call = lambda: abi.fa_fwd(tq, tk, tv, o, lse, B, H, N, d, scale, int(w["causal"]), stream)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if abi.fa_last_device_error() != abi.FA_OK:
+        raise RuntimeError(f"device-side error in {name}")
+    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms_mean, ms_med = statistics.mean(ms), statistics.median(ms)
+    flops = attn_flops(B, H, N, d, w["causal"])
+    tf = flops / (ms_mean * 1e-3) / 1e12
+    out = {"ms_mean": ms_mean, "ms_median": ms_med, "TFLOP/s": tf,
+           "TFLOP/s_median": flops / (ms_med * 1e-3) / 1e12,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"]},
+           "launches": reps}
+    out.update(attention_errors(q, k, v, o, lse, scale, w["causal"], n_heads=2))
+    del tq, tk, tv, o, lse
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ our arm
 def our_arm(args, rank, world, local_rank):
     import torch
@@ -417,7 +506,17 @@ def our_arm(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.2)   # let the sampler come up before the timed region
+    time.sleep(0.2)   # let the sampler come up
+    # Load window: the same steps, untimed, for at least --load-seconds right before the
+    # timed ones, so that the clock record covers the kernels running.
+    t_load0 = time.time()
+    while time.time() - t_load0 < args.load_seconds:
+        for _ in range(20):
+            abi.fa_fwd(dq, dk, dv, do, dlse, B, H, N, d, scale, int(causal), stream)
+            abi.online_softmax_rows(dx, dm, dl, rows, length, stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -429,16 +528,23 @@ def our_arm(args, rank, world, local_rank):
         ev[i][2].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
+    t_load1 = time.time()
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    time.sleep(0.1)   # the samples of the last loaded moments arrive
+    clocks = sampler.stop(window=(t_load0, t_load1 + 0.05))
+    clocks["load_window_s"] = t_load1 - t_load0
     if abi.fa_last_device_error() != abi.FA_OK:
         raise RuntimeError("device-side error in the timed region")
 
-    attn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    rows_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    attn_list = [e[0].elapsed_time(e[1]) for e in ev]
+    rows_list = [e[1].elapsed_time(e[2]) for e in ev]
+    attn_ms, rows_ms = statistics.mean(attn_list), statistics.mean(rows_list)
+    attn_med, rows_med = statistics.median(attn_list), statistics.median(rows_list)
     step_ms = t_start.elapsed_time(t_end) / args.steps
-    attn_ms, rows_ms, step_ms = max_over_ranks([attn_ms, rows_ms, step_ms], dev)
+    attn_ms, rows_ms, step_ms, attn_med, rows_med = max_over_ranks(
+        [attn_ms, rows_ms, step_ms, attn_med, rows_med], dev)
+    errors = attention_errors(q, k, v, do, dlse, scale, causal) if rank == 0 else None
 
     flops = attn_flops(B, H, N, d, causal)
     rbytes = row_bytes(rows, length)
@@ -483,7 +589,10 @@ def our_arm(args, rank, world, local_rank):
         "config": run_config(world),
         "pct_of_peak": per_gpu_tflops / peaks["bf16_tflops"] * 100.0,
         "ms_attention": attn_ms,
+        "ms_attention_median": attn_med,
         "ms_rows": rows_ms,
+        "ms_rows_median": rows_med,
+        "errors": errors,
         "row_softmax": {
             "value": row_gbs, "unit": "GB/s",
             "roofline": {"bound": "hbm", "achieved": per_gpu_gbs, "peak": peaks["hbm_gbs"],
@@ -501,6 +610,12 @@ def our_arm(args, rank, world, local_rank):
                 "api": "online_softmax_07_gb300.attention_forward(pinned host tensors)"},
         "gpu_launches": 2 * args.steps,
     }
+    if rank == 0 and not args.no_workloads:
+        # The other attention configurations, each on this GPU alone (not part of the
+        # step): B4 H16 N4096 d64 and the long sequence B1 H8 N32768 d128 causal, Q std 4.
+        del qh, kh, vh, oh, lh
+        out["workloads"] = {n: extra_workload(n, peaks, stream) for n in
+                            ("attn_bf16_b4h16n4096d64", "attn_bf16_b1h8n32768d128_causal_qstd4")}
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(q, k, v, x, budget_s=args.cpu_seconds)
     return out
@@ -840,6 +955,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the extra attention configurations after the bench step")
+    ap.add_argument("--load-seconds", type=float, default=1.0,
+                    help="untimed steps run under the clock sampler before the timed ones")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--suite", action="store_true",
                     help="one line per workload instead of the bench line (1 GPU)")

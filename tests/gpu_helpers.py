@@ -69,10 +69,21 @@ def check_attention(o, lse, o_ref, lse_ref, dtype="bf16"):
     return float(err.max()), float(err.mean())
 
 
+def block_edge_rows(N: int) -> list:
+    """Rows at the edges of the forward kernel's work: 128-row Q tiles inside 256-row
+    query blocks.  The first tile, the tile edge inside the first block (127 / 128), the
+    first block edge (255 / 256) and the second (511 / 512), the last block's first row
+    and its first tile-1 row, and the last rows (where the most rescales have
+    happened)."""
+    last_block = ((N - 1) // 256) * 256
+    cand = (0, 127, 128, 255, 256, 511, 512, last_block, last_block + 127, last_block + 128,
+            N - 129, N - 1)
+    return sorted({r for r in cand if 0 <= r < N})
+
+
 def sample_rows(N: int, count: int, seed: int) -> np.ndarray:
-    """Seeded rows without replacement plus the first tile, a tile edge and the last
-    rows (where the most rescales have happened)."""
-    forced = sorted({r for r in (0, 127, 128, N - 129, N - 1) if 0 <= r < N})
+    """Seeded rows without replacement plus the block-edge rows above."""
+    forced = block_edge_rows(N)
     rest = np.setdiff1d(np.arange(N), forced)
     g = np.random.Generator(np.random.PCG64(seed))
     pick = g.choice(rest, size=min(count - len(forced), rest.size), replace=False)

@@ -191,15 +191,15 @@ def _full_size(name, rows_per_head):
 
 
 def test_workload_b4h16n4096d64_sampled():
-    _full_size("attn_bf16_b4h16n4096d64", 64)
+    _full_size("attn_bf16_b4h16n4096d64", 128)
 
 
 def test_workload_b2h16n8192d128_causal_sampled():
-    _full_size("attn_bf16_b2h16n8192d128_causal", 64)
+    _full_size("attn_bf16_b2h16n8192d128_causal", 128)
 
 
 def test_workload_b2h16n8191d128_causal_sampled():
-    _full_size("attn_bf16_b2h16n8191d128_causal", 64)
+    _full_size("attn_bf16_b2h16n8191d128_causal", 128)
 
 
 def test_workload_b1h8n32768d128_causal_qstd4_sampled():
