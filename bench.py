@@ -27,8 +27,8 @@ Printed JSON (one line, rank 0):
   cpu_baseline  the fp64 oracle timed on a bounded sample of the same workload on the
              host cores (rank 0, one GPU only).
 ``--impl reference`` times the oracle alone (see ``reference_arm``); ``--suite``,
-``--backward [B,H,N,d,causal]``, ``--forward B,H,N,d,causal[,splits]`` and
-``--rows state|softmax``
+``--backward [B,H,N,d,causal]``, ``--forward B,H,N,d,causal[,splits]``, ``--block-study``
+and ``--rows state|softmax``
 print per-workload lines instead (the commands the committed profiles were taken with).
 """
 
@@ -904,6 +904,58 @@ def forward_run(args):
           flush=True)
 
 
+def block_study(args):
+    """The block-size study: each attention workload (B4 H16 N4096 d64; B2 H16 N8192 d128
+    causal; B1 H8 N32768 d128 causal, Q std 4) through fa_fwd_block with 64-, 128- and (at
+    d = 64) 256-key tiles: median and mean of 20 CUDA-event-timed launches after 3 warm-ups,
+    TFLOP/s, and the O / LSE errors against the fp64 oracle on 34 seeded rows of four
+    heads.  One JSON line per (workload, block)."""
+    import torch
+
+    from online_softmax_07_gb300 import abi, synth
+    from online_softmax_07_gb300.build import build_library
+
+    build_library()
+    abi.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    for name in ("attn_bf16_b4h16n4096d64", "attn_bf16_b2h16n8192d128_causal",
+                 "attn_bf16_b1h8n32768d128_causal_qstd4"):
+        w = synth.WORKLOADS[name]
+        q, k, v = synth.workload_attention_inputs(name)
+        B, H, N, d = q.shape
+        tq, tk, tv = (torch.from_numpy(t).to(dev, torch.bfloat16) for t in (q, k, v))
+        o = torch.empty_like(tq)
+        lse = torch.empty((B, H, N), device=dev)
+        scale = 1.0 / math.sqrt(d)
+        for block_n in ((64, 128, 256) if d == 64 else (64, 128)):
+            call = lambda: abi.fa_fwd_block(tq, tk, tv, o, lse, B, H, N, d, scale,
+                                            int(w["causal"]), abi.FA_BF16, block_n, stream)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(20)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                call()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            if abi.fa_last_device_error() != abi.FA_OK:
+                raise RuntimeError("device-side error")
+            ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+            med = statistics.median(ms)
+            tf = attn_flops(B, H, N, d, w["causal"]) / (med * 1e-3) / 1e12
+            line = {"workload": name, "block_n": block_n, "merges_per_row": -(-N // block_n),
+                    "ms_median": med, "ms_mean": statistics.mean(ms), "TFLOP/s": tf,
+                    "frac_of_bf16_peak": tf / peaks["bf16_tflops"]}
+            line.update(attention_errors(q, k, v, o, lse, scale, w["causal"], n_heads=4))
+            print(json.dumps(line), flush=True)
+        del tq, tk, tv, o, lse
+        torch.cuda.empty_cache()
+
+
 def rows_run(args):
     """The row kernels alone on the 4096 x 32768 fp32 workload (N(0, 9) with the special
     rows): --rows state times online_softmax_rows, --rows softmax online_softmax_forward
@@ -968,6 +1020,9 @@ def main():
     ap.add_argument("--forward", metavar="B,H,N,d,causal[,splits]",
                     help="time the bf16 forward alone on one shape, split-KV with splits > 1 "
                          "(0: the library's default count) (1 GPU)")
+    ap.add_argument("--block-study", action="store_true",
+                    help="time and check the forward with 64-, 128- and 256-key tiles on the "
+                         "attention workloads (1 GPU)")
     ap.add_argument("--rows", metavar="state|softmax",
                     help="time a row kernel alone on the 4096 x 32768 workload (1 GPU)")
     args = ap.parse_args()
@@ -986,6 +1041,9 @@ def main():
         return
     if args.rows:
         rows_run(args)
+        return
+    if args.block_study:
+        block_study(args)
         return
     if world > 1 and args.impl == "ours":
         import torch

@@ -91,6 +91,25 @@ fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float*
                     fa_dtype dtype, cudaStream_t stream);
 
 /*
+ * Attention forward with a chosen key block: the number of keys per K/V tile, i.e. per
+ * step of the online-softmax tile loop ("Softmax 数值稳定性与 IO-Aware Attention" §七)
+ * and so the number of (m, l) merges per row (N / block_n).  "Flash Attention 和标准
+ * Attention 输出完全一样吗" suggests a larger block (128 -> 256) to reduce the merges;
+ * "为什么 Flash Attention 算出来的结果和标准注意力有微小差异？有损但值得" ("罪魁祸首是
+ * online softmax 里那步 rescale") says the error grows with their number.  This entry
+ * exists for that study: same operation, arguments and results as fa_fwd_dt.
+ *
+ * block_n: 0 or 128 = fa_fwd_dt (the kernel the library otherwise runs; any dtype fa_fwd_dt
+ *          takes); 64 (d = 64 or 128) or 256 (d = 64): the same tcgen05 kernel built with
+ *          64- or 256-key tiles, FA_BF16 only.  Other values: FA_ERR_INVALID; 256 with
+ *          d = 128 or a 16-bit type other than bf16: FA_ERR_UNSUPPORTED.
+ * Errors: as fa_fwd_dt.
+ */
+fa_status fa_fwd_block(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                       int block_n, cudaStream_t stream);
+
+/*
  * Split-KV attention forward.  Same operation, arguments and results as fa_fwd_dt (bf16
  * or fp16, d in {64, 128}); each query block's K/V tiles are divided into num_splits
  * contiguous chunks processed by separate thread blocks, which raises the parallelism

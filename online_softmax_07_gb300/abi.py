@@ -1,6 +1,7 @@
 """ctypes binding of the C ABI in include/fa.h (argument marshalling only).
 
 The functions here carry the C names and signatures: ``fa_fwd``, ``fa_fwd_dt``,
+``fa_fwd_block``,
 ``fa_fwd_splitkv``, ``fa_fwd_splitkv_workspace_bytes``, ``fa_fwd_splitkv_default_splits``,
 ``fa_fwd_splitkv_splits_for``, ``fa_fwd_splitkv_static``, ``fa_bwd``, ``fa_bwd_workspace_bytes``,
 ``fa_fwd_host``, ``fa_fwd_host_workspace_bytes``,
@@ -29,6 +30,8 @@ _SIGNATURES = {
                + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_dt": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 4
                   + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "fa_fwd_block": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 4
+                     + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_splitkv": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 4
                        + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                           ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
@@ -136,6 +139,13 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream=None) -> None:
 def fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream=None) -> None:
     _check(load().fa_fwd_dt(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
                             float(scale), int(causal), int(dtype), _stream(stream)), "fa_fwd_dt")
+
+
+def fa_fwd_block(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, block_n, stream=None) -> None:
+    """fa_fwd_dt with the keys per K/V tile chosen (block-size study: 64, 128 or 256)."""
+    _check(load().fa_fwd_block(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                               float(scale), int(causal), int(dtype), int(block_n),
+                               _stream(stream)), "fa_fwd_block")
 
 
 def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,

@@ -62,16 +62,16 @@ cudaError_t encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return cudaSuccess;
 }
 
-// A [BH, N, d] bf16 or fp16 tensor seen by TMA as 3-D (d innermost), boxes of 128 rows x 64
-// columns (128 bytes) with the 128-byte swizzle.  Rows past N read as zero and are
-// not written by stores.
+// A [BH, N, d] bf16 or fp16 tensor seen by TMA as 3-D (d innermost), boxes of box_rows
+// rows x 64 columns (128 bytes) with the 128-byte swizzle.  Rows past N read as zero and
+// are not written by stores.
 bool encode_bhnd(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base,
-                 int BH, int N, int d, bool f16) {
+                 int BH, int N, int d, bool f16, int box_rows) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxCols), static_cast<cuuint32_t>(kBlockM),
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxCols), static_cast<cuuint32_t>(box_rows),
                              1};
   const cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
@@ -156,7 +156,7 @@ long long nqb_of(int N) { return (static_cast<long long>(N) + 2 * kBlockM - 1) /
 // (caller-sized) and the combine kernel then writes o and lse.
 fa_status run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, fa_dtype dtype, int splits, float* ws_o,
-                 float* ws_lse, cudaStream_t stream) {
+                 float* ws_lse, cudaStream_t stream, int block_n = kDefaultBlockN) {
   const long long BH = static_cast<long long>(B) * H;
   const long long nqb = nqb_of(N);
   if (nqb * BH * splits > INT_MAX) return FA_ERR_INVALID;
@@ -168,8 +168,10 @@ fa_status run_tc(const void* q, const void* k, const void* v, void* o, float* ls
   CUtensorMap tq, tk, tv, to;
   const int bh = static_cast<int>(BH);
   const bool f16 = dtype == FA_F16;
-  if (!encode_bhnd(enc, &tq, q, bh, N, d, f16) || !encode_bhnd(enc, &tk, k, bh, N, d, f16) ||
-      !encode_bhnd(enc, &tv, v, bh, N, d, f16) || !encode_bhnd(enc, &to, o, bh, N, d, f16))
+  if (!encode_bhnd(enc, &tq, q, bh, N, d, f16, kBlockM) ||
+      !encode_bhnd(enc, &tk, k, bh, N, d, f16, block_n) ||
+      !encode_bhnd(enc, &tv, v, bh, N, d, f16, block_n) ||
+      !encode_bhnd(enc, &to, o, bh, N, d, f16, kBlockM))
     return FA_ERR_CUDA;
   AttnTcParams p;
   p.lse = lse;
@@ -190,12 +192,17 @@ fa_status run_tc(const void* q, const void* k, const void* v, void* o, float* ls
   p.n_pad = static_cast<int>(nqb * 2 * kBlockM);
   p.ws_o = ws_o;
   p.ws_lse = ws_lse;
-  if (d == 64)
-    e = f16 ? launch_attn_tc<64, true>(tq, tk, tv, to, p, stream)
-            : launch_attn_tc<64, false>(tq, tk, tv, to, p, stream);
+  if (block_n == 64)  // block-size study kernels (bf16)
+    e = d == 64 ? launch_attn_tc<64, 64, false>(tq, tk, tv, to, p, stream)
+                : launch_attn_tc<128, 64, false>(tq, tk, tv, to, p, stream);
+  else if (block_n == 256)
+    e = launch_attn_tc<64, 256, false>(tq, tk, tv, to, p, stream);
+  else if (d == 64)
+    e = f16 ? launch_attn_tc<64, 128, true>(tq, tk, tv, to, p, stream)
+            : launch_attn_tc<64, 128, false>(tq, tk, tv, to, p, stream);
   else
-    e = f16 ? launch_attn_tc<128, true>(tq, tk, tv, to, p, stream)
-            : launch_attn_tc<128, false>(tq, tk, tv, to, p, stream);
+    e = f16 ? launch_attn_tc<128, 128, true>(tq, tk, tv, to, p, stream)
+            : launch_attn_tc<128, 128, false>(tq, tk, tv, to, p, stream);
   if (e != cudaSuccess || splits == 1) return from_cuda(e);
   return from_cuda(launch_splitkv_combine(ws_o, ws_lse, o, lse, bh, N, p.n_pad, d, splits, f16,
                                           stream));
@@ -244,7 +251,7 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits
 int fa_fwd_splitkv_splits_for(int B, int H, int N, int causal, int sms) {
   if (B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1) || sms <= 0) return 1;
   const long long blocks = nqb_of(N) * B * H;
-  const long long kv_tiles = (static_cast<long long>(N) + kBlockN - 1) / kBlockN;
+  const long long kv_tiles = (static_cast<long long>(N) + kDefaultBlockN - 1) / kDefaultBlockN;
   // Causal: floor(2 sms / blocks + 0.2), the longest block over the average work per SM;
   // not causal: as many pieces as still run in one wave.  (Measured on GB300, 152 SMs:
   // causal 64 blocks best at 4 splits, 128 and 160 at 2, 256 at 1-2; not causal 32
@@ -287,6 +294,20 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, cudaStream_t stream) {
   return fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, FA_BF16, stream);
+}
+
+fa_status fa_fwd_block(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, float scale, int causal, fa_dtype dtype, int block_n,
+                       cudaStream_t stream) {
+  if (block_n == 0 || block_n == kDefaultBlockN)
+    return fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream);
+  if (block_n != 64 && block_n != 256) return FA_ERR_INVALID;
+  fa_status st = check_tc_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype);
+  if (st != FA_OK) return st;
+  if (dtype != FA_BF16 || (block_n == 256 && d != 64)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H == 0 || N == 0) return FA_OK;
+  return run_tc(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, 1, nullptr, nullptr, stream,
+                block_n);
 }
 
 fa_status online_softmax_rows(const float* x, float* m_out, float* l_out, int rows, int len,

@@ -109,8 +109,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   CUtensorMap tq, tk, tv, tdo;
   const int bh = static_cast<int>(BH);
   const bool f16 = dtype == FA_F16;
-  if (!encode_bhnd(enc, &tq, q, bh, N, d, f16) || !encode_bhnd(enc, &tk, k, bh, N, d, f16) ||
-      !encode_bhnd(enc, &tv, v, bh, N, d, f16) || !encode_bhnd(enc, &tdo, dout, bh, N, d, f16))
+  if (!encode_bhnd(enc, &tq, q, bh, N, d, f16, kBlockM) ||
+      !encode_bhnd(enc, &tk, k, bh, N, d, f16, kBlockM) ||
+      !encode_bhnd(enc, &tv, v, bh, N, d, f16, kBlockM) ||
+      !encode_bhnd(enc, &tdo, dout, bh, N, d, f16, kBlockM))
     return FA_ERR_CUDA;
   AttnBwdParams p;
   p.lse2 = nullptr;  // set by the launcher from the workspace

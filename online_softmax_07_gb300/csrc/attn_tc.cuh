@@ -20,11 +20,10 @@
 //  * each softmax thread owns one query row of its tile (TMEM lane = row), so row max
 //    and row sum need no shuffles;
 //  * the rescale reference m is moved only when a row's maximum grows by more than
-//    a factor 2^64 for bf16 (2^8 for fp16; kRescaleLog2); between moves alpha = 1 and
-//    the O rescale is skipped.  The identity behind the merge rule holds for any common
-//    reference, so O and LSE are the same in exact arithmetic; P then lies in
-//    [0, 2^64] instead of [0, 1], which bf16 and fp32 represent with the same relative
-//    precision.
+//    2^8 (kRescaleLog2); between moves alpha = 1 and the O rescale is skipped.  The
+//    identity behind the merge rule holds for any common reference, so O and LSE are
+//    the same in exact arithmetic; P then lies in [0, 2^8] instead of [0, 1], which
+//    bf16 and fp32 represent with the same relative precision.
 #pragma once
 
 #include <cstdint>
@@ -35,9 +34,9 @@
 namespace osfa {
 
 constexpr int kBlockM = 128;        // query rows per tile = TMEM lanes
-constexpr int kBlockN = 128;        // keys per K/V tile
+constexpr int kDefaultBlockN = 128; // keys per K/V tile unless a block size is chosen
 constexpr int kBoxCols = 64;        // bf16 per 128-byte swizzled row
-constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 128 bytes
+constexpr int kBoxBytes = 128 * 128;  // one TMA box of a Q or O tile: 128 rows x 128 bytes
 // Warps 0-3: softmax of tile 0; 4-7: softmax of tile 1; 8: MMA issue; 9: TMA loads;
 // 10-11 idle (they complete the third warpgroup so that it can hand its registers to
 // the softmax warpgroups).
@@ -46,33 +45,46 @@ constexpr int kRegsSoftmax = 208;  // per thread, softmax warpgroups
 constexpr int kRegsIssue = 88;     // per thread, MMA / TMA warpgroup (384 x 168 = 256 x 208 + 128 x 88)
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
-// Lazy rescale threshold in log2 units: P = 2^(s' - m) stays below 2^kRescaleLog2.  bf16
-// holds any such P to the same relative precision (its range reaches 2^127), so the
-// reference moves only for growth beyond 2^64 (sums of up to 2^17 such terms times |v|
-// stay far inside fp32); fp16 P must stay below 65504, so 2^8 there.
+// Lazy rescale threshold in log2 units: P = 2^(s' - m) stays below 2^kRescaleLog2.  The
+// range of bf16 would allow far more, but a stale reference also costs accuracy: with
+// the reference at the row maximum the largest term of a row is P = 1 exactly, with a
+// stale one it is rounded to 16 bits like the rest, and on rows dominated by one key
+// that rounding goes straight into O.  A 2^64 threshold (rescales almost never) raised
+// the largest O error on a Q-std-4 set from 1.6e-2 to 2.7e-2 (kernel-arithmetic
+// emulation against the fp64 oracle); 2^8 keeps it near that of an eager reference
+// (1.5e-2) and keeps fp16 P below its 65504 limit.
 template <bool F16>
-constexpr float kRescaleLog2 = F16 ? 8.0f : 64.0f;
+constexpr float kRescaleLog2 = 8.0f;
 
-template <int D>
+// D: head dimension; BN: keys per K/V tile (the "block size" of the tile loop).  BN = 128
+// is the kernel the library runs; BN = 64 (both d) and 256 (d = 64) are built for the
+// block-size study.
+template <int D, int BN>
 struct AttnTcCfg {
   static_assert(D == 64 || D == 128, "head dimension");
+  static_assert(BN == 64 || BN == 128 || (BN == 256 && D == 64), "key block");
   static constexpr int kBoxes = D / kBoxCols;
-  static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D bf16
-  static constexpr int kSlots = (D == 128) ? 5 : 8;       // K/V ring depth
+  static constexpr int kQTileBytes = kBoxes * kBoxBytes;  // 128 query rows x D
+  static constexpr int kKvBoxBytes = BN * 128;            // BN keys x 64 columns
+  static constexpr int kTileBytes = kBoxes * kKvBoxBytes; // one K or V tile: BN keys x D
+  // K/V ring depth: the slots that fit next to the two Q tiles in about 224 KB.
+  static constexpr int kSlots = (D == 128) ? (BN == 64 ? 10 : 5) : (BN == 64 ? 16 : BN == 128 ? 8 : 6);
   static constexpr bool kPairWait = (D == 64);  // one landing barrier per K/V pair
   static constexpr int kSmemQ0 = 0;
-  static constexpr int kSmemQ1 = kTileBytes;
-  static constexpr int kSmemSlots = 2 * kTileBytes;
+  static constexpr int kSmemQ1 = kQTileBytes;
+  static constexpr int kSmemSlots = 2 * kQTileBytes;
   static constexpr int kSmemBars = kSmemSlots + kSlots * kTileBytes;
   static constexpr int kSmemBytes = kSmemBars + 512 + 1024;  // + barriers + alignment slack
-  // TMEM columns.  d = 128: S/P of tile 0 and 1, then O of tile 0 and 1.  d = 64: the O
-  // accumulators take only 128 columns, which leaves room for a third S/P buffer; the
-  // two tiles then use three S/P buffers in rotation (kTripleS), so that the next S of a
-  // tile can be computed while its current P is still being formed.
-  static constexpr bool kTripleS = (D == 64);
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColS2 = 256;
-  static constexpr uint32_t kColO0 = kTripleS ? 384 : 256, kColO1 = kColO0 + D;
+  // TMEM columns: kSBufs S/P buffers of BN columns, then O of tile 0 and 1.  d = 128:
+  // two buffers (one per tile).  d = 64: the O accumulators take only 128 columns, which
+  // leaves room for a third buffer, so that the next S of a tile can be computed while
+  // its current P is still being formed; at BN = 256 one 256-column buffer is all that
+  // fits, and the two tiles take turns.
+  static constexpr int kSBufs = (D == 128) ? 2 : (BN == 256 ? 1 : 3);
+  static constexpr uint32_t kColO0 = kSBufs * BN, kColO1 = kColO0 + D;
   static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColO1 + D <= kTmemCols, "TMEM columns");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 struct AttnTcParams {
@@ -94,8 +106,9 @@ struct AttnTcParams {
   float* ws_lse;
 };
 
-// F16 = false: bf16 Q, K, V, O (and P); F16 = true: fp16.
-template <int D, bool F16>
+// F16 = false: bf16 Q, K, V, O (and P); F16 = true: fp16.  tk and tv have BN-row boxes,
+// tq and to 128-row boxes.
+template <int D, int BN, bool F16>
 cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, const AttnTcParams& p, cudaStream_t stream);
 

@@ -1,8 +1,8 @@
-// tcgen05 attention forward, head dimension 128, bf16 (kernel body in attn_tc_impl.cuh).
+// tcgen05 attention forward, head dimension 128, bf16, 128-key tiles (kernel body in attn_tc_impl.cuh).
 #include "attn_tc_impl.cuh"
 
 namespace osfa {
-template cudaError_t launch_attn_tc<128, false>(const CUtensorMap&, const CUtensorMap&,
-                                                 const CUtensorMap&, const CUtensorMap&,
-                                                 const AttnTcParams&, cudaStream_t);
+template cudaError_t launch_attn_tc<128, 128, false>(const CUtensorMap&, const CUtensorMap&,
+                                                  const CUtensorMap&, const CUtensorMap&,
+                                                  const AttnTcParams&, cudaStream_t);
 }  // namespace osfa

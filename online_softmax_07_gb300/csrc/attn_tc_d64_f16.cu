@@ -1,8 +1,8 @@
-// tcgen05 attention forward, head dimension 64, fp16 (kernel body in attn_tc_impl.cuh).
+// tcgen05 attention forward, head dimension 64, fp16, 128-key tiles (kernel body in attn_tc_impl.cuh).
 #include "attn_tc_impl.cuh"
 
 namespace osfa {
-template cudaError_t launch_attn_tc<64, true>(const CUtensorMap&, const CUtensorMap&,
-                                                 const CUtensorMap&, const CUtensorMap&,
-                                                 const AttnTcParams&, cudaStream_t);
+template cudaError_t launch_attn_tc<64, 128, true>(const CUtensorMap&, const CUtensorMap&,
+                                                  const CUtensorMap&, const CUtensorMap&,
+                                                  const AttnTcParams&, cudaStream_t);
 }  // namespace osfa

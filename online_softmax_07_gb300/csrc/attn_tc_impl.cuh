@@ -4,12 +4,16 @@
 
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "attn_tc.cuh"
 
 namespace osfa {
 
-// K/V pairs tracked at once (kv_full barriers); more than the ring holds.
+// K/V pairs tracked at once (kv_full / kv_empty barriers in pair mode); more than the
+// ring holds.  Per-slot mode uses kv_full[slot] for up to kKvFullBars slots.
 constexpr int kKvBars = 8;
+constexpr int kKvFullBars = 16;
 
 struct AttnTcBarriers {
   uint64_t q_full;
@@ -27,12 +31,12 @@ struct AttnTcBarriers {
   // Landing of the K/V loads.  d = 64 (kPairWait): K_j and V_j both land on
   // kv_full[j % 8], so one wait covers the pair.  d = 128: each ring slot has its own
   // full barrier (kv_full[slot]): the MMA warp waits for K_{j+1} without waiting for
-  // V_{j+1}, which the 5-slot ring may load a tile later.  Each ring slot is released on
+  // V_{j+1}, which an odd-sized ring may load a tile later.  Each ring slot is released on
   // its own (slot_empty) when the products reading it are done, except with kPairWait,
   // where the ring is deep enough to release both slots of pair j once, after the last
   // product reading the pair (kv_empty[j % 8]).
-  uint64_t kv_full[8];
-  uint64_t slot_empty[8];
+  uint64_t kv_full[kKvFullBars];
+  uint64_t slot_empty[kKvFullBars];
   uint64_t kv_empty[8];  // kPairWait: both slots of pair j released at once
   uint32_t tmem_base;
   int abort;
@@ -68,13 +72,16 @@ __device__ __forceinline__ uint32_t pack_elem2(float lo, float hi) {
   }
 }
 
-template <int D, bool F16>
+template <int D, int BN, bool F16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_o, const AttnTcParams p) {
-  using Cfg = AttnTcCfg<D>;
+  using Cfg = AttnTcCfg<D, BN>;
+  constexpr int NS = Cfg::kSBufs;
+  static_assert(Cfg::kSlots <= kKvFullBars, "a landing / release barrier per ring slot");
+  static_assert(!Cfg::kPairWait || Cfg::kSlots / 2 <= kKvBars, "pairs in flight within kKvBars");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -105,10 +112,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bh = full * p.head_group + r % rem;
     }
   }
-  const int nblk = (p.N + kBlockN - 1) / kBlockN;
+  const int nblk = (p.N + BN - 1) / BN;
   // K/V tiles each Q tile needs: all of them, or up to its diagonal tile (causal).
-  const int nb0 = p.causal ? min(nblk, (qb * 2 * kBlockM + kBlockM - 1) / kBlockN + 1) : nblk;
-  const int nb1 = p.causal ? min(nblk, (qb * 2 * kBlockM + 2 * kBlockM - 1) / kBlockN + 1) : nblk;
+  const int nb0 = p.causal ? min(nblk, (qb * 2 * kBlockM + kBlockM - 1) / BN + 1) : nblk;
+  const int nb1 = p.causal ? min(nblk, (qb * 2 * kBlockM + 2 * kBlockM - 1) / BN + 1) : nblk;
   // This block's K/V tiles: all of them, or (split-KV) the split-th chunk of the tiles
   // tile 1 needs; tile 0 takes the part of the chunk below its own limit.  Tiles are
   // numbered from jlo; n0, n1 count them (n0 may be 0, and with splits > 1 so may n1).
@@ -146,10 +153,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(smem_u32(&bars->pv_done[t]), 1);
     }
     mbar_init(smem_u32(&bars->mma_drain), 1);
-    for (int u = 0; u < kKvBars; ++u) {
-      mbar_init(smem_u32(&bars->kv_full[u]), 1);
-      mbar_init(smem_u32(&bars->kv_empty[u]), 1);
-    }
+    // Every landing barrier either mode may use: kv_full[j % kKvBars] for pairs,
+    // kv_full[slot] per slot (up to kSlots of them).
+    for (int u = 0; u < kKvFullBars; ++u) mbar_init(smem_u32(&bars->kv_full[u]), 1);
+    for (int u = 0; u < kKvBars; ++u) mbar_init(smem_u32(&bars->kv_empty[u]), 1);
     for (int s = 0; s < Cfg::kSlots; ++s) mbar_init(smem_u32(&bars->slot_empty[s]), 1);
     bars->abort = 0;
     mbar_init_fence();
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_o);
       const uint32_t qbar = smem_u32(&bars->q_full);
-      mbar_arrive_expect_tx(qbar, 2 * Cfg::kTileBytes);
+      mbar_arrive_expect_tx(qbar, 2 * Cfg::kQTileBytes);
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -205,8 +212,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 sbase + Cfg::kSmemSlots + ((2 * j + h) % Cfg::kSlots) * Cfg::kTileBytes;
 #pragma unroll
             for (int b = 0; b < Cfg::kBoxes; ++b)
-              tma_load_3d(dst + b * kBoxBytes, h ? &tm_v : &tm_k, full, b * kBoxCols,
-                          (jlo + j) * kBlockN, bh);
+              tma_load_3d(dst + b * Cfg::kKvBoxBytes, h ? &tm_v : &tm_k, full, b * kBoxCols,
+                          (jlo + j) * BN, bh);
           }
           issued = j + 1;
         }
@@ -230,7 +237,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint32_t dst = sbase + Cfg::kSmemSlots + slot * Cfg::kTileBytes;
 #pragma unroll
           for (int b = 0; b < Cfg::kBoxes; ++b)
-            tma_load_3d(dst + b * kBoxBytes, tm, full, b * kBoxCols, (jlo + (it >> 1)) * kBlockN, bh);
+            tma_load_3d(dst + b * Cfg::kKvBoxBytes, tm, full, b * kBoxCols, (jlo + (it >> 1)) * BN,
+                        bh);
           issued = it + 1;
         }
         // Every issued copy must land before the block's shared memory goes away: the
@@ -245,7 +253,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop with warp-uniform values; elect.sync inside the
     // MMA and commit wrappers lets one lane issue each instruction.
-    constexpr uint32_t kIdescS = idesc_f16kind(kBlockM, kBlockN, false, F16);
+    constexpr uint32_t kIdescS = idesc_f16kind(kBlockM, BN, false, F16);
     constexpr uint32_t kIdescPV = idesc_f16kind(kBlockM, D, true, F16);
     // Descriptors of the tile bases; an operand at byte offset `off` inside a tile is
     // base + (off >> 4) (the start-address field never overflows: shared memory is
@@ -253,8 +261,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint64_t dQ0 = desc_sw128(sbase + Cfg::kSmemQ0, 16, 1024);
     const uint64_t dQ1 = desc_sw128(sbase + Cfg::kSmemQ1, 16, 1024);
     const uint64_t dSlot0K = desc_sw128(sbase + Cfg::kSmemSlots, 16, 1024);
-    const uint64_t dSlot0V = desc_sw128(sbase + Cfg::kSmemSlots, kBoxBytes, 1024);
-    const uint32_t tS0 = tbase + Cfg::kColS0, tS1 = tbase + Cfg::kColS1;
+    const uint64_t dSlot0V = desc_sw128(sbase + Cfg::kSmemSlots, Cfg::kKvBoxBytes, 1024);
+    const uint32_t tS0 = tbase, tS1 = tbase + BN;  // two-buffer mode
     const uint32_t tO0 = tbase + Cfg::kColO0, tO1 = tbase + Cfg::kColO1;
     auto slot_off16 = [](int it) {
       return static_cast<uint64_t>(((it % Cfg::kSlots) * Cfg::kTileBytes) >> 4);
@@ -270,15 +278,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                                (it / Cfg::kSlots) & 1, abort, p.status));
     };
     // S_t = Q_t K^T: K-major A and B, 16 columns (32 bytes) of d per instruction, all
-    // issued under one elect.
+    // issued under one elect; columns 64.. of d lie in the second box of each tile.
     auto issue_s = [&](uint32_t tS, uint64_t dQ, int itK) {
       const uint64_t dK = dSlot0K + slot_off16(itK);
       uint64_t a[D / 16], b[D / 16];
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        a[kk] = dQ + off16;
-        b[kk] = dK + off16;
+        a[kk] = dQ + (((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+        b[kk] = dK + (((kk >> 2) * Cfg::kKvBoxBytes + (kk & 3) * 32) >> 4);
       }
       if constexpr (D == 64) mma_ss4_elect(tS, a, b, kIdescS, 0u);
       else mma_ss8_elect(tS, a, b, kIdescS, 0u);
@@ -286,29 +293,64 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // O_t += P_t V: P from TMEM (bf16 packed two per column), V MN-major in shared
     // memory; 16 keys (2 KB of the V tile) per instruction, all under one elect.
     auto issue_pv = [&](uint32_t tO, uint32_t tP, int itV, bool acc) {
-      static_assert(kBlockN == 128, "eight 16-key products per P V");
       const uint64_t dV = dSlot0V + slot_off16(itV);
-      uint32_t a[8];
-      uint64_t b[8];
+      uint32_t a[BN / 16];
+      uint64_t b[BN / 16];
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < BN / 16; ++kk) {
         a[kk] = tP + kk * 8;
         b[kk] = dV + ((kk * 2048) >> 4);
       }
-      mma_ts8_elect(tO, a, b, kIdescPV, acc ? 1u : 0u);
+      if constexpr (BN == 64) mma_ts4_elect(tO, a, b, kIdescPV, acc ? 1u : 0u);
+      else if constexpr (BN == 128) mma_ts8_elect(tO, a, b, kIdescPV, acc ? 1u : 0u);
+      else mma_ts16_elect(tO, a, b, kIdescPV, acc ? 1u : 0u);
     };
 
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->q_full), 0, abort, p.status));
     if constexpr (Cfg::kPairWait) ok = ok && wait_kv(0);
     else ok = ok && wait_full(0);
-    if constexpr (Cfg::kTripleS) {
+    if constexpr (NS == 1) {
+      // One S/P buffer (BN = 256 at d = 64): the tiles take turns.  The S at position q
+      // of the sequence S_0(0), S_1(0), S_0(1), ... (S_1(j) at min(j+1, n0) + j once tile 0
+      // has run out) overwrites the P of position q - 1, so it is issued right after that
+      // P V: S(0), P(0) V, S(1), P(1) V, ...
+      const int npos = n0 + n1;
+      auto pos_tile = [&](int q) { return q < 2 * n0 ? (q & 1) : 1; };
+      auto pos_j = [&](int q) { return q < 2 * n0 ? (q >> 1) : q - n0; };
+      if (ok) {
+        tc_fence_after();
+        const int t0 = pos_tile(0);
+        issue_s(tbase, t0 ? dQ1 : dQ0, 0);
+        mma_commit_elect(smem_u32(&bars->s_full[2 * t0]));
+      }
+      for (int q = 0; ok && q < npos; ++q) {
+        const int t = pos_tile(q), j = pos_j(q);
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->p_ready[2 * t + (j & 1)]),
+                                                     (j >> 1) & 1, abort, p.status))))
+          break;
+        tc_fence_after();
+        issue_pv(tbase + (t ? Cfg::kColO1 : Cfg::kColO0), tbase, 2 * j + 1, j > 0);
+        if (j + 1 == (t ? n1 : n0)) mma_commit_elect(smem_u32(&bars->o_final[t]));
+        // P_1(j) V is the last product reading K_j or V_j.
+        if (t == 1) mma_commit_elect(smem_u32(&bars->kv_empty[j % kKvBars]));
+        if (q + 1 < npos) {
+          const int tn = pos_tile(q + 1), jn = pos_j(q + 1);
+          if (jn > j) {
+            if (!(ok = wait_kv(jn))) break;
+            tc_fence_after();
+          }
+          issue_s(tbase, tn ? dQ1 : dQ0, 2 * jn);
+          mma_commit_elect(smem_u32(&bars->s_full[2 * tn + (jn & 1)]));
+        }
+      }
+    } else if constexpr (NS == 3) {
       // Three S/P buffers in rotation: the S issued at position pos of the sequence
       // S_0(0), S_1(0), S_0(1), S_1(1), ... (S_0(j) at 2j, S_1(j) at min(j+1, n0) + j once
       // tile 0 has run out) goes to buffer pos % 3.  Per K/V tile j the pipe receives
       // S_0(j+1), P_0(j) V, S_1(j+1), P_1(j) V: the next S of a tile is computed while its
       // softmax still works on the current one.  The buffer an S overwrites last held the
       // S three positions earlier, whose P V was issued before (in-order pipe).
-      auto colS = [&](int pos) { return tbase + static_cast<uint32_t>((pos % 3) * 128); };
+      auto colS = [&](int pos) { return tbase + static_cast<uint32_t>((pos % 3) * BN); };
       auto wait_bar = [&](uint64_t* bar, int parity) {
         const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, abort, p.status));
         if (r) tc_fence_after();
@@ -417,7 +459,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int rr = wq * 32 + lane; // row within the tile
     const int r0 = qb * 2 * kBlockM + t * kBlockM;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS_fixed = tbase + lane_off + (t ? Cfg::kColS1 : Cfg::kColS0);
     const uint32_t tO = tbase + lane_off + (t ? Cfg::kColO1 : Cfg::kColO0);
     const float sl2 = p.scale_log2;
     float m2 = -INFINITY;  // rescale reference, log2 units of the scaled score
@@ -430,42 +471,61 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // With three S buffers, S_t(j) is in buffer (its position in the rotation) % 3.
-      const uint32_t tS =
-          Cfg::kTripleS
-              ? tbase + lane_off + static_cast<uint32_t>(((t ? min(j + 1, n0) + j : 2 * j) % 3) * 128)
-              : tS_fixed;
-      // S_t(j) and its row maximum: the TMEM load reduces the 128 values it brings in.
-      uint32_t sr[128];
-      float rowmax;
-      tmem_ld128_max_wait(tS, sr, rowmax);
-      float* s = reinterpret_cast<float*>(sr);
+      // Where S_t(j) is: two buffers, one per tile; three buffers in rotation, S_t(j) in
+      // buffer (its position in the sequence S_0(0), S_1(0), S_0(1), ...) % 3; one buffer
+      // shared by both tiles.
+      const int pos = t ? min(j + 1, n0) + j : 2 * j;
+      const int buf = NS == 2 ? t : (NS == 3 ? pos % 3 : 0);
+      const uint32_t tS = tbase + lane_off + static_cast<uint32_t>(buf * BN);
 
-      // Mask: keys >= N (ragged last tile) and, on the diagonal tile, keys > row.  (The
-      // condition is the same for the whole warp.)  The loaded maximum counted the masked
-      // keys, so it is taken again over the kept ones: four chains of three-input max.
-      const int key0 = (jlo + j) * kBlockN;
-      const bool diag = p.causal && (key0 + kBlockN - 1 > r0);
-      if (diag || key0 + kBlockN > p.N) {
-        int lim = p.N - 1 - key0;
-        if (p.causal) lim = min(lim, r0 + rr - key0);
+      // Keys >= N (ragged last tile) and, on the diagonal tile, keys > row are masked.
+      // (The condition is the same for the whole warp.)
+      const int key0 = (jlo + j) * BN;
+      const bool masked = (p.causal && (key0 + BN - 1 > r0)) || key0 + BN > p.N;
+      int lim = p.N - 1 - key0;
+      if (p.causal) lim = min(lim, r0 + rr - key0);
+      // Loads columns c0 .. c0 + W - 1 of S_t(j) (W = 64 or 128) with their maximum from
+      // the TMEM load's reduction; on a masked tile the masked keys become -inf and the
+      // maximum is taken again over the kept ones (four chains of three-input max).
+      auto load_chunk = [&](int c0, auto width, uint32_t* sr) -> float {
+        constexpr int W = decltype(width)::value;
+        float mxl;
+        if constexpr (W == 128) tmem_ld128_max_wait(tS + c0, sr, mxl);
+        else tmem_ld64_max_wait(tS + c0, sr, mxl);
+        if (masked) {
+          float* sv = reinterpret_cast<float*>(sr);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
-        float mx[4] = {s[0], s[1], s[2], s[3]};
+          for (int c = 0; c < W; ++c) sv[c] = (c0 + c <= lim) ? sv[c] : -INFINITY;
+          float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-        for (int c = 4; c < 128; c += 2)
-          mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], s[c], s[c + 1]);
-        rowmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+          for (int c = 4; c < W; c += 2) mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], sv[c], sv[c + 1]);
+          mxl = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+        }
+        return mxl;
+      };
+      constexpr int kChunk = BN < 128 ? BN : 128;   // columns held in registers at once
+      using ChunkW = std::integral_constant<int, kChunk>;
+      uint32_t sr[kChunk];
+      float* s = reinterpret_cast<float*>(sr);
+      float rowmax;
+      if constexpr (BN == 256) {
+        // Two 128-column halves: the upper half for its maximum only, then the lower
+        // half, which stays in registers (the upper one is loaded again below).
+        const float mx_hi = load_chunk(128, ChunkW{}, sr);
+        rowmax = fmaxf(load_chunk(0, ChunkW{}, sr), mx_hi);
+      } else {
+        rowmax = load_chunk(0, ChunkW{}, sr);
       }
       const float m2_new = fmaxf(m2, rowmax * sl2);
       const float m2_use = (m2_new > m2 + kRescaleLog2<F16>) ? m2_new : m2;
       const float alpha = ex2_approx(m2 - m2_use);  // 1 if unchanged, 0 on the first tile
 
-      // Rescale O_t by alpha.  S_t(j) complete implies P_t(j-1) V done (one issuing
-      // thread, completion tracked in order), so O_t is stable here.  (With three S
-      // buffers that does not hold; the rescale then comes after the exponentials.)
+      // Rescale O_t by alpha.  With one or two S buffers, S_t(j) complete implies P_t(j-1)
+      // V done (one issuing thread, S_t(j) issued after it, completion tracked in order),
+      // so O_t is stable here.  (With three buffers that does not hold; the rescale then
+      // comes after the exponentials.)
       const bool rescale = j > 0 && __any_sync(0xffffffffu, m2_use != m2);
-      if (!Cfg::kTripleS && rescale) {
+      if (NS != 3 && rescale) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -478,25 +538,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       m2 = m2_use;
 
       // P = exp2(s * scale * log2 e - m2) on pairs (packed fp32 FMA, two MUFU ex2),
-      // row sum in packed fp32, P packed to bf16 pairs and stored over the first 64
-      // columns of S_t in four pieces.
+      // row sum in packed fp32, P packed to 16-bit pairs and stored over the first BN / 2
+      // columns of S_t, 16 columns (32 keys) at a time.
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm2 = f2_pack(-m2, -m2);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      auto exp_chunk = [&](int c0) {  // the kChunk scores in s are keys c0 .. c0 + kChunk - 1
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        uint32_t pk[16];
+        for (int h = 0; h < kChunk / 32; ++h) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = 32 * h + 2 * i;
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-          pk[i] = pack_elem2<F16>(p0, p1);
+          for (int i = 0; i < 16; ++i) {
+            const int c = 32 * h + 2 * i;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negm2), x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+            pk[i] = pack_elem2<F16>(p0, p1);
+          }
+          tmem_st16(tS + c0 / 2 + 16 * h, pk);
         }
-        tmem_st16(tS + 16 * h, pk);
+      };
+      exp_chunk(0);
+      if constexpr (BN == 256) {
+        // The upper half again (its columns are still S: the P of the lower half went to
+        // columns 0 .. 63).
+        load_chunk(128, ChunkW{}, sr);
+        exp_chunk(128);
       }
       float a0, a1, a2, a3, a4, a5, a6, a7;
       f2_unpack(acc[0], a0, a1);
@@ -504,7 +573,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       f2_unpack(acc[2], a4, a5);
       f2_unpack(acc[3], a6, a7);
       l = l * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
-      if constexpr (Cfg::kTripleS) {
+      if constexpr (NS == 3) {
         if (rescale) {
           // S_t(j) may have finished before P_t(j-1) V.  The MMA thread's products
           // complete in issue order, so wait for the first product it issues after
@@ -626,17 +695,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
-template <int D, bool F16>
+template <int D, int BN, bool F16>
 cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, const AttnTcParams& p, cudaStream_t stream) {
-  using Cfg = AttnTcCfg<D>;
+  using Cfg = AttnTcCfg<D, BN>;
   static_assert(sizeof(AttnTcBarriers) <= 512, "barrier block");
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, F16>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, BN, F16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.nqb) * p.BH * p.splits;
-  attn_fwd_tc_kernel<D, F16><<<static_cast<unsigned>(grid), kAttnThreads, Cfg::kSmemBytes, stream>>>(
+  attn_fwd_tc_kernel<D, BN, F16><<<static_cast<unsigned>(grid), kAttnThreads, Cfg::kSmemBytes, stream>>>(
       tq, tk, tv, to, p);
   return cudaGetLastError();
 }

@@ -16,9 +16,9 @@ namespace osfa {
 cudaError_t status_word(unsigned** out);
 // cuTensorMapEncodeTiled from the driver (looked up once).
 cudaError_t encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out);
-// TMA map of a [BH, N, d] bf16/fp16 tensor, 128-row x 64-column boxes, 128-byte swizzle.
+// TMA map of a [BH, N, d] bf16/fp16 tensor, box_rows x 64-column boxes, 128-byte swizzle.
 bool encode_bhnd(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base,
-                 int BH, int N, int d, bool f16);
+                 int BH, int N, int d, bool f16, int box_rows);
 bool aligned(const void* p, uintptr_t a);
 fa_status from_cuda(cudaError_t e);
 // Host-side argument checks of the tensor-core forward entry points (bf16/fp16, d in

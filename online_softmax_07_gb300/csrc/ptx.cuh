@@ -265,6 +265,55 @@ __device__ __forceinline__ void mma_ts8_elect(uint32_t d_tmem, const uint32_t* a
       : "memory");
 }
 
+
+// 4 tcgen05.mma (A from TMEM, B from shared memory) into one accumulator under a single
+// elect.sync; a[k]: TMEM address of the k-th A operand, b[k]: descriptor of the k-th B.
+__device__ __forceinline__ void mma_ts4_elect(uint32_t d_tmem, const uint32_t* a, const uint64_t* b,
+                                                uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %2, 0;\n\t"
+      "setp.eq.b32 t, %2, %2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %1, f;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %1, t;\n\t"
+      "}"
+      :: "r"(d_tmem), "r"(idesc), "r"(acc), "r"(a[0]), "l"(b[0]), "r"(a[1]), "l"(b[1]), "r"(a[2]), "l"(b[2]), "r"(a[3]), "l"(b[3])
+      : "memory");
+}
+
+// 16 tcgen05.mma (A from TMEM, B from shared memory) into one accumulator under a single
+// elect.sync; a[k]: TMEM address of the k-th A operand, b[k]: descriptor of the k-th B.
+__device__ __forceinline__ void mma_ts16_elect(uint32_t d_tmem, const uint32_t* a, const uint64_t* b,
+                                                uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %2, 0;\n\t"
+      "setp.eq.b32 t, %2, %2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %1, f;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], %12, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%13], %14, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%15], %16, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%17], %18, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%19], %20, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%21], %22, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%23], %24, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%25], %26, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%27], %28, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%29], %30, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%31], %32, %1, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%33], %34, %1, t;\n\t"
+      "}"
+      :: "r"(d_tmem), "r"(idesc), "r"(acc), "r"(a[0]), "l"(b[0]), "r"(a[1]), "l"(b[1]), "r"(a[2]), "l"(b[2]), "r"(a[3]), "l"(b[3]), "r"(a[4]), "l"(b[4]), "r"(a[5]), "l"(b[5]), "r"(a[6]), "l"(b[6]), "r"(a[7]), "l"(b[7]), "r"(a[8]), "l"(b[8]), "r"(a[9]), "l"(b[9]), "r"(a[10]), "l"(b[10]), "r"(a[11]), "l"(b[11]), "r"(a[12]), "l"(b[12]), "r"(a[13]), "l"(b[13]), "r"(a[14]), "l"(b[14]), "r"(a[15]), "l"(b[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"

@@ -181,6 +181,28 @@ def test_splitkv_static_argument_checks(lib, args, expect):
     assert st == expect, abi.status_str(st)
 
 
+@pytest.mark.parametrize("block_n,d,dtype,expect", [
+    (32, 64, abi.FA_BF16, abi.FA_ERR_INVALID),
+    (192, 64, abi.FA_BF16, abi.FA_ERR_INVALID),
+    (256, 128, abi.FA_BF16, abi.FA_ERR_UNSUPPORTED),    # 256-key tiles only at d = 64
+    (64, 64, abi.FA_F16, abi.FA_ERR_UNSUPPORTED),       # study kernels are bf16 only
+    (64, 64, abi.FA_F32, abi.FA_ERR_UNSUPPORTED),
+    (64, 96, abi.FA_BF16, abi.FA_ERR_UNSUPPORTED),
+])
+def test_fa_fwd_block_argument_checks(lib, block_n, d, dtype, expect):
+    st = lib.fa_fwd_block(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 256, d, 0.1, 1, dtype, block_n, None)
+    assert st == expect, abi.status_str(st)
+
+
+def test_fa_fwd_block_empty_and_bad_scale(lib):
+    # checked on the host before any CUDA call, whatever the block size
+    for block_n in (64, 256):
+        assert lib.fa_fwd_block(FAKE, FAKE, FAKE, FAKE, None, 0, 1, 256, 64, 0.1, 1, abi.FA_BF16,
+                                block_n, None) == abi.FA_OK
+        assert lib.fa_fwd_block(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 256, 64, -1.0, 1, abi.FA_BF16,
+                                block_n, None) == abi.FA_ERR_INVALID
+
+
 def test_splitkv_rejects_f32(lib):
     st = lib.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 100, 64, 0.1, 0, 2, FAKE, 1 << 30,
                             abi.FA_F32, None)

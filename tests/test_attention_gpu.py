@@ -50,8 +50,8 @@ def test_bf16_large_logits_rescales(d, causal):
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_growing_logits_force_every_rescale(d, dtype):
     """Keys whose scores grow along the sequence: every 128-key tile raises the row max
-    by 48 (natural log units), more than the kernel's lazy-rescale thresholds (64 log2
-    units = 44.4 for bf16, 8 for fp16), so the O rescale runs on every tile."""
+    by 48 (natural log units), far more than the kernel's lazy-rescale threshold (8 log2
+    units = 5.5), so the O rescale runs on every tile."""
     N = 1024
     rnd = synth.round_to_bf16 if dtype == "bf16" else synth.round_to_f16
     q, k, v = synth.attention_inputs(1, 1, N, d, seed=72000 + d, dtype=dtype)
@@ -67,8 +67,8 @@ def test_growing_logits_force_every_rescale(d, dtype):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_f16_large_logits_rescales(d):
-    """fp16 with Q standard deviation 4 (its lazy-rescale threshold is 2^8, so the
-    reference moves often) against the oracle."""
+    """fp16 with Q standard deviation 4 (the lazy-rescale reference moves often) against
+    the oracle."""
     q, k, v = synth.attention_inputs(1, 2, 900, d, seed=71500 + d, dtype="f16", q_std=4.0)
     scale = 1.0 / math.sqrt(d)
     for causal in (False, True):
