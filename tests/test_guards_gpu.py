@@ -98,6 +98,25 @@ def test_forward_output_guards(N, d, causal):
     assert bool(torch.isfinite(o.t.float()).all()) and bool(torch.isfinite(lse.t).all())
 
 
+@pytest.mark.parametrize("N", [1, 65, 257, 1000, 8191])
+@pytest.mark.parametrize("d,block_n", [(64, 64), (64, 256), (128, 64)])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_block_size_output_guards(N, d, block_n, causal):
+    """The 64- and 256-key tile kernels (rings of 16, 6 and 10 slots) keep the guards of
+    O and LSE and leave the inputs alone."""
+    import torch
+    B, H = 1, 2
+    ins = _inputs(B, H, N, d, 101500 + N + d + block_n, torch.bfloat16)
+    copies = [g.t.clone() for g in ins]
+    o = Guarded((B, H, N, d), torch.bfloat16)
+    lse = Guarded((B, H, N), torch.float32)
+    abi.fa_fwd_block(ins[0].t, ins[1].t, ins[2].t, o.t, lse.t, B, H, N, d, 1 / math.sqrt(d),
+                     causal, abi.FA_BF16, block_n)
+    _check(o, lse, *ins)
+    _unchanged(ins, copies)
+    assert bool(torch.isfinite(o.t.float()).all()) and bool(torch.isfinite(lse.t).all())
+
+
 @pytest.mark.parametrize("N", [1, 100, 257])
 def test_forward_f32_guards(N):
     import torch
