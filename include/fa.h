@@ -244,16 +244,20 @@ fa_status online_softmax_forward(const float* x, float* y, float* m_out, float* 
  *   lse                 [B, H, N] fp32, required
  *   dq, dk, dv          [B, H, N, d], dtype, written (fp32 accumulation inside)
  *   workspace           caller-owned device scratch of at least
- *                       fa_bwd_workspace_bytes(B, H, N) bytes (fp32 LSE*log2(e) and D
- *                       per query row); its contents are overwritten
+ *                       fa_bwd_workspace_bytes_dt(B, H, N, d, dtype) bytes (fp32
+ *                       LSE*log2(e) and D per query row; bf16/fp16 at d = 64 also the
+ *                       fp32 dQ accumulator); its contents are overwritten
  * Alignment: bf16/fp16: every pointer but lse 16 bytes, lse 4; fp32: 4 bytes, the
  * workspace 16.  B*H*N == 0 is a no-op (FA_OK).
- * Every output element is written exactly once by one block (no atomics), so results
- * are deterministic.  Stream order: the call is ordered on `stream` like a single launch;
- * inside it (bf16/fp16), the dQ pass runs on an internal stream of the library that forks
- * from `stream` after the statistics pass and joins it after the dQ pass, so that it can
- * overlap the dK/dV pass (stream capture sees the fork and the join).  Enqueueing is
- * serialised across host threads.  Errors: FA_ERR_INVALID (null pointer, lse missing, negative size,
+ * Determinism: dK and dV elements are each written once by one block.  dQ likewise at
+ * d = 128 and for fp32; at d = 64 (bf16/fp16) each key tile's block adds its share of dQ
+ * into the fp32 accumulator (TMA reduce-adds), in an order that varies from run to run,
+ * so dQ may differ in its last bits between runs.  Stream order: the call is ordered on
+ * `stream` like a single launch.  At d = 128 (bf16/fp16) the dQ pass runs on an internal
+ * stream of the library that forks from `stream` after the statistics pass and joins it
+ * after the dQ pass, so that it can overlap the dK/dV pass (stream capture sees the fork
+ * and the join); at d = 64 every launch is on `stream`.  Enqueueing is serialised across
+ * host threads.  Errors: FA_ERR_INVALID (null pointer, lse missing, negative size,
  * scale not finite and > 0, causal not 0/1, workspace too small), FA_ERR_UNSUPPORTED
  * (d or dtype), FA_ERR_ALIGN, FA_ERR_CUDA.
  */
@@ -262,7 +266,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* workspace, size_t workspace_bytes,
                  fa_dtype dtype, cudaStream_t stream);
 
-/* Workspace fa_bwd needs, in bytes: 8 * B * H * ceil(N / 128) * 128 (0 for negative sizes). */
+/* Workspace fa_bwd needs for this head dimension and dtype, in bytes, with
+ * n_pad = ceil(N / 128) * 128: bf16/fp16 at d = 64: 264 * B * H * n_pad (8 bytes of row
+ * statistics and a 64-float dQ accumulator row per padded query row); bf16/fp16 at
+ * d = 128 and fp32 (1 <= d <= 128): 8 * B * H * n_pad.  0 for negative sizes, for a d or
+ * dtype fa_bwd does not support, and for problems of more than INT_MAX 128-row tiles. */
+size_t fa_bwd_workspace_bytes_dt(int B, int H, int N, int d, fa_dtype dtype);
+
+/* A workspace size that serves every d and dtype of fa_bwd: the largest value of
+ * fa_bwd_workspace_bytes_dt, 264 * B * H * n_pad (0 for negative sizes). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N);
 
 /* Static, never-NULL description of a status code. */

@@ -4,6 +4,7 @@ The functions here carry the C names and signatures: ``fa_fwd``, ``fa_fwd_dt``,
 ``fa_fwd_block``,
 ``fa_fwd_splitkv``, ``fa_fwd_splitkv_workspace_bytes``, ``fa_fwd_splitkv_default_splits``,
 ``fa_fwd_splitkv_splits_for``, ``fa_fwd_splitkv_static``, ``fa_bwd``, ``fa_bwd_workspace_bytes``,
+``fa_bwd_workspace_bytes_dt``,
 ``fa_fwd_host``, ``fa_fwd_host_workspace_bytes``,
 ``online_softmax_rows``, ``online_softmax_forward``, ``fa_status_str``,
 ``fa_last_device_error`` and ``fa_selftest_wait_timeout``.  Pointer arguments accept a CUDA ``torch.Tensor``
@@ -49,6 +50,7 @@ _SIGNATURES = {
                + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
                   ctypes.c_void_p]),
     "fa_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 3),
+    "fa_bwd_workspace_bytes_dt": (ctypes.c_size_t, [ctypes.c_int] * 5),
     "online_softmax_rows": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2
                             + [ctypes.c_void_p]),
     "online_softmax_forward": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 2
@@ -201,6 +203,10 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspa
 
 def fa_bwd_workspace_bytes(B, H, N) -> int:
     return int(load().fa_bwd_workspace_bytes(B, H, N))
+
+
+def fa_bwd_workspace_bytes_dt(B, H, N, d, dtype) -> int:
+    return int(load().fa_bwd_workspace_bytes_dt(B, H, N, d, dtype))
 
 
 def online_softmax_rows(x, m_out, l_out, rows, length, stream=None) -> None:

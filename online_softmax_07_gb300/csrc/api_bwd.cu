@@ -19,8 +19,30 @@ namespace {
 
 long long bwd_n_pad(int N) { return (static_cast<long long>(N) + kBlockM - 1) / kBlockM * kBlockM; }
 
-// fp32 LSE * log2(e) and fp32 D per (head, padded query row).
-long long bwd_ws_bytes(long long BH, int N) { return 2 * BH * bwd_n_pad(N) * 4; }
+// fp32 LSE * log2(e) and fp32 D per (head, padded query row); the tensor-core path at
+// d = 64 also keeps its fp32 dQ accumulator there (64 floats per padded row).  The fp32
+// path needs D for each real row (B * H * N floats), within the same 8 bytes a row.
+// 0 for sizes fa_bwd rejects (more than INT_MAX tiles).
+long long bwd_ws_bytes(long long BH, int N, int d, fa_dtype dtype) {
+  const long long n_pad = bwd_n_pad(N);
+  if (BH * (n_pad / kBlockM) > INT_MAX) return 0;
+  if (dtype == FA_F32) return 2 * BH * n_pad * 4;
+  return bwd_tc_ws_bytes(BH, n_pad, d);
+}
+
+// TMA map of the d = 64 dQ accumulator: [BH, n_pad, 64] fp32, boxes of 32 rows x 32
+// columns (128 bytes), 128-byte swizzle (the reduction warps' staging layout).
+bool encode_dq_acc(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const float* base,
+                   int BH, int n_pad) {
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(n_pad), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {64 * 4, static_cast<cuuint64_t>(n_pad) * 64 * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 // The query-outer pass's stream and its fork / join events, created once per device.
 // Enqueueing is serialised by the mutex, so that each event's latest record is the one
@@ -64,7 +86,15 @@ extern "C" {
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N) {
   if (B < 0 || H < 0 || N < 0) return 0;
-  return static_cast<size_t>(bwd_ws_bytes(static_cast<long long>(B) * H, N));
+  return static_cast<size_t>(bwd_ws_bytes(static_cast<long long>(B) * H, N, 64, FA_BF16));
+}
+
+size_t fa_bwd_workspace_bytes_dt(int B, int H, int N, int d, fa_dtype dtype) {
+  if (B < 0 || H < 0 || N < 0) return 0;
+  if (dtype == FA_F32 ? (d < 1 || d > 128)
+                      : ((dtype != FA_BF16 && dtype != FA_F16) || (d != 64 && d != 128)))
+    return 0;
+  return static_cast<size_t>(bwd_ws_bytes(static_cast<long long>(B) * H, N, d, dtype));
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -87,9 +117,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   for (const void* ptr : ptrs)
     if (!aligned(ptr, f32 ? 4 : 16)) return FA_ERR_ALIGN;
   if (!aligned(lse, 4) || !aligned(workspace, 16)) return FA_ERR_ALIGN;
-  if (workspace_bytes < static_cast<size_t>(bwd_ws_bytes(BH, N))) return FA_ERR_INVALID;
   const long long nblk = bwd_n_pad(N) / kBlockM;
   if (nblk * BH > INT_MAX) return FA_ERR_INVALID;
+  if (workspace_bytes < static_cast<size_t>(bwd_ws_bytes(BH, N, d, dtype))) return FA_ERR_INVALID;
   if (f32) {
     // CUDA cores, warp per row: D (fp32, first B*H*N floats of the workspace), then the
     // key pass and the query pass.
@@ -106,7 +136,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (e != cudaSuccess) return FA_ERR_CUDA;
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if ((e = encode_fn(&enc)) != cudaSuccess) return FA_ERR_CUDA;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tacc;
   const int bh = static_cast<int>(BH);
   const bool f16 = dtype == FA_F16;
   if (!encode_bhnd(enc, &tq, q, bh, N, d, f16, kBlockM) ||
@@ -114,6 +144,12 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
       !encode_bhnd(enc, &tv, v, bh, N, d, f16, kBlockM) ||
       !encode_bhnd(enc, &tdo, dout, bh, N, d, f16, kBlockM))
     return FA_ERR_CUDA;
+  const int n_pad = static_cast<int>(nblk * kBlockM);
+  // d = 64: the dQ accumulator follows LSE * log2(e) and D in the workspace.
+  if (d == 64 && !encode_dq_acc(enc, &tacc, static_cast<const float*>(workspace) + 2 * BH * n_pad,
+                                bh, n_pad))
+    return FA_ERR_CUDA;
+  if (d != 64) tacc = tq;  // not read at d = 128
   AttnBwdParams p;
   p.lse2 = nullptr;  // set by the launcher from the workspace
   p.dd = nullptr;
@@ -123,11 +159,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.status = status;
   p.N = N;
   p.BH = bh;
+  p.dq_acc = nullptr;  // set by the launcher (d = 64)
   p.nblk = static_cast<int>(nblk);
-  p.n_pad = static_cast<int>(nblk * kBlockM);
-  // Heads scheduled together: as many as keep the tiles each pass streams (two [N, d]
-  // tensors per head) within about 64 MB of L2.
-  const long long stream_head_bytes = 2LL * N * d * 2;
+  p.n_pad = n_pad;
+  // Heads scheduled together: as many as keep what each pass streams per head within
+  // about 64 MB of L2 (two [N, d] tensors, and at d = 64 the head's fp32 dQ accumulator
+  // rows, which every key tile's block adds into).
+  const long long stream_head_bytes = 2LL * N * d * 2 + (d == 64 ? 256LL * N : 0LL);
   p.head_group = static_cast<int>(
       std::max(1LL, std::min(BH, (64LL << 20) / std::max(1LL, stream_head_bytes))));
   p.causal = causal;
@@ -138,11 +176,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   BwdFork* fk = nullptr;
   if ((e = fork_of_current_device(&fk)) != cudaSuccess) return FA_ERR_CUDA;
   if (d == 64)
-    e = f16 ? launch_attn_bwd<64, true>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream, fk)
-            : launch_attn_bwd<64, false>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream, fk);
+    e = f16 ? launch_attn_bwd<64, true>(tq, tk, tv, tdo, tacc, o, dout, lse, ws, p, stream, fk)
+            : launch_attn_bwd<64, false>(tq, tk, tv, tdo, tacc, o, dout, lse, ws, p, stream, fk);
   else
-    e = f16 ? launch_attn_bwd<128, true>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream, fk)
-            : launch_attn_bwd<128, false>(tq, tk, tv, tdo, o, dout, lse, ws, p, stream, fk);
+    e = f16 ? launch_attn_bwd<128, true>(tq, tk, tv, tdo, tacc, o, dout, lse, ws, p, stream, fk)
+            : launch_attn_bwd<128, false>(tq, tk, tv, tdo, tacc, o, dout, lse, ws, p, stream, fk);
   return from_cuda(e);
 }
 

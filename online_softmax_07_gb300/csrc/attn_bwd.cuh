@@ -8,7 +8,7 @@
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D) with D_i = sum_c dO_ic O_ic,
 //   dQ = scale * dS K,  dK = scale * dS^T Q.
 //
-// GB300 mapping, three launches:
+// GB300 mapping at d = 128, three launches (d = 64: see AttnBwd1Cfg below):
 //  * bwd_prep: D_i and LSE_i * log2(e) for every query row into the caller's workspace
 //    (rows past N get D = 0 and +inf, so that padded queries drop out of every sum);
 //  * bwd_dkdv: one CTA per 128-key tile j keeps K_j, V_j in shared memory and dV_j, dK_j
@@ -71,9 +71,50 @@ struct AttnBwdCfg {
   static constexpr int kDqSmemBytes = kDqSmemBars + 512 + 1024;
 };
 
+// One-pass backward at d = 64 (the key-outer pass also forms dQ): each key-tile CTA
+// computes, per query tile i, the partial dQ_i += dS_ij K_j with a sixth tile product
+// (dS staged in shared memory, queries contiguous) into TMEM, and the element-wise warps
+// add it into an fp32 dQ accumulator in the workspace by TMA reduce-adds (element-wise
+// fp32 adds at L2), each warp its 32 x 32 share, during the next query tile (by then the
+// partial is complete).  A finalize launch
+// scales and rounds the accumulator into dQ.  This replaces the query-outer pass, which
+// recomputes S, P, dP and dS once more; at d = 64 the element-wise work, not the tensor
+// pipe, bounds both passes.  The accumulation order across CTAs varies, so dQ's fp32
+// sums (and at times its last bit after rounding) vary from run to run; dK and dV stay
+// deterministic.  Warp roles as in the two-pass kernels (a block of more than 384
+// threads would be compiled with 128 registers a thread, too few for the element-wise
+// warps).
+
+struct AttnBwd1Cfg {
+  static constexpr int kBoxes = 1;
+  static constexpr int kTileBytes = kBoxBytes;  // 128 rows x 64, 16-bit
+  static constexpr int kStages = 3;
+  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kSmemFixed0 = 0;           // K_j
+  static constexpr int kSmemFixed1 = kTileBytes;  // V_j
+  static constexpr int kSmemStages = 2 * kTileBytes;
+  // dS of the current tile pair, [key][query]: two 64-query boxes of 128 keys x 128 B,
+  // 128-byte swizzle (the MN-major A operand of dS K_j).
+  static constexpr int kSmemDS = kSmemStages + kStages * kStageBytes;
+  // dQ staging: per element-wise warp one box of 32 rows x 32 fp32 (4 KB).
+  static constexpr int kRedBoxBytes = 32 * 128;
+  static constexpr int kSmemRed = kSmemDS + 2 * kTileBytes;
+  static constexpr int kSmemBars = kSmemRed + 8 * kRedBoxBytes;
+  static constexpr int kSmemBytes = kSmemBars + 512 + 1024;
+  // TMEM: S^T, dP^T (dS^T packed over it), dV, dK, P^T (16-bit, two queries a column:
+  // its own columns, so that the next S^T may overwrite S^T as soon as the element-wise
+  // warps hold it in registers) and the dQ partial.
+  static constexpr bool kDouble = false;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 320;
+  static constexpr uint32_t kColX = 0;  // unused (one S^T buffer)
+  static constexpr uint32_t kColP = 384, kColDQ = 448;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
 struct AttnBwdParams {
   const float* lse2;   // [BH, n_pad]: LSE * log2(e), +inf for rows >= N
   const float* dd;     // [BH, n_pad]: D = rowsum(dO * O), 0 for rows >= N
+  float* dq_acc;       // one-pass backward: [BH, n_pad, 64] fp32 dQ / scale accumulator
   void* dq;            // [BH, N, d] outputs, 16-bit
   void* dk;
   void* dv;
@@ -97,10 +138,18 @@ struct BwdFork {
   cudaEvent_t fork, join;
 };
 
+// Workspace bytes of the tensor-core backward: fp32 LSE * log2(e) and D per padded query
+// row, and at d = 64 the fp32 dQ accumulator (64 floats per padded row) after them.
+inline long long bwd_tc_ws_bytes(long long BH, long long n_pad, int d) {
+  return BH * n_pad * (2 * 4 + (d == 64 ? 64 * 4 : 0));
+}
+
+// tdq_acc: at d = 64 a TMA map of the dQ accumulator ([BH, n_pad, 64] fp32, boxes of
+// 32 x 32, 128-byte swizzle); unused at d = 128.
 template <int D, bool F16>
 cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const void* o, const void* dout,
-                            const float* lse, float* ws, const AttnBwdParams& p,
+                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const void* o,
+                            const void* dout, const float* lse, float* ws, const AttnBwdParams& p,
                             cudaStream_t stream, const BwdFork* fork);
 
 }  // namespace osfa

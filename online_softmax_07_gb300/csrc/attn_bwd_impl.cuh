@@ -4,6 +4,9 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <type_traits>
+
 #include "attn_bwd.cuh"
 #include "attn_tc_impl.cuh"  // shared-memory / instruction descriptors, 16-bit packing
 
@@ -23,6 +26,7 @@ struct AttnBwdBarriers {
   uint64_t stage_empty[4];
   uint64_t v_full[4];       // query-outer: the V ring
   uint64_t v_empty[4];
+  uint64_t s_free;          // one-pass (d = 64): the element-wise warps hold S^T in registers
   uint32_t tmem_base;
   int abort;
 };
@@ -37,6 +41,36 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
       : "memory");
 }
 
+// Element-wise add of a shared-memory box into the global tensor of `tmap` (fp32 adds,
+// done at L2); completion tracked like a TMA store, by bulk groups.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int x, int y,
+                                                  int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// mbar_wait with a non-blocking probe first: in these loops most waits find their phase
+// complete, and mbarrier.test_wait reports that sooner than the potentially suspending
+// try_wait (measured: 1.6 % on the d = 64 backward).
+__device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                         unsigned* status) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0 || mbar_wait(bar, parity, abort, status);
+}
+
+// Instruction-descriptor bit 15 (kind::f16): the A operand is MN-major in shared memory.
+constexpr uint32_t kIdescAMnMajor = 1u << 15;
+
 // Two 16-bit values of the kernel's element type (lower address in bits 0..15) to fp32.
 template <bool F16>
 __device__ __forceinline__ void unpack_elem2(uint32_t v, float& lo, float& hi) {
@@ -49,6 +83,25 @@ __device__ __forceinline__ void unpack_elem2(uint32_t v, float& lo, float& hi) {
     lo = __uint_as_float(v << 16);
     hi = __uint_as_float(v & 0xFFFF0000u);
   }
+}
+
+// Four 16-byte shared-memory stores of v[0..15] to the chunks C0 .. C0+3 of a 128-byte-
+// swizzled row: chunk c goes to (base ^ (16 c)), base being the row's address plus its
+// swizzle term 16 (row % 8).  The XORs sit inside the asm, so that one base register
+// stays live instead of an address per chunk.
+template <int C0>
+__device__ __forceinline__ void st_shared_swz4(uint32_t base, const uint32_t* v) {
+  asm volatile(
+      "{\n\t.reg .b32 a;\n\t"
+      "xor.b32 a, %0, %17;\n\tst.shared.v4.b32 [a], {%1, %2, %3, %4};\n\t"
+      "xor.b32 a, %0, %18;\n\tst.shared.v4.b32 [a], {%5, %6, %7, %8};\n\t"
+      "xor.b32 a, %0, %19;\n\tst.shared.v4.b32 [a], {%9, %10, %11, %12};\n\t"
+      "xor.b32 a, %0, %20;\n\tst.shared.v4.b32 [a], {%13, %14, %15, %16};\n\t}"
+      ::"r"(base), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+      "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+      "r"(v[13]), "r"(v[14]), "r"(v[15]), "n"(C0 * 16), "n"((C0 + 1) * 16), "n"((C0 + 2) * 16),
+      "n"((C0 + 3) * 16)
+      : "memory");
 }
 
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
@@ -93,12 +146,22 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __re
                                                             const float* __restrict__ lse,
                                                             float* __restrict__ lse2,
                                                             float* __restrict__ dd, int BH, int N,
-                                                            int n_pad) {
+                                                            int n_pad, float* __restrict__ dq_acc) {
   constexpr int kPer = D / 32;  // 16-bit elements per lane and row: 2 or 4
   const long long total = static_cast<long long>(BH) * n_pad;
   const long long row0 =
       (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kPrepRows;
   const int lane = threadIdx.x & 31;
+  if (dq_acc != nullptr) {
+    // One-pass backward (d = 64): the fp32 dQ accumulator rows of these query rows start
+    // at zero (64 floats = 16 float4 per row).
+#pragma unroll
+    for (int r = 0; r < kPrepRows; ++r) {
+      const long long row = row0 + r;
+      if (row < total && lane < 16)
+        reinterpret_cast<float4*>(dq_acc + row * 64)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   uint32_t av[kPrepRows][kPer / 2], bv[kPrepRows][kPer / 2];
   bool real[kPrepRows];
 #pragma unroll
@@ -166,15 +229,17 @@ __device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t* a, flo
 }
 
 // ------------------------------------------------------------------------------------
-// Key-outer pass: dK_j, dV_j.
+// Key-outer pass: dK_j, dV_j; with Fused (d = 64 only) also the dQ partials dS K_j.
 // ------------------------------------------------------------------------------------
-template <int D, bool F16>
+template <int D, bool F16, bool Fused>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_do, const AttnBwdParams p) {
-  using Cfg = AttnBwdCfg<D>;
+                         const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dqacc, const AttnBwdParams p) {
+  static_assert(!Fused || D == 64, "the one-pass backward is for d = 64");
+  using Cfg = std::conditional_t<Fused, AttnBwd1Cfg, AttnBwdCfg<D>>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -202,6 +267,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&bars->stage_full[s]), 1);
       mbar_init(smem_u32(&bars->stage_empty[s]), 1);
     }
+    mbar_init(smem_u32(&bars->s_free), 8);
     bars->abort = 0;
     mbar_init_fence();
   }
@@ -235,7 +301,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int issued = 0;
       for (int it = 0; it < nq; ++it) {
         const int s = it % Cfg::kStages;
-        if (!mbar_wait(smem_u32(&bars->stage_empty[s]), ((it / Cfg::kStages) & 1) ^ 1, abort,
+        if (!bwd_wait(smem_u32(&bars->stage_empty[s]), ((it / Cfg::kStages) & 1) ^ 1, abort,
                        p.status))
           break;
         const uint32_t full = smem_u32(&bars->stage_full[s]);
@@ -254,9 +320,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       // Every issued copy must land before the block's shared memory goes away.
       int no_abort = 0;
-      mbar_wait(fbar, 0, &no_abort, p.status);
+      bwd_wait(fbar, 0, &no_abort, p.status);
       for (int it = max(0, issued - Cfg::kStages); it < issued; ++it)
-        mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]), (it / Cfg::kStages) & 1,
+        bwd_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]), (it / Cfg::kStages) & 1,
                   &no_abort, p.status);
     }
   } else if (warp == kBwdWarpMma) {
@@ -268,7 +334,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tS = tbase + Cfg::kColS, tDP = tbase + Cfg::kColDP;
     const uint32_t tDV = tbase + Cfg::kColAcc0, tDK = tbase + Cfg::kColAcc1;
     auto wait_bar = [&](uint64_t* bar, int parity) {
-      const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, abort, p.status));
+      const bool r = __all_sync(0xffffffffu, bwd_wait(smem_u32(bar), parity, abort, p.status));
       if (r) tc_fence_after();
       return r;
     };
@@ -340,6 +406,79 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit_elect(smem_u32(&bars->dp_full[0]));
         }
       }
+    } else if constexpr (Fused) {
+      // One pass (d = 64), per query tile it:
+      //   S^T(it+1) (once the element-wise warps hold S^T(it) in registers)  |
+      //   dV(it) = P^T(it) dO_it (P^T in its own columns)  |
+      //   dK(it)  |  dQ(it) = dS(it) K_j  |  dP^T(it+1)
+      // dQ(it): A = dS from shared memory, MN-major (queries contiguous, the two 64-query
+      // boxes 16 KB apart), B = K_j, MN-major, 16 keys (2 KB of each) per step.  Products
+      // complete in issue order (one issuing thread), so the commit of dP^T(it+1) also
+      // reports dV(it), dK(it) and dQ(it) done: the element-wise warps wait for nothing
+      // else before they overwrite P^T and the dS staging or drain the dQ partial, and
+      // dQ(it+1) is issued only after ds_ready(it+1), which they signal after that drain.
+      // The products go out in groups under one elect each: this warp shares its
+      // scheduler with two element-wise warps, and every instruction on its path costs.
+      constexpr uint32_t kIdescDQ = idesc_f16kind(kBlockM, D, true, F16) | kIdescAMnMajor;
+      const uint64_t dDS = desc_sw128(sbase + Cfg::kSmemDS, kBoxBytes, 1024);
+      const uint64_t dKmn = desc_sw128(sbase + Cfg::kSmemFixed0, kBoxBytes, 1024);
+      auto group_t = [&](uint32_t tD, uint64_t dA, uint64_t dB) {  // S^T or dP^T, K = 64
+        uint64_t a[4], b[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          a[kk] = dA + 2 * kk;
+          b[kk] = dB + 2 * kk;
+        }
+        mma_ss4_elect(tD, a, b, kIdescS, 0u);
+      };
+      // dV or dK: A = 16 queries (8 packed columns) per step, the 64-query halves `half`
+      // columns apart.
+      auto group_acc = [&](uint32_t tAcc, uint32_t tA, uint32_t half, uint64_t dB, bool acc) {
+        uint32_t a[8];
+        uint64_t b[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          a[kk] = tA + (kk >> 2) * half + (kk & 3) * 8;
+          b[kk] = dB + kk * 128;
+        }
+        mma_ts8_elect(tAcc, a, b, kIdescAcc, acc ? 1u : 0u);
+      };
+      const uint32_t tP = tbase + Cfg::kColP, tDQ = tbase + Cfg::kColDQ;
+      if (ok) {
+        group_t(tS, dK, desc_k(0, 0));
+        mma_commit_elect(smem_u32(&bars->s_full[0]));
+        group_t(tDP, dV, desc_k(0, 1));
+        mma_commit_elect(smem_u32(&bars->dp_full[0]));
+      }
+      for (int it = 0; ok && it < nq; ++it) {
+        const bool more = it + 1 < nq;
+        if (more) {
+          if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
+                              ((it + 1) / Cfg::kStages) & 1) &&
+                     wait_bar(&bars->s_free, it & 1)))
+            break;
+          group_t(tS, dK, desc_k(it + 1, 0));
+          mma_commit_elect(smem_u32(&bars->s_full[0]));
+        }
+        if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
+        group_acc(tDV, tP, 32, desc_mn(it, 1), it > 0);
+        if (!(ok = wait_bar(&bars->ds_ready[0], it & 1))) break;
+        group_acc(tDK, tDP, 64, desc_mn(it, 0), it > 0);
+        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
+        {
+          uint64_t a[8], b[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            a[kk] = dDS + kk * 128;
+            b[kk] = dKmn + kk * 128;
+          }
+          mma_ss8_elect(tDQ, a, b, kIdescDQ, 0u);
+        }
+        if (more) {
+          group_t(tDP, dV, desc_k(it + 1, 1));
+          mma_commit_elect(smem_u32(&bars->dp_full[0]));
+        }
+      }
     } else {
     if (ok) {
       issue_t(tS, dK, desc_k(0, 0));
@@ -370,7 +509,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
     mma_commit_elect(smem_u32(&bars->mma_drain));
     int no_abort = 0;
-    mbar_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
+    bwd_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ element-wise warps
@@ -382,17 +521,152 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    // P^T of 32 queries (columns c0 .. c0+31 of this key's row) from S^T:
+    // exp2(S^T * scale * log2 e - LSE * log2 e), kept in fp32 pairs (pv, for dS^T) and
+    // packed to 16 bits (pk, the A operand of dV); causal diagonal tile: query q sees key r
+    // iff r <= q.
+    auto p_chunk = [&](const uint32_t* sr, const float* lse2s, int c0, bool diag, uint64_t* pv,
+                       uint32_t* pk) {
+      const float4* l4 = reinterpret_cast<const float4*>(lse2s + c0);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 l = l4[c4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 4 * c4 + 2 * e;
+          const uint64_t negl = e ? f2_pack(-l.z, -l.w) : f2_pack(-l.x, -l.y);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
+                           negl),
+                    x0, x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (diag) {
+            if (c0 + c < r) p0 = 0.f;
+            if (c0 + c + 1 < r) p1 = 0.f;
+          }
+          pv[c >> 1] = f2_pack(p0, p1);
+          pk[c >> 1] = pack_elem2<F16>(p0, p1);
+        }
+      }
+    };
+    // dS^T = P^T * (dP^T - D) of 32 queries, packed to 16 bits.
+    auto ds_chunk = [&](const uint32_t* dr, const float* dds, int c0, const uint64_t* pv,
+                        uint32_t* pd) {
+      const float4* d4 = reinterpret_cast<const float4*>(dds + c0);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 dq4 = d4[c4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 4 * c4 + 2 * e;
+          const uint64_t negd = e ? f2_pack(-dq4.z, -dq4.w) : f2_pack(-dq4.x, -dq4.y);
+          const uint64_t ds = f2_mul(
+              pv[c >> 1], f2_add(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), negd));
+          float d0, d1;
+          f2_unpack(ds, d0, d1);
+          pd[c >> 1] = pack_elem2<F16>(d0, d1);
+        }
+      }
+    };
+    // One-pass: the dQ partial of query tile t (TMEM lanes 32 wq .. +31 = its queries,
+    // columns 32 h .. +31) goes through this warp's 32 x 32 fp32 staging box (128-byte
+    // swizzle) into the accumulator by a TMA reduce-add.  Called once the partial is
+    // known complete (dP^T of tile t + 1 seen, or the final commit).
+    auto reduce_dq = [&](int t) {
+      if constexpr (Fused) {
+        uint32_t a[32];
+        tmem_ld32_wait(tbase + lane_off + Cfg::kColDQ + 32 * h, a);
+        tc_fence_before();
+        if (lane == 0) bulk_wait_group_read_0();  // the last reduce-add has read the box
+        __syncwarp();
+        const uint32_t row =
+            sbase + Cfg::kSmemRed + warp * Cfg::kRedBoxBytes + lane * 128 + ((lane & 7) << 4);
+        st_shared_swz4<0>(row, a);
+        st_shared_swz4<4>(row, a + 16);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dqacc, sbase + Cfg::kSmemRed + warp * Cfg::kRedBoxBytes, 32 * h,
+                            (i0 + t) * kBlockM + wq * 32, bh);
+          bulk_commit_group();
+        }
+      }
+    };
     // The statistics of query tile it come in by TMA with its stage; the warps wait on the
     // stage's own barrier to see them, for tile it+1 at the end of tile it (off the path
     // from S^T to P^T; the stage is refilled only after these warps are done with it).
-    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->stage_full[0]), 0, abort, p.status));
+    ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->stage_full[0]), 0, abort, p.status));
+    if constexpr (Fused) {
+      // One pass (d = 64), per query tile it: S^T into registers, "S^T free" (the next S^T
+      // may overwrite it), P; then, once dP^T(it) is in (which also reports dV, dK and dQ
+      // of tile it - 1 complete), P^T into its own columns, p_done, the dQ partial of tile
+      // it - 1 drained, dS^T over dP^T and dS into the shared-memory staging, ds_ready.
+      const uint32_t tP = tbase + lane_off + Cfg::kColP;
+      for (int it = 0; ok && it < nq; ++it) {
+        ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        const float* lse2s = reinterpret_cast<const float*>(
+            smem + Cfg::kSmemStages + (it % Cfg::kStages) * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
+        const float* dds = lse2s + 128;
+        const bool diag = p.causal && i0 + it == j;
+        uint64_t pv[32];
+        uint32_t pk[32];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t sr[32];
+          tmem_ld32_wait(tS + 64 * h + 32 * ch, sr);
+          if (ch == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
+          }
+          p_chunk(sr, lse2s, 64 * h + 32 * ch, diag, pv + 16 * ch, pk + 16 * ch);
+        }
+        ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        // P^T: query q of this warp's half in column q / 2 of the P^T columns.
+        tmem_st16(tP + 32 * h, pk);
+        tmem_st16(tP + 32 * h + 16, pk + 16);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_done[0]));
+        if (it > 0) reduce_dq(it - 1);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = 64 * h + 32 * ch;
+          uint32_t dr[32], pd[16];
+          tmem_ld32_wait(tDP + c0, dr);
+          ds_chunk(dr, dds, c0, pv + 16 * ch, pd);
+          tmem_st16(tDP + 64 * h + 16 * ch, pd);
+          // Row r (this key) of box h: queries 64h + 32ch .. +31 are its 16-byte chunks
+          // 4ch .. 4ch+3, each at its 128-byte-swizzle position (chunk ^ (r % 8)).
+          const uint32_t row = sbase + Cfg::kSmemDS + h * kBoxBytes + r * 128 + ((r & 7) << 4);
+          if (ch == 0)
+            st_shared_swz4<0>(row, pd);
+          else
+            st_shared_swz4<4>(row, pd);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();  // dS is read by the tensor pipe
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready[0]));
+        if (it + 1 < nq)
+          ok = __all_sync(0xffffffffu,
+                          bwd_wait(smem_u32(&bars->stage_full[(it + 1) % Cfg::kStages]),
+                                    ((it + 1) / Cfg::kStages) & 1, abort, p.status));
+      }
+    } else {
     for (int it = 0; ok && it < nq; ++it) {
       // S^T of this query tile: buffer it % 2 with two buffers (barrier phase it / 2).
       const uint32_t tSb = Cfg::kDouble && (it & 1) ? tbase + lane_off + Cfg::kColX : tS;
       ok = __all_sync(0xffffffffu,
                       Cfg::kDouble
-                          ? mbar_wait(smem_u32(&bars->s_full[it & 1]), (it >> 1) & 1, abort, p.status)
-                          : mbar_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
+                          ? bwd_wait(smem_u32(&bars->s_full[it & 1]), (it >> 1) & 1, abort, p.status)
+                          : bwd_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
       const int i = i0 + it;
@@ -400,36 +674,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           smem + Cfg::kSmemStages + (it % Cfg::kStages) * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
       const float* dds = lse2s + 128;
       const bool diag = p.causal && i == j;  // query q sees key r iff r <= q
-      // P^T = exp2(S^T * scale * log2 e - LSE * log2 e): kept in registers for dS^T and
-      // stored (16-bit) over the first half of this warp's S^T columns for dV.
+      // P^T: kept in registers for dS^T and stored (16-bit) over the first half of this
+      // warp's S^T columns for dV.
       uint64_t pv[32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * h + 32 * ch;    // first query (column) of this chunk
-        uint32_t sr[32];
+        uint32_t sr[32], pk[16];
         tmem_ld32_wait(tSb + c0, sr);
-        const float4* l4 = reinterpret_cast<const float4*>(lse2s + c0);
-        uint32_t pk[16];
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l = l4[c4];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 4 * c4 + 2 * e;
-            const uint64_t negl = e ? f2_pack(-l.z, -l.w) : f2_pack(-l.x, -l.y);
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
-                             negl),
-                      x0, x1);
-            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (diag) {
-              if (c0 + c < r) p0 = 0.f;
-              if (c0 + c + 1 < r) p1 = 0.f;
-            }
-            pv[16 * ch + (c >> 1)] = f2_pack(p0, p1);
-            pk[c >> 1] = pack_elem2<F16>(p0, p1);
-          }
-        }
+        p_chunk(sr, lse2s, c0, diag, pv + 16 * ch, pk);
         tmem_st16(tSb + 64 * h + 16 * ch, pk);
       }
       tmem_wait_st();
@@ -438,31 +691,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&bars->p_done[Cfg::kDouble ? (it & 1) : 0]));
 
       // dS^T = P^T * (dP^T - D), stored over the first half of this warp's dP^T columns.
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * h + 32 * ch;
-        uint32_t dr[32];
+        uint32_t dr[32], pd[16];
         tmem_ld32_wait(tDP + c0, dr);
-        const float4* d4 = reinterpret_cast<const float4*>(dds + c0);
-        uint32_t pd[16];
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 dq4 = d4[c4];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 4 * c4 + 2 * e;
-            const uint64_t negd = e ? f2_pack(-dq4.z, -dq4.w) : f2_pack(-dq4.x, -dq4.y);
-            const uint64_t ds = f2_mul(
-                pv[16 * ch + (c >> 1)],
-                f2_add(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), negd));
-            float d0, d1;
-            f2_unpack(ds, d0, d1);
-            pd[c >> 1] = pack_elem2<F16>(d0, d1);
-          }
-        }
+        ds_chunk(dr, dds, c0, pv + 16 * ch, pd);
         tmem_st16(tDP + 64 * h + 16 * ch, pd);
       }
       tmem_wait_st();
@@ -471,11 +708,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready[0]));
       if (it + 1 < nq)
         ok = __all_sync(0xffffffffu,
-                        mbar_wait(smem_u32(&bars->stage_full[(it + 1) % Cfg::kStages]),
+                        bwd_wait(smem_u32(&bars->stage_full[(it + 1) % Cfg::kStages]),
                                   ((it + 1) / Cfg::kStages) & 1, abort, p.status));
     }
+    }
     if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
+      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
+    }
+    if (Fused && ok) {
+      tc_fence_after();
+      reduce_dq(nq - 1);
     }
     const int kg = j * kBlockM + r;
     if (ok) {
@@ -491,6 +733,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld32_wait(tbase + lane_off + Cfg::kColAcc1 + col, a);
         if (kg < p.N) store_row32<F16>(dk_row + col * 2, a, p.scale);
       }
+    }
+    // The reduce-adds in flight read this block's shared memory: they finish first.
+    if constexpr (Fused) {
+      if (lane == 0) bulk_wait_group_0();
+      __syncwarp();
     }
   }
 
@@ -584,7 +831,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int issued_k = 0, issued_v = 0;
       for (int it = 0; it < nk; ++it) {
         const int sk = it % Cfg::kDqSlotsK;
-        if (!mbar_wait(smem_u32(&bars->stage_empty[sk]), ((it / Cfg::kDqSlotsK) & 1) ^ 1, abort,
+        if (!bwd_wait(smem_u32(&bars->stage_empty[sk]), ((it / Cfg::kDqSlotsK) & 1) ^ 1, abort,
                        p.status))
           break;
         const uint32_t kfull = smem_u32(&bars->stage_full[sk]);
@@ -596,7 +843,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t vfull = kfull;
         if constexpr (Cfg::kDqSplitKV) {
           const int sv = it % Cfg::kDqSlotsV;
-          if (!mbar_wait(smem_u32(&bars->v_empty[sv]), ((it / Cfg::kDqSlotsV) & 1) ^ 1, abort,
+          if (!bwd_wait(smem_u32(&bars->v_empty[sv]), ((it / Cfg::kDqSlotsV) & 1) ^ 1, abort,
                          p.status))
             break;
           vfull = smem_u32(&bars->v_full[sv]);
@@ -608,13 +855,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(v_addr(it) + b * kBoxBytes, &tm_v, vfull, b * kBoxCols, it * kBlockM, bh);
       }
       int no_abort = 0;
-      mbar_wait(fbar, 0, &no_abort, p.status);
+      bwd_wait(fbar, 0, &no_abort, p.status);
       for (int it = max(0, issued_k - Cfg::kDqSlotsK); it < issued_k; ++it)
-        mbar_wait(smem_u32(&bars->stage_full[it % Cfg::kDqSlotsK]), (it / Cfg::kDqSlotsK) & 1,
+        bwd_wait(smem_u32(&bars->stage_full[it % Cfg::kDqSlotsK]), (it / Cfg::kDqSlotsK) & 1,
                   &no_abort, p.status);
       if constexpr (Cfg::kDqSplitKV) {
         for (int it = max(0, issued_v - Cfg::kDqSlotsV); it < issued_v; ++it)
-          mbar_wait(smem_u32(&bars->v_full[it % Cfg::kDqSlotsV]), (it / Cfg::kDqSlotsV) & 1,
+          bwd_wait(smem_u32(&bars->v_full[it % Cfg::kDqSlotsV]), (it / Cfg::kDqSlotsV) & 1,
                     &no_abort, p.status);
       }
     }
@@ -625,7 +872,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t dDO = desc_sw128(sbase + Cfg::kSmemFixed1, 16, 1024);  // A of dP
     const uint32_t tS = tbase + Cfg::kColS, tDP = tbase + Cfg::kColDP, tDQ = tbase + Cfg::kColAcc0;
     auto wait_bar = [&](uint64_t* bar, int parity) {
-      const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, abort, p.status));
+      const bool r = __all_sync(0xffffffffu, bwd_wait(smem_u32(bar), parity, abort, p.status));
       if (r) tc_fence_after();
       return r;
     };
@@ -730,7 +977,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
     mma_commit_elect(smem_u32(&bars->mma_drain));
     int no_abort = 0;
-    mbar_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
+    bwd_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
     __syncwarp();
   } else {
     const int h = warp >> 2;
@@ -748,7 +995,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t negl2 = f2_pack(-lse2, -lse2);
     const uint64_t negd2 = f2_pack(-dd, -dd);
     for (int it = 0; it < nk; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
       const int key0 = it * kBlockM;
@@ -787,8 +1034,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t tDPb = Cfg::kDouble && (it & 1) ? tbase + lane_off + Cfg::kColX : tDP;
       ok = __all_sync(0xffffffffu,
                       Cfg::kDouble
-                          ? mbar_wait(smem_u32(&bars->dp_full[it & 1]), (it >> 1) & 1, abort, p.status)
-                          : mbar_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
+                          ? bwd_wait(smem_u32(&bars->dp_full[it & 1]), (it >> 1) & 1, abort, p.status)
+                          : bwd_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -814,7 +1061,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready[Cfg::kDouble ? (it & 1) : 0]));
     }
     if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
+      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
     }
     if (ok) {
       tc_fence_after();
@@ -837,27 +1084,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// dQ = scale * accumulator, rounded to 16 bits, for the N real rows of each head; a thread
+// takes 8 columns of one row (two 16-byte loads, one 16-byte store).
+template <bool F16>
+__global__ void __launch_bounds__(256) attn_bwd_dq_finalize_kernel(const float* __restrict__ acc,
+                                                                   uint16_t* __restrict__ dq,
+                                                                   long long rows, int N,
+                                                                   int n_pad, float scale) {
+  const long long step = static_cast<long long>(gridDim.x) * 256;
+  for (long long t = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; t < rows * 8;
+       t += step) {
+    const long long row = t >> 3;  // bh * N + q
+    const int c8 = static_cast<int>(t & 7) * 8;
+    const long long bh = row / N;
+    const long long q = row - bh * N;
+    const float4* src = reinterpret_cast<const float4*>(acc + (bh * n_pad + q) * 64 + c8);
+    const float4 a = src[0], b = src[1];
+    *reinterpret_cast<uint4*>(dq + row * 64 + c8) = make_uint4(
+        pack_elem2<F16>(a.x * scale, a.y * scale), pack_elem2<F16>(a.z * scale, a.w * scale),
+        pack_elem2<F16>(b.x * scale, b.y * scale), pack_elem2<F16>(b.z * scale, b.w * scale));
+  }
+}
+
 template <int D, bool F16>
 cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const void* o, const void* dout,
-                            const float* lse, float* ws, const AttnBwdParams& p0,
-                            cudaStream_t stream, const BwdFork* fork) {
+                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const void* o,
+                            const void* dout, const float* lse, float* ws,
+                            const AttnBwdParams& p0, cudaStream_t stream, const BwdFork* fork) {
   using Cfg = AttnBwdCfg<D>;
   static_assert(sizeof(AttnBwdBarriers) <= 512, "barrier block");
   static_assert(Cfg::kSmemBytes <= 227 * 1024 && Cfg::kDqSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(AttnBwd1Cfg::kSmemBytes <= 227 * 1024, "shared memory");
+  constexpr bool kFused = (D == 64);
   AttnBwdParams p = p0;
+  const long long rows = static_cast<long long>(p.BH) * p.n_pad;
   float* lse2 = ws;
-  float* dd = ws + static_cast<long long>(p.BH) * p.n_pad;
+  float* dd = ws + rows;
   p.lse2 = lse2;
   p.dd = dd;
-  const long long rows = static_cast<long long>(p.BH) * p.n_pad;
+  p.dq_acc = kFused ? ws + 2 * rows : nullptr;
   attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((rows + 8 * kPrepRows - 1) / (8 * kPrepRows)),
                                  256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dd, p.BH,
-      p.N, p.n_pad);
+      p.N, p.n_pad, p.dq_acc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, F16>,
+  const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.BH) * p.nblk);
+  if constexpr (kFused) {
+    // One pass over the key tiles, then dQ from its accumulator.
+    using C1 = AttnBwd1Cfg;
+    if ((e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, F16, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C1::kSmemBytes)) !=
+        cudaSuccess)
+      return e;
+    attn_bwd_dkdv_kernel<D, F16, true><<<grid, kBwdThreads, C1::kSmemBytes, stream>>>(
+        tq, tk, tv, tdo, tdq_acc, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const long long out_rows = static_cast<long long>(p.BH) * p.N;
+    const long long fin_blocks = std::min<long long>((out_rows * 8 + 255) / 256, 1LL << 20);
+    attn_bwd_dq_finalize_kernel<F16><<<static_cast<unsigned>(fin_blocks), 256, 0, stream>>>(
+        p.dq_acc, static_cast<uint16_t*>(p.dq), out_rows, p.N, p.n_pad, p.scale);
+    return cudaGetLastError();
+  }
+  if ((e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, F16, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes)) !=
       cudaSuccess)
     return e;
@@ -865,10 +1154,10 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kDqSmemBytes)) !=
       cudaSuccess)
     return e;
-  const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.BH) * p.nblk);
   // The fork point is the prep's completion, recorded before the key-outer launch.
   if (fork != nullptr && (e = cudaEventRecord(fork->fork, stream)) != cudaSuccess) return e;
-  attn_bwd_dkdv_kernel<D, F16><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  attn_bwd_dkdv_kernel<D, F16, false><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(
+      tq, tk, tv, tdo, tdq_acc, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (fork == nullptr) {
     attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, stream>>>(tq, tk, tv, tdo, p);

@@ -210,11 +210,33 @@ def test_splitkv_rejects_f32(lib):
 
 
 def test_bwd_workspace_size(lib):
-    # 2 fp32 per (head, query row), rows padded to a multiple of 128
-    assert abi.fa_bwd_workspace_bytes(2, 3, 300) == 2 * 6 * 384 * 4
-    assert abi.fa_bwd_workspace_bytes(1, 1, 128) == 2 * 128 * 4
+    # Per (head, query row), rows padded to a multiple of 128: 2 fp32 statistics, and for
+    # bf16/fp16 at d = 64 a 64-float dQ accumulator row.
+    dt = abi.fa_bwd_workspace_bytes_dt
+    assert dt(2, 3, 300, 128, abi.FA_BF16) == 2 * 6 * 384 * 4
+    assert dt(2, 3, 300, 128, abi.FA_F16) == 2 * 6 * 384 * 4
+    assert dt(2, 3, 300, 64, abi.FA_BF16) == (2 + 64) * 6 * 384 * 4
+    assert dt(1, 1, 128, 64, abi.FA_F16) == (2 + 64) * 128 * 4
+    assert dt(1, 1, 128, 64, abi.FA_F32) == 2 * 128 * 4
+    assert dt(1, 1, 100, 17, abi.FA_F32) == 2 * 128 * 4
+    assert dt(1, 1, 100, 96, abi.FA_BF16) == 0       # unsupported d
+    assert dt(1, 1, 100, 129, abi.FA_F32) == 0
+    assert dt(1, 1, 100, 64, 7) == 0                 # unsupported dtype
+    assert dt(-1, 1, 100, 64, abi.FA_BF16) == 0
+    assert dt(0, 4, 100, 64, abi.FA_BF16) == 0
+    # The dtype-free size serves every case: the d = 64 one.
+    assert abi.fa_bwd_workspace_bytes(2, 3, 300) == (2 + 64) * 6 * 384 * 4
+    assert abi.fa_bwd_workspace_bytes(1, 1, 128) == (2 + 64) * 128 * 4
     assert abi.fa_bwd_workspace_bytes(0, 4, 100) == 0
     assert abi.fa_bwd_workspace_bytes(-1, 4, 100) == 0
+
+
+def test_bwd_d64_workspace_must_hold_the_dq_accumulator(lib):
+    """A workspace that serves d = 128 is too small at d = 64 (rejected before any launch)."""
+    small = abi.fa_bwd_workspace_bytes_dt(1, 2, 300, 128, abi.FA_BF16)
+    st = lib.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 300, 64, 0.1, 0,
+                    FAKE, small, abi.FA_BF16, None)
+    assert st == abi.FA_ERR_INVALID
 
 
 @pytest.mark.parametrize("args,expect", [

@@ -73,6 +73,8 @@ def _check(name, got, ref, rel_rms_gate=None, max_rel_gate=None):
     (1, 1, 64, 64, False),
     (1, 2, 256, 128, True),
     (1, 1, 383, 64, False),
+    (2, 3, 1000, 64, True),    # d = 64: up to 8 query tiles per key tile (dQ buffers reused)
+    (1, 2, 1000, 64, False),
 ])
 def test_backward_all_rows(B, H, N, d, causal):
     q, k, v, do = _inputs(B, H, N, d, seed=900 + N + d)
@@ -112,13 +114,27 @@ def test_backward_large_logits(d):
         _check(name, g, r)
 
 
-def test_backward_deterministic():
-    """Every output element is written once by one block: two runs agree bitwise."""
-    q, k, v, do = _inputs(1, 4, 1000, 128, seed=970)
+def _dq_close(got, ref):
+    """dQ at d = 64 is summed in fp32 by several blocks in a varying order: two runs may
+    differ by the rounding of those sums, at most about one 16-bit ulp per element."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    tol = 2.0 ** -7 * np.abs(ref) + 1e-5 * np.abs(ref).max()
+    return bool(np.all(np.abs(got - ref) <= tol))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_deterministic(d):
+    """dK and dV elements are written once by one block: two runs agree bitwise; dQ too
+    at d = 128, and within the rounding of its fp32 sums at d = 64."""
+    q, k, v, do = _inputs(1, 4, 1000, d, seed=970 + d)
     a = _run_bwd(q, k, v, do, 0.09, True)
     b = _run_bwd(q, k, v, do, 0.09, True)
-    for x, y in zip(a, b):
-        assert np.array_equal(x, y)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    if d == 128:
+        assert np.array_equal(a[0], b[0])
+    else:
+        assert _dq_close(a[0], b[0])
 
 
 @pytest.mark.parametrize("B,H,N,d,causal,n_sample", [
@@ -234,8 +250,10 @@ def _bwd_call(j, stream):
 
 def test_backward_concurrent_threads():
     """Three host threads, each with its own stream and inputs, call fa_bwd at the same
-    time: the dQ pass runs on a stream of the library that all calls share, forked from
-    and joined to each caller's stream; every result must equal the sequential one."""
+    time: at d = 128 the dQ pass runs on a stream of the library that all calls share,
+    forked from and joined to each caller's stream; at d = 64 the dQ accumulator sits in
+    each call's own workspace.  Every result must equal the sequential one (dQ at d = 64
+    within the rounding of its fp32 sums)."""
     import threading
 
     import torch
@@ -256,7 +274,11 @@ def test_backward_concurrent_threads():
                     g.fill_(float("nan"))
             _bwd_call(j, s)
             s.synchronize()
-            if not all(torch.equal(g, r) for g, r in zip(j["g"], refs[t])):
+            same = [torch.equal(g, r) for g, r in zip(j["g"], refs[t])]
+            if j["d"] == 64:
+                same[0] = _dq_close(j["g"][0].float().cpu().numpy(),
+                                    refs[t][0].float().cpu().numpy())
+            if not all(same):
                 ok[t] = False
 
     threads = [threading.Thread(target=worker, args=(t,)) for t in range(len(jobs))]
@@ -268,11 +290,13 @@ def test_backward_concurrent_threads():
     assert all(ok)
 
 
-def test_backward_in_cuda_graph():
-    """A captured fa_bwd (the fork to the library's dQ stream and the join back are part
-    of the capture) replays to the same gradients as the eager call."""
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_in_cuda_graph(d):
+    """A captured fa_bwd (at d = 128 the fork to the library's dQ stream and the join back
+    are part of the capture; at d = 64 the zeroing of the dQ accumulator) replays to the
+    same gradients as the eager call (dQ at d = 64 within the rounding of its sums)."""
     import torch
-    j = _bwd_job(2, 2, 900, 128, True, 2400)
+    j = _bwd_job(2, 2, 900, d, True, 2400 + d)
     _bwd_call(j, torch.cuda.current_stream())
     torch.cuda.synchronize()
     ref = [g.clone() for g in j["g"]]
@@ -288,5 +312,9 @@ def test_backward_in_cuda_graph():
             g.fill_(float("nan"))
         graph.replay()
         torch.cuda.synchronize()
-        assert all(torch.equal(g, r) for g, r in zip(j["g"], ref))
+        assert torch.equal(j["g"][1], ref[1]) and torch.equal(j["g"][2], ref[2])
+        if d == 128:
+            assert torch.equal(j["g"][0], ref[0])
+        else:
+            assert _dq_close(j["g"][0].float().cpu().numpy(), ref[0].float().cpu().numpy())
     assert abi.fa_last_device_error() == abi.FA_OK
