@@ -20,7 +20,9 @@
 //    dQ += dS K_j the same way while K_j, V_j stream.
 // Splitting dQ into its own pass recomputes S and dP once more (7 tile products per
 // tile pair instead of 5) but needs no atomic accumulation: every output element is
-// written once, by one CTA, so the result is deterministic.
+// written once, by one CTA, so the result is deterministic.  At d = 128 the key-outer
+// pass fills all 512 TMEM columns (S^T, dP^T, dV, dK), leaving none for a dQ partial;
+// at d = 64 there is room, and one pass does all (AttnBwd1Cfg).
 #pragma once
 
 #include <cstdint>
@@ -36,12 +38,13 @@ constexpr int kBwdThreads = 384;
 constexpr int kBwdWarpMma = 8;
 constexpr int kBwdWarpLoad = 9;
 
+// Two-pass backward (d = 128).
 template <int D>
 struct AttnBwdCfg {
-  static_assert(D == 64 || D == 128, "head dimension");
+  static_assert(D == 128, "the two-pass backward is for d = 128");
   static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D, 16-bit
-  static constexpr int kStages = (D == 128) ? 2 : 4;      // streamed tile pairs in flight
+  static constexpr int kStages = 2;                       // streamed tile pairs in flight
   // A stage holds two streamed tiles and, for the key-outer pass, 128 LSE*log2(e)
   // and 128 D values of the query tile (1 KB).
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;
@@ -50,23 +53,16 @@ struct AttnBwdCfg {
   static constexpr int kSmemStages = 2 * kTileBytes;
   static constexpr int kSmemBars = kSmemStages + kStages * kStageBytes;
   static constexpr int kSmemBytes = kSmemBars + 512 + 1024;  // + barriers + alignment slack
-  // TMEM columns: S (or S^T), dP (or dP^T), then one or two fp32 accumulators.  At
-  // d = 64 these take 384 columns and a second S^T buffer (key-outer pass) or dP buffer
-  // (query-outer pass) fits at kColX (kDouble).
-  static constexpr bool kDouble = (D == 64);
+  // TMEM columns: S (or S^T), dP (or dP^T), then one or two fp32 accumulators: all 512.
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
-  static constexpr uint32_t kColX = 384;
   static constexpr uint32_t kTmemCols = 512;
-  // Query-outer pass at d = 128: K and V stream through separate rings, since K_j is
-  // held until dQ += dS K_j (its last use) and V_j only until dP = dO V_j^T; K gets the
-  // deeper ring, three slots, and V two, beside the resident Q_i, dO_i.  At d = 64 a
-  // single ring of four K|V pairs (one barrier per pair) measured faster.
-  static constexpr bool kDqSplitKV = (D == 128);
-  static constexpr int kDqSlotsK = kDqSplitKV ? 3 : 4;  // K slots, or K|V pairs
-  static constexpr int kDqSlotsV = kDqSplitKV ? 2 : 0;
-  static constexpr int kDqSlotBytes = kDqSplitKV ? kTileBytes : 2 * kTileBytes;
+  // Query-outer pass: K and V stream through separate rings, since K_j is held until
+  // dQ += dS K_j (its last use) and V_j only until dP = dO V_j^T; K gets the deeper
+  // ring, three slots, and V two, beside the resident Q_i, dO_i.
+  static constexpr int kDqSlotsK = 3;
+  static constexpr int kDqSlotsV = 2;
   static constexpr int kDqSmemK = kSmemStages;
-  static constexpr int kDqSmemV = kDqSmemK + kDqSlotsK * kDqSlotBytes;
+  static constexpr int kDqSmemV = kDqSmemK + kDqSlotsK * kTileBytes;
   static constexpr int kDqSmemBars = kDqSmemV + kDqSlotsV * kTileBytes;
   static constexpr int kDqSmemBytes = kDqSmemBars + 512 + 1024;
 };
@@ -104,9 +100,7 @@ struct AttnBwd1Cfg {
   // TMEM: S^T, dP^T (dS^T packed over it), dV, dK, P^T (16-bit, two queries a column:
   // its own columns, so that the next S^T may overwrite S^T as soon as the element-wise
   // warps hold it in registers) and the dQ partial.
-  static constexpr bool kDouble = false;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 320;
-  static constexpr uint32_t kColX = 0;  // unused (one S^T buffer)
   static constexpr uint32_t kColP = 384, kColDQ = 448;
   static constexpr uint32_t kTmemCols = 512;
 };

@@ -14,12 +14,10 @@ namespace osfa {
 
 struct AttnBwdBarriers {
   uint64_t fixed_full;   // TMA -> all: the two resident tiles are in shared memory
-  // With one S (dP) buffer only index 0 of these is used; with two (d = 64), index b
-  // belongs to buffer b (s_full, dp_full) or to tile pairs of parity b (p_done, ds_ready).
-  uint64_t s_full[2];    // MMA -> element-wise: S (or S^T) of a tile pair in TMEM
-  uint64_t dp_full[2];   // MMA -> element-wise: dP (or dP^T) in TMEM
-  uint64_t p_done[2];    // element-wise -> MMA: P^T stored (key-outer) / S read (query-outer)
-  uint64_t ds_ready[2];  // element-wise -> MMA: dS (or dS^T) stored in TMEM
+  uint64_t s_full;       // MMA -> element-wise: S (or S^T) of a tile pair in TMEM
+  uint64_t dp_full;      // MMA -> element-wise: dP (or dP^T) in TMEM
+  uint64_t p_done;       // element-wise -> MMA: P^T stored (key-outer) / S read (query-outer)
+  uint64_t ds_ready;     // element-wise -> MMA: dS (or dS^T) stored in TMEM
   uint64_t acc_final;    // MMA -> element-wise: the last accumulation finished
   uint64_t mma_drain;    // MMA warp: all of its MMAs finished (before TMEM is freed)
   uint64_t stage_full[4];   // key-outer: Q_i, dO_i stages; query-outer: the K ring
@@ -255,12 +253,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->fixed_full), 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bars->s_full[b]), 1);
-      mbar_init(smem_u32(&bars->dp_full[b]), 1);
-      mbar_init(smem_u32(&bars->p_done[b]), 8);    // one arrival per element-wise warp
-      mbar_init(smem_u32(&bars->ds_ready[b]), 8);
-    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->dp_full), 1);
+    mbar_init(smem_u32(&bars->p_done), 8);    // one arrival per element-wise warp
+    mbar_init(smem_u32(&bars->ds_ready), 8);
     mbar_init(smem_u32(&bars->acc_final), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
     for (int s = 0; s < Cfg::kStages; ++s) {
@@ -370,43 +366,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Each TMEM region is overwritten only after the product that reads it (one issuing
     // thread: products complete in issue order).
     bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0);
-    if constexpr (Cfg::kDouble) {
-      // Two S^T buffers (d = 64): S^T(it) in buffer it % 2, so S^T(it+2) is issued right
-      // after dV(it) has consumed P^T(it) and the element-wise warps never wait for their
-      // next S^T on this chain.  Order per query tile it:
-      //   dV(it)  |  S^T(it+2)  |  dK(it)  |  dP^T(it+1)
-      // p_done alternates between two barriers: the element-wise warps may finish P^T(it+1)
-      // before this warp has taken P^T(it).
-      auto colS = [&](int i) { return tbase + ((i & 1) ? Cfg::kColX : Cfg::kColS); };
-      if (ok) {
-        issue_t(colS(0), dK, desc_k(0, 0));
-        mma_commit_elect(smem_u32(&bars->s_full[0]));
-        issue_t(tDP, dV, desc_k(0, 1));
-        mma_commit_elect(smem_u32(&bars->dp_full[0]));
-        if (nq > 1 && (ok = wait_bar(&bars->stage_full[1 % Cfg::kStages], (1 / Cfg::kStages) & 1))) {
-          issue_t(colS(1), dK, desc_k(1, 0));
-          mma_commit_elect(smem_u32(&bars->s_full[1]));
-        }
-      }
-      for (int it = 0; ok && it < nq; ++it) {
-        if (!(ok = wait_bar(&bars->p_done[it & 1], (it >> 1) & 1))) break;
-        issue_acc(tDV, colS(it), desc_mn(it, 1), it > 0);
-        if (it + 2 < nq) {
-          if (!(ok = wait_bar(&bars->stage_full[(it + 2) % Cfg::kStages],
-                              ((it + 2) / Cfg::kStages) & 1)))
-            break;
-          issue_t(colS(it), dK, desc_k(it + 2, 0));
-          mma_commit_elect(smem_u32(&bars->s_full[it & 1]));
-        }
-        if (!(ok = wait_bar(&bars->ds_ready[0], it & 1))) break;
-        issue_acc(tDK, tDP, desc_mn(it, 0), it > 0);
-        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
-        if (it + 1 < nq) {
-          issue_t(tDP, dV, desc_k(it + 1, 1));
-          mma_commit_elect(smem_u32(&bars->dp_full[0]));
-        }
-      }
-    } else if constexpr (Fused) {
+    if constexpr (Fused) {
       // One pass (d = 64), per query tile it:
       //   S^T(it+1) (once the element-wise warps hold S^T(it) in registers)  |
       //   dV(it) = P^T(it) dO_it (P^T in its own columns)  |
@@ -446,9 +406,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t tP = tbase + Cfg::kColP, tDQ = tbase + Cfg::kColDQ;
       if (ok) {
         group_t(tS, dK, desc_k(0, 0));
-        mma_commit_elect(smem_u32(&bars->s_full[0]));
+        mma_commit_elect(smem_u32(&bars->s_full));
         group_t(tDP, dV, desc_k(0, 1));
-        mma_commit_elect(smem_u32(&bars->dp_full[0]));
+        mma_commit_elect(smem_u32(&bars->dp_full));
       }
       for (int it = 0; ok && it < nq; ++it) {
         const bool more = it + 1 < nq;
@@ -458,11 +418,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      wait_bar(&bars->s_free, it & 1)))
             break;
           group_t(tS, dK, desc_k(it + 1, 0));
-          mma_commit_elect(smem_u32(&bars->s_full[0]));
+          mma_commit_elect(smem_u32(&bars->s_full));
         }
-        if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
+        if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
         group_acc(tDV, tP, 32, desc_mn(it, 1), it > 0);
-        if (!(ok = wait_bar(&bars->ds_ready[0], it & 1))) break;
+        if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
         group_acc(tDK, tDP, 64, desc_mn(it, 0), it > 0);
         mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
         {
@@ -476,33 +436,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (more) {
           group_t(tDP, dV, desc_k(it + 1, 1));
-          mma_commit_elect(smem_u32(&bars->dp_full[0]));
+          mma_commit_elect(smem_u32(&bars->dp_full));
         }
       }
     } else {
     if (ok) {
       issue_t(tS, dK, desc_k(0, 0));
-      mma_commit_elect(smem_u32(&bars->s_full[0]));
+      mma_commit_elect(smem_u32(&bars->s_full));
       issue_t(tDP, dV, desc_k(0, 1));
-      mma_commit_elect(smem_u32(&bars->dp_full[0]));
+      mma_commit_elect(smem_u32(&bars->dp_full));
     }
     for (int it = 0; ok && it < nq; ++it) {
       const bool more = it + 1 < nq;
-      if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
+      if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
       issue_acc(tDV, tS, desc_mn(it, 1), it > 0);
       if (more) {
         if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
                             ((it + 1) / Cfg::kStages) & 1)))
           break;
         issue_t(tS, dK, desc_k(it + 1, 0));
-        mma_commit_elect(smem_u32(&bars->s_full[0]));
+        mma_commit_elect(smem_u32(&bars->s_full));
       }
-      if (!(ok = wait_bar(&bars->ds_ready[0], it & 1))) break;
+      if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
       issue_acc(tDK, tDP, desc_mn(it, 0), it > 0);
       mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
       if (more) {
         issue_t(tDP, dV, desc_k(it + 1, 1));
-        mma_commit_elect(smem_u32(&bars->dp_full[0]));
+        mma_commit_elect(smem_u32(&bars->dp_full));
       }
     }
     }
@@ -603,7 +563,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // it - 1 drained, dS^T over dP^T and dS into the shared-memory staging, ds_ready.
       const uint32_t tP = tbase + lane_off + Cfg::kColP;
       for (int it = 0; ok && it < nq; ++it) {
-        ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
+        ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
         if (!ok) break;
         tc_fence_after();
         const float* lse2s = reinterpret_cast<const float*>(
@@ -623,7 +583,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           p_chunk(sr, lse2s, 64 * h + 32 * ch, diag, pv + 16 * ch, pk + 16 * ch);
         }
-        ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
+        ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
         if (!ok) break;
         tc_fence_after();
         // P^T: query q of this warp's half in column q / 2 of the P^T columns.
@@ -632,7 +592,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->p_done[0]));
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
         if (it > 0) reduce_dq(it - 1);
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
@@ -653,7 +613,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_proxy_async_smem();  // dS is read by the tensor pipe
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready[0]));
+        if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
         if (it + 1 < nq)
           ok = __all_sync(0xffffffffu,
                           bwd_wait(smem_u32(&bars->stage_full[(it + 1) % Cfg::kStages]),
@@ -661,12 +621,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     } else {
     for (int it = 0; ok && it < nq; ++it) {
-      // S^T of this query tile: buffer it % 2 with two buffers (barrier phase it / 2).
-      const uint32_t tSb = Cfg::kDouble && (it & 1) ? tbase + lane_off + Cfg::kColX : tS;
-      ok = __all_sync(0xffffffffu,
-                      Cfg::kDouble
-                          ? bwd_wait(smem_u32(&bars->s_full[it & 1]), (it >> 1) & 1, abort, p.status)
-                          : bwd_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
       const int i = i0 + it;
@@ -681,17 +636,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * h + 32 * ch;    // first query (column) of this chunk
         uint32_t sr[32], pk[16];
-        tmem_ld32_wait(tSb + c0, sr);
+        tmem_ld32_wait(tS + c0, sr);
         p_chunk(sr, lse2s, c0, diag, pv + 16 * ch, pk);
-        tmem_st16(tSb + 64 * h + 16 * ch, pk);
+        tmem_st16(tS + 64 * h + 16 * ch, pk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->p_done[Cfg::kDouble ? (it & 1) : 0]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
 
       // dS^T = P^T * (dP^T - D), stored over the first half of this warp's dP^T columns.
-      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -705,7 +660,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready[0]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
       if (it + 1 < nq)
         ok = __all_sync(0xffffffffu,
                         bwd_wait(smem_u32(&bars->stage_full[(it + 1) % Cfg::kStages]),
@@ -773,12 +728,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->fixed_full), 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bars->s_full[b]), 1);
-      mbar_init(smem_u32(&bars->dp_full[b]), 1);
-      mbar_init(smem_u32(&bars->p_done[b]), 8);    // one arrival per element-wise warp
-      mbar_init(smem_u32(&bars->ds_ready[b]), 8);
-    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->dp_full), 1);
+    mbar_init(smem_u32(&bars->p_done), 8);    // one arrival per element-wise warp
+    mbar_init(smem_u32(&bars->ds_ready), 8);
     mbar_init(smem_u32(&bars->acc_final), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
     for (int s = 0; s < Cfg::kDqSlotsK; ++s) {
@@ -802,14 +755,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tbase = bars->tmem_base;
   volatile int* abort = &bars->abort;
   auto k_addr = [&](int it) {
-    return sbase + Cfg::kDqSmemK + (it % Cfg::kDqSlotsK) * Cfg::kDqSlotBytes;
+    return sbase + Cfg::kDqSmemK + (it % Cfg::kDqSlotsK) * Cfg::kTileBytes;
   };
-  auto v_addr = [&](int it) {
-    if constexpr (Cfg::kDqSplitKV)
-      return sbase + Cfg::kDqSmemV + (it % Cfg::kDqSlotsV) * Cfg::kTileBytes;
-    else
-      return k_addr(it) + Cfg::kTileBytes;  // the second tile of the pair
-  };
+  auto v_addr = [&](int it) { return sbase + Cfg::kDqSmemV + (it % Cfg::kDqSlotsV) * Cfg::kTileBytes; };
 
   if (warp >= 10) {
     // idle
@@ -826,8 +774,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sbase + Cfg::kSmemFixed0 + b * kBoxBytes, &tm_q, fbar, b * kBoxCols, i * kBlockM, bh);
         tma_load_3d(sbase + Cfg::kSmemFixed1 + b * kBoxBytes, &tm_do, fbar, b * kBoxCols, i * kBlockM, bh);
       }
-      // K_it and V_it in turn (with split rings V_it's slot frees before K_it+1's: dP is
-      // done before dQ).  With pairs, one barrier covers both tiles.
+      // K_it and V_it in turn (V_it's slot frees before K_it+1's: dP is done before dQ).
       int issued_k = 0, issued_v = 0;
       for (int it = 0; it < nk; ++it) {
         const int sk = it % Cfg::kDqSlotsK;
@@ -835,21 +782,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        p.status))
           break;
         const uint32_t kfull = smem_u32(&bars->stage_full[sk]);
-        mbar_arrive_expect_tx(kfull, Cfg::kDqSplitKV ? Cfg::kTileBytes : 2 * Cfg::kTileBytes);
+        mbar_arrive_expect_tx(kfull, Cfg::kTileBytes);
 #pragma unroll
         for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_load_3d(k_addr(it) + b * kBoxBytes, &tm_k, kfull, b * kBoxCols, it * kBlockM, bh);
         issued_k = it + 1;
-        uint32_t vfull = kfull;
-        if constexpr (Cfg::kDqSplitKV) {
-          const int sv = it % Cfg::kDqSlotsV;
-          if (!bwd_wait(smem_u32(&bars->v_empty[sv]), ((it / Cfg::kDqSlotsV) & 1) ^ 1, abort,
-                         p.status))
-            break;
-          vfull = smem_u32(&bars->v_full[sv]);
-          mbar_arrive_expect_tx(vfull, Cfg::kTileBytes);
-          issued_v = it + 1;
-        }
+        const int sv = it % Cfg::kDqSlotsV;
+        if (!bwd_wait(smem_u32(&bars->v_empty[sv]), ((it / Cfg::kDqSlotsV) & 1) ^ 1, abort,
+                      p.status))
+          break;
+        const uint32_t vfull = smem_u32(&bars->v_full[sv]);
+        mbar_arrive_expect_tx(vfull, Cfg::kTileBytes);
+        issued_v = it + 1;
 #pragma unroll
         for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_load_3d(v_addr(it) + b * kBoxBytes, &tm_v, vfull, b * kBoxCols, it * kBlockM, bh);
@@ -859,11 +803,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int it = max(0, issued_k - Cfg::kDqSlotsK); it < issued_k; ++it)
         bwd_wait(smem_u32(&bars->stage_full[it % Cfg::kDqSlotsK]), (it / Cfg::kDqSlotsK) & 1,
                   &no_abort, p.status);
-      if constexpr (Cfg::kDqSplitKV) {
-        for (int it = max(0, issued_v - Cfg::kDqSlotsV); it < issued_v; ++it)
-          bwd_wait(smem_u32(&bars->v_full[it % Cfg::kDqSlotsV]), (it / Cfg::kDqSlotsV) & 1,
-                    &no_abort, p.status);
-      }
+      for (int it = max(0, issued_v - Cfg::kDqSlotsV); it < issued_v; ++it)
+        bwd_wait(smem_u32(&bars->v_full[it % Cfg::kDqSlotsV]), (it / Cfg::kDqSlotsV) & 1,
+                 &no_abort, p.status);
     }
   } else if (warp == kBwdWarpMma) {
     constexpr uint32_t kIdescS = idesc_f16kind(kBlockM, kBlockM, false, F16);
@@ -881,17 +823,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto wait_k = [&](int it) {
       return wait_bar(&bars->stage_full[it % Cfg::kDqSlotsK], (it / Cfg::kDqSlotsK) & 1);
     };
-    // With pairs V_it came with K_it: nothing more to wait for, nothing to release early.
     auto wait_v = [&](int it) {
-      if constexpr (Cfg::kDqSplitKV)
-        return wait_bar(&bars->v_full[it % Cfg::kDqSlotsV], (it / Cfg::kDqSlotsV) & 1);
-      else
-        return true;
+      return wait_bar(&bars->v_full[it % Cfg::kDqSlotsV], (it / Cfg::kDqSlotsV) & 1);
     };
-    auto release_v = [&](int it) {
-      if constexpr (Cfg::kDqSplitKV)
-        mma_commit_elect(smem_u32(&bars->v_empty[it % Cfg::kDqSlotsV]));
-    };
+    auto release_v = [&](int it) { mma_commit_elect(smem_u32(&bars->v_empty[it % Cfg::kDqSlotsV])); };
     // S = Q_i K_j^T into tS, or dP = dO_i V_j^T into tDP: queries on lanes, keys on
     // columns; the streamed tile is the K-major B operand.
     auto issue_n = [&](uint32_t tD, uint64_t dA, uint64_t dB) {
@@ -906,72 +841,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //   dQ += dS(it) K_it (dS stored over dP(it))  |  dP(it+1)
     // so the next S is computed while dS(it) is being formed.
     bool ok = wait_bar(&bars->fixed_full, 0) && wait_k(0) && wait_v(0);
-    if constexpr (Cfg::kDouble) {
-      // Two dP buffers (d = 64): dP(it) and dS(it) in buffer it % 2, so dP(it+1) is issued
-      // together with S(it+1) instead of after dQ(it).  Order per key tile it:
-      //   S(it+1), dP(it+1) (once S(it) is in registers)  |  dQ += dS(it) K_it
-      // ds_ready alternates between two barriers: the element-wise warps may finish dS(it+1)
-      // before this warp has taken dS(it).
-      auto colDP = [&](int i) { return tbase + ((i & 1) ? Cfg::kColX : Cfg::kColDP); };
-      if (ok) {
-        issue_n(tS, dQ, k_desc(0, 16));
-        mma_commit_elect(smem_u32(&bars->s_full[0]));
-        issue_n(colDP(0), dDO, v_desc(0));
-        mma_commit_elect(smem_u32(&bars->dp_full[0]));
-        release_v(0);
+    if (ok) {
+      issue_n(tS, dQ, k_desc(0, 16));
+      mma_commit_elect(smem_u32(&bars->s_full));
+      issue_n(tDP, dDO, v_desc(0));
+      mma_commit_elect(smem_u32(&bars->dp_full));
+      release_v(0);
+    }
+    for (int it = 0; ok && it < nk; ++it) {
+      const bool more = it + 1 < nk;
+      if (more) {
+        if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
+        if (!(ok = wait_k(it + 1))) break;
+        issue_n(tS, dQ, k_desc(it + 1, 16));
+        mma_commit_elect(smem_u32(&bars->s_full));
       }
-      for (int it = 0; ok && it < nk; ++it) {
-        if (it + 1 < nk) {
-          if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
-          if (!(ok = wait_k(it + 1) && wait_v(it + 1))) break;
-          issue_n(tS, dQ, k_desc(it + 1, 16));
-          mma_commit_elect(smem_u32(&bars->s_full[0]));
-          issue_n(colDP(it + 1), dDO, v_desc(it + 1));
-          mma_commit_elect(smem_u32(&bars->dp_full[(it + 1) & 1]));
-          release_v(it + 1);
-        }
-        if (!(ok = wait_bar(&bars->ds_ready[it & 1], (it >> 1) & 1))) break;
-        const uint64_t dKmn = k_desc(it, kBoxBytes);
+      if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
+      // dQ += dS K_j: dS (16 keys = 8 packed columns per step) from the dP columns.
+      const uint64_t dKmn = k_desc(it, kBoxBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBlockM / 16; ++kk) {
-          const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
-          mma_bf16_ts_elect(tDQ, colDP(it) + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
-                            (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kDqSlotsK]));
+      for (int kk = 0; kk < kBlockM / 16; ++kk) {
+        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+        mma_bf16_ts_elect(tDQ, tDP + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
+                          (it > 0 || kk > 0) ? 1u : 0u);
       }
-    } else {
-      if (ok) {
-        issue_n(tS, dQ, k_desc(0, 16));
-        mma_commit_elect(smem_u32(&bars->s_full[0]));
-        issue_n(tDP, dDO, v_desc(0));
-        mma_commit_elect(smem_u32(&bars->dp_full[0]));
-        release_v(0);
-      }
-      for (int it = 0; ok && it < nk; ++it) {
-        const bool more = it + 1 < nk;
-        if (more) {
-          if (!(ok = wait_bar(&bars->p_done[0], it & 1))) break;
-          if (!(ok = wait_k(it + 1))) break;
-          issue_n(tS, dQ, k_desc(it + 1, 16));
-          mma_commit_elect(smem_u32(&bars->s_full[0]));
-        }
-        if (!(ok = wait_bar(&bars->ds_ready[0], it & 1))) break;
-        // dQ += dS K_j: dS (16 keys = 8 packed columns per step) from the dP columns.
-        const uint64_t dKmn = k_desc(it, kBoxBytes);
-#pragma unroll
-        for (int kk = 0; kk < kBlockM / 16; ++kk) {
-          const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
-          mma_bf16_ts_elect(tDQ, tDP + acol, dKmn + ((kk * 2048) >> 4), kIdescAcc,
-                            (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kDqSlotsK]));
-        if (more) {
-          if (!(ok = wait_v(it + 1))) break;
-          issue_n(tDP, dDO, v_desc(it + 1));
-          mma_commit_elect(smem_u32(&bars->dp_full[0]));
-          release_v(it + 1);
-        }
+      mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kDqSlotsK]));
+      if (more) {
+        if (!(ok = wait_v(it + 1))) break;
+        issue_n(tDP, dDO, v_desc(it + 1));
+        mma_commit_elect(smem_u32(&bars->dp_full));
+        release_v(it + 1);
       }
     }
     if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
@@ -995,7 +894,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t negl2 = f2_pack(-lse2, -lse2);
     const uint64_t negd2 = f2_pack(-dd, -dd);
     for (int it = 0; it < nk; ++it) {
-      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full[0]), it & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
       const int key0 = it * kBlockM;
@@ -1027,22 +926,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (it + 1 < nk) {  // S(it) is in registers: the next S may overwrite it
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->p_done[0]));
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
       }
-      // dS = P * (dP - D), stored (16-bit) over the first half of this warp's dP columns
-      // (dP of this key tile: buffer it % 2 with two buffers, barrier phase it / 2).
-      const uint32_t tDPb = Cfg::kDouble && (it & 1) ? tbase + lane_off + Cfg::kColX : tDP;
-      ok = __all_sync(0xffffffffu,
-                      Cfg::kDouble
-                          ? bwd_wait(smem_u32(&bars->dp_full[it & 1]), (it >> 1) & 1, abort, p.status)
-                          : bwd_wait(smem_u32(&bars->dp_full[0]), it & 1, abort, p.status));
+      // dS = P * (dP - D), stored (16-bit) over the first half of this warp's dP columns.
+      ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * h + 32 * ch;
         uint32_t dr[32];
-        tmem_ld32_wait(tDPb + c0, dr);
+        tmem_ld32_wait(tDP + c0, dr);
         uint32_t pd[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
@@ -1053,12 +947,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           f2_unpack(ds, d0, d1);
           pd[c >> 1] = pack_elem2<F16>(d0, d1);
         }
-        tmem_st16(tDPb + 64 * h + 16 * ch, pd);
+        tmem_st16(tDP + 64 * h + 16 * ch, pd);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready[Cfg::kDouble ? (it & 1) : 0]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
     }
     if (ok) {
       ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->acc_final), 0, abort, p.status));
@@ -1111,10 +1005,8 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const void* o,
                             const void* dout, const float* lse, float* ws,
                             const AttnBwdParams& p0, cudaStream_t stream, const BwdFork* fork) {
-  using Cfg = AttnBwdCfg<D>;
+  static_assert(D == 64 || D == 128, "head dimension");
   static_assert(sizeof(AttnBwdBarriers) <= 512, "barrier block");
-  static_assert(Cfg::kSmemBytes <= 227 * 1024 && Cfg::kDqSmemBytes <= 227 * 1024, "shared memory");
-  static_assert(AttnBwd1Cfg::kSmemBytes <= 227 * 1024, "shared memory");
   constexpr bool kFused = (D == 64);
   AttnBwdParams p = p0;
   const long long rows = static_cast<long long>(p.BH) * p.n_pad;
@@ -1133,6 +1025,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   if constexpr (kFused) {
     // One pass over the key tiles, then dQ from its accumulator.
     using C1 = AttnBwd1Cfg;
+    static_assert(C1::kSmemBytes <= 227 * 1024, "shared memory");
     if ((e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, F16, true>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C1::kSmemBytes)) !=
         cudaSuccess)
@@ -1145,30 +1038,36 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
     attn_bwd_dq_finalize_kernel<F16><<<static_cast<unsigned>(fin_blocks), 256, 0, stream>>>(
         p.dq_acc, static_cast<uint16_t*>(p.dq), out_rows, p.N, p.n_pad, p.scale);
     return cudaGetLastError();
+  } else {
+    // Two passes: dK, dV key-outer on `stream`, dQ query-outer on the side stream.
+    using Cfg = AttnBwdCfg<D>;
+    static_assert(Cfg::kSmemBytes <= 227 * 1024 && Cfg::kDqSmemBytes <= 227 * 1024,
+                  "shared memory");
+    if ((e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, F16, false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, F16>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfg::kDqSmemBytes)) != cudaSuccess)
+      return e;
+    // The fork point is the prep's completion, recorded before the key-outer launch.
+    if (fork != nullptr && (e = cudaEventRecord(fork->fork, stream)) != cudaSuccess) return e;
+    attn_bwd_dkdv_kernel<D, F16, false><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(
+        tq, tk, tv, tdo, tdq_acc, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (fork == nullptr) {
+      attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, stream>>>(tq, tk, tv,
+                                                                                  tdo, p);
+      return cudaGetLastError();
+    }
+    if ((e = cudaStreamWaitEvent(fork->side, fork->fork, 0)) != cudaSuccess) return e;
+    attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, fork->side>>>(
+        tq, tk, tv, tdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(fork->join, fork->side)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(stream, fork->join, 0);
   }
-  if ((e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, F16, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes)) !=
-      cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, F16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kDqSmemBytes)) !=
-      cudaSuccess)
-    return e;
-  // The fork point is the prep's completion, recorded before the key-outer launch.
-  if (fork != nullptr && (e = cudaEventRecord(fork->fork, stream)) != cudaSuccess) return e;
-  attn_bwd_dkdv_kernel<D, F16, false><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(
-      tq, tk, tv, tdo, tdq_acc, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (fork == nullptr) {
-    attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, stream>>>(tq, tk, tv, tdo, p);
-    return cudaGetLastError();
-  }
-  if ((e = cudaStreamWaitEvent(fork->side, fork->fork, 0)) != cudaSuccess) return e;
-  attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, fork->side>>>(tq, tk, tv, tdo,
-                                                                                    p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = cudaEventRecord(fork->join, fork->side)) != cudaSuccess) return e;
-  return cudaStreamWaitEvent(stream, fork->join, 0);
 }
 
 }  // namespace osfa
