@@ -195,8 +195,9 @@ def test_softmax_output_guards(rows, length, mode):
 @pytest.mark.parametrize("N,d,causal", [(129, 64, 1), (300, 128, 0), (257, 128, 1),
                                         (1, 64, 0)])
 def test_backward_guards(N, d, causal):
-    """dQ, dK, dV and the backward's workspace (rows padded to 128; the prep kernel
-    writes four query rows per warp) keep their guards; Q, K, V, O, LSE and dO are not
+    """dQ, dK, dV and the backward's workspace, sized exactly for this d (rows padded to
+    128; the prep kernel writes four query rows per warp; at d = 64 the dQ accumulator
+    takes the TMA reduce-adds) keep their guards; Q, K, V, O, LSE and dO are not
     written."""
     import torch
     B, H = 1, 2
@@ -210,7 +211,7 @@ def test_backward_guards(N, d, causal):
     fixed = ins + [o, lse, dout]
     copies = [g.t.clone() for g in fixed]
     grads = [Guarded((B, H, N, d), torch.bfloat16) for _ in range(3)]
-    nbytes = abi.fa_bwd_workspace_bytes(B, H, N)
+    nbytes = abi.fa_bwd_workspace_bytes_dt(B, H, N, d, abi.FA_BF16)
     ws = Guarded((nbytes,), torch.uint8)
     abi.fa_bwd(ins[0].t, ins[1].t, ins[2].t, o.t, lse.t, dout.t, grads[0].t, grads[1].t,
                grads[2].t, B, H, N, d, scale, causal, ws.t, nbytes, abi.FA_BF16)
