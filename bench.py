@@ -103,6 +103,9 @@ KERNEL_FILES = {
                              "attn_tc_impl.cuh", "ptx.cuh", "attn_bwd_d128.cu", "api_bwd.cu"],
     "attn_bwd_dq_kernel": ["attn_bwd.cuh", "attn_bwd_impl.cuh", "attn_tc.cuh",
                            "attn_tc_impl.cuh", "ptx.cuh", "attn_bwd_d128.cu", "api_bwd.cu"],
+    # the d = 64 instance of attn_bwd_dkdv_kernel: the one-pass backward
+    "attn_bwd_dkdv_kernel_d64": ["attn_bwd.cuh", "attn_bwd_impl.cuh", "attn_tc.cuh",
+                                 "attn_tc_impl.cuh", "ptx.cuh", "attn_bwd_d64.cu", "api_bwd.cu"],
 }
 
 
@@ -699,8 +702,10 @@ def suite(args):
 
     def bwd_line(name, q, k, v, do, causal):
         """fa_bwd after fa_fwd; TFLOP/s counts the five algorithmic products
-        (2.5 x the forward's FLOPs); errors against the oracle on 32 seeded query and
-        key rows (plus the first and last) of the first and last head."""
+        (2.5 x the forward's FLOPs; the kernels execute those five at d = 64, one pass with
+        the dQ partials, and seven at d = 128, where the dQ pass recomputes S and dP); errors
+        against the oracle on 32 seeded query and key rows (plus the first and last) of
+        the first and last head."""
         import oracle
         B, H, N, d = q.shape
         tq, tk, tv, tdo = (torch.from_numpy(t).to(dev, torch.bfloat16) for t in (q, k, v, do))
@@ -708,7 +713,7 @@ def suite(args):
         lse = torch.empty((B, H, N), device=dev)
         scale = 1.0 / math.sqrt(d)
         abi.fa_fwd_dt(tq, tk, tv, o, lse, B, H, N, d, scale, int(causal), abi.FA_BF16, stream)
-        nbytes = abi.fa_bwd_workspace_bytes(B, H, N)
+        nbytes = abi.fa_bwd_workspace_bytes_dt(B, H, N, d, abi.FA_BF16)
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         gq, gk, gv = torch.empty_like(tq), torch.empty_like(tq), torch.empty_like(tq)
         fn = lambda: abi.fa_bwd(tq, tk, tv, o, lse, tdo, gq, gk, gv, B, H, N, d, scale,
@@ -726,7 +731,7 @@ def suite(args):
                 rel[key].append(float(np.linalg.norm(got - r) / np.linalg.norm(r)))
         line = {"workload": name.replace("attn_", "attn_bwd_"), "dtype": "bf16", "ms": ms,
                 "TFLOP/s": tf, "pct_of_bf16_peak": 100 * tf / peaks["bf16_tflops"],
-                "executed_TFLOP/s": tf * 7 / 5}
+                "executed_TFLOP/s": tf * (5 if d == 64 else 7) / 5}
         line.update({f"{k}_rel_rms_err": max(v) for k, v in rel.items()})
         print(json.dumps(line), flush=True)
 
@@ -785,8 +790,9 @@ def backward_run(args):
     """The backward alone: by default on the B=2 H=16 N=8192 d=128 causal workload with the
     suite's seeded dO, or on the shape --backward B,H,N,d,causal gives (bf16, Q, K, V, dO
     i.i.d. N(0,1) drawn on the device from fixed seeds): fa_fwd once for O and LSE, then
-    --warmup and --steps fa_bwd calls (each a prep, a dK/dV and a dQ launch) timed with
-    CUDA events.  One JSON line; this is the command the backward's launch lists and ncu
+    --warmup and --steps fa_bwd calls (three launches each: at d = 128 a prep, the dK/dV
+    pass and the dQ pass; at d = 64 a prep, the one-pass kernel and the dQ finalize) timed
+    with CUDA events.  One JSON line; this is the command the backward's launch lists and ncu
     captures are taken with."""
     import torch
 
@@ -821,7 +827,7 @@ def backward_run(args):
     lse = torch.empty((B, H, N), device=dev)
     scale = 1.0 / math.sqrt(d)
     abi.fa_fwd_dt(tq, tk, tv, o, lse, B, H, N, d, scale, causal, abi.FA_BF16, stream)
-    nbytes = abi.fa_bwd_workspace_bytes(B, H, N)
+    nbytes = abi.fa_bwd_workspace_bytes_dt(B, H, N, d, abi.FA_BF16)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     gq, gk, gv = torch.empty_like(tq), torch.empty_like(tq), torch.empty_like(tq)
 

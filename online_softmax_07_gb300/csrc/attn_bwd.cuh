@@ -68,7 +68,7 @@ struct AttnBwdCfg {
 };
 
 // One-pass backward at d = 64 (the key-outer pass also forms dQ): each key-tile CTA
-// computes, per query tile i, the partial dQ_i += dS_ij K_j with a sixth tile product
+// computes, per query tile i, the partial dQ_i += dS_ij K_j with a fifth tile product
 // (dS staged in shared memory, queries contiguous) into TMEM, and the element-wise warps
 // add it into an fp32 dQ accumulator in the workspace by TMA reduce-adds (element-wise
 // fp32 adds at L2), each warp its 32 x 32 share, during the next query tile (by then the
