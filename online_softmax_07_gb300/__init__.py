@@ -214,9 +214,9 @@ def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, stream=N
     q, k, v, o, dout = (t.contiguous() for t in ts)
     lse = lse.contiguous()
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = abi.fa_bwd_workspace_bytes(B, H, N)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     dtype = abi.FA_BF16 if q.dtype == torch.bfloat16 else abi.FA_F16
+    ws_bytes = abi.fa_bwd_workspace_bytes_dt(B, H, N, d, dtype)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
         fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, int(bool(causal)), ws,
                ws_bytes, dtype)
