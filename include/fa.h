@@ -244,9 +244,9 @@ fa_status online_softmax_forward(const float* x, float* y, float* m_out, float* 
  *   lse                 [B, H, N] fp32, required
  *   dq, dk, dv          [B, H, N, d], dtype, written (fp32 accumulation inside)
  *   workspace           caller-owned device scratch of at least
- *                       fa_bwd_workspace_bytes_dt(B, H, N, d, dtype) bytes (fp32
- *                       LSE*log2(e) and D per query row; bf16/fp16 at d = 64 also the
- *                       fp32 dQ accumulator); its contents are overwritten
+ *                       fa_bwd_workspace_bytes_dt(B, H, N, d, dtype) bytes (per query
+ *                       row: fp32 statistics, or at d = 64 with bf16/fp16 their bf16
+ *                       terms and the fp32 dQ accumulator); its contents are overwritten
  * Alignment: bf16/fp16: every pointer but lse 16 bytes, lse 4; fp32: 4 bytes, the
  * workspace 16.  B*H*N == 0 is a no-op (FA_OK).
  * Determinism: dK and dV elements are each written once by one block.  dQ likewise at
@@ -267,14 +267,14 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  fa_dtype dtype, cudaStream_t stream);
 
 /* Workspace fa_bwd needs for this head dimension and dtype, in bytes, with
- * n_pad = ceil(N / 128) * 128: bf16/fp16 at d = 64: 264 * B * H * n_pad (8 bytes of row
- * statistics and a 64-float dQ accumulator row per padded query row); bf16/fp16 at
+ * n_pad = ceil(N / 128) * 128: bf16/fp16 at d = 64: 288 * B * H * n_pad (16 bf16 row
+ * statistics terms and a 64-float dQ accumulator row per padded query row); bf16/fp16 at
  * d = 128 and fp32 (1 <= d <= 128): 8 * B * H * n_pad.  0 for negative sizes, for a d or
  * dtype fa_bwd does not support, and for problems of more than INT_MAX 128-row tiles. */
 size_t fa_bwd_workspace_bytes_dt(int B, int H, int N, int d, fa_dtype dtype);
 
 /* A workspace size that serves every d and dtype of fa_bwd: the largest value of
- * fa_bwd_workspace_bytes_dt, 264 * B * H * n_pad (0 for negative sizes). */
+ * fa_bwd_workspace_bytes_dt, 288 * B * H * n_pad (0 for negative sizes). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N);
 
 /* Static, never-NULL description of a status code. */

@@ -19,9 +19,10 @@ namespace {
 
 long long bwd_n_pad(int N) { return (static_cast<long long>(N) + kBlockM - 1) / kBlockM * kBlockM; }
 
-// fp32 LSE * log2(e) and fp32 D per (head, padded query row); the tensor-core path at
-// d = 64 also keeps its fp32 dQ accumulator there (64 floats per padded row).  The fp32
-// path needs D for each real row (B * H * N floats), within the same 8 bytes a row.
+// Per (head, padded query row): the tensor-core path keeps fp32 LSE * log2(e) and D at
+// d = 128 (8 bytes), and at d = 64 its bf16 statistics terms and fp32 dQ accumulator
+// (32 + 256 bytes); the fp32 path needs D for each real row (B * H * N floats), within 8
+// bytes a row.
 // 0 for sizes fa_bwd rejects (more than INT_MAX tiles).
 long long bwd_ws_bytes(long long BH, int N, int d, fa_dtype dtype) {
   const long long n_pad = bwd_n_pad(N);
@@ -40,6 +41,20 @@ bool encode_dq_acc(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const 
   const cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides,
                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// TMA map of the d = 64 statistics terms: [BH, n_pad, 16] bf16 (32-byte rows), boxes of
+// 128 rows, 32-byte swizzle (the B operand layout of the statistics step).
+bool encode_aug(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, int BH,
+                int n_pad) {
+  const cuuint64_t dims[3] = {16, static_cast<cuuint64_t>(n_pad), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {16 * 2, static_cast<cuuint64_t>(n_pad) * 16 * 2};
+  const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(kBlockM), 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -136,7 +151,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (e != cudaSuccess) return FA_ERR_CUDA;
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if ((e = encode_fn(&enc)) != cudaSuccess) return FA_ERR_CUDA;
-  CUtensorMap tq, tk, tv, tdo, tacc;
+  CUtensorMap tq, tk, tv, tdo, tacc, taug;
   const int bh = static_cast<int>(BH);
   const bool f16 = dtype == FA_F16;
   if (!encode_bhnd(enc, &tq, q, bh, N, d, f16, kBlockM) ||
@@ -145,14 +160,17 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
       !encode_bhnd(enc, &tdo, dout, bh, N, d, f16, kBlockM))
     return FA_ERR_CUDA;
   const int n_pad = static_cast<int>(nblk * kBlockM);
-  // d = 64: the dQ accumulator follows LSE * log2(e) and D in the workspace.
-  if (d == 64 && !encode_dq_acc(enc, &tacc, static_cast<const float*>(workspace) + 2 * BH * n_pad,
-                                bh, n_pad))
+  // d = 64: the workspace holds the statistics terms (32 bytes per row), then the dQ
+  // accumulator (256 bytes per row).
+  if (d == 64 && (!encode_aug(enc, &taug, workspace, bh, n_pad) ||
+                  !encode_dq_acc(enc, &tacc, static_cast<const float*>(workspace) + 8 * BH * n_pad,
+                                 bh, n_pad)))
     return FA_ERR_CUDA;
-  if (d != 64) tacc = tq;  // not read at d = 128
+  if (d != 64) tacc = taug = tq;  // not read at d = 128
   AttnBwdParams p;
   p.lse2 = nullptr;  // set by the launcher from the workspace
   p.dd = nullptr;
+  p.aug = nullptr;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -176,11 +194,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   BwdFork* fk = nullptr;
   if ((e = fork_of_current_device(&fk)) != cudaSuccess) return FA_ERR_CUDA;
   if (d == 64)
-    e = f16 ? launch_attn_bwd<64, true>(tq, tk, tv, tdo, tacc, o, dout, lse, ws, p, stream, fk)
-            : launch_attn_bwd<64, false>(tq, tk, tv, tdo, tacc, o, dout, lse, ws, p, stream, fk);
+    e = f16 ? launch_attn_bwd<64, true>(tq, tk, tv, tdo, tacc, taug, o, dout, lse, ws, p, stream, fk)
+            : launch_attn_bwd<64, false>(tq, tk, tv, tdo, tacc, taug, o, dout, lse, ws, p, stream, fk);
   else
-    e = f16 ? launch_attn_bwd<128, true>(tq, tk, tv, tdo, tacc, o, dout, lse, ws, p, stream, fk)
-            : launch_attn_bwd<128, false>(tq, tk, tv, tdo, tacc, o, dout, lse, ws, p, stream, fk);
+    e = f16 ? launch_attn_bwd<128, true>(tq, tk, tv, tdo, tacc, taug, o, dout, lse, ws, p, stream, fk)
+            : launch_attn_bwd<128, false>(tq, tk, tv, tdo, tacc, taug, o, dout, lse, ws, p, stream, fk);
   return from_cuda(e);
 }
 

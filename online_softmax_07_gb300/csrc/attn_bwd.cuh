@@ -80,18 +80,34 @@ struct AttnBwdCfg {
 // deterministic.  Warp roles as in the two-pass kernels (a block of more than 384
 // threads would be compiled with 128 registers a thread, too few for the element-wise
 // warps).
+//
+// The row statistics enter through the tensor core instead of the element-wise warps:
+// every query row carries bf16 terms of -LSE/scale and of -D (a high and a low part each,
+// together exact to about 2^-18 of the value), and one more K = 16 step of S^T and of dP^T
+// multiplies them by a constant tile of ones, so that TMEM receives S^T - LSE/scale and
+// dP^T - D.  P = exp2(scale log2(e) (S - LSE/scale)) and dS = P (dP - D) then need no
+// per-query value in the element-wise warps (each would be the same 64 values loaded by
+// all 32 lanes of a warp).  The extra step is a bf16 product whatever the input type.
 
 struct AttnBwd1Cfg {
   static constexpr int kBoxes = 1;
   static constexpr int kTileBytes = kBoxBytes;  // 128 rows x 64, 16-bit
   static constexpr int kStages = 3;
-  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  // Statistics terms of a query tile: 128 rows x 16 bf16 (32 B, 32-byte swizzle):
+  // [-LSE/scale high, low, -D high, low, 0 ...].
+  static constexpr int kAugBytes = 128 * 32;
+  static constexpr int kStageBytes = 2 * kTileBytes + kAugBytes;  // Q_i, dO_i, terms
   static constexpr int kSmemFixed0 = 0;           // K_j
   static constexpr int kSmemFixed1 = kTileBytes;  // V_j
   static constexpr int kSmemStages = 2 * kTileBytes;
+  // The constant A operands of the statistics step, 128 rows x 16 bf16 each (32-byte
+  // swizzle): rows [1, 1, 0, 0, 0, 0, 0, 0] (picks -LSE/scale) and [0, 0, 1, 1, 0, ...]
+  // (picks -D), the same 8-element pattern in both 16-byte halves of a row, so that the
+  // swizzle cannot move a one onto a term of the other statistic.
+  static constexpr int kSmemOnes = kSmemStages + kStages * kStageBytes;
   // dS of the current tile pair, [key][query]: two 64-query boxes of 128 keys x 128 B,
   // 128-byte swizzle (the MN-major A operand of dS K_j).
-  static constexpr int kSmemDS = kSmemStages + kStages * kStageBytes;
+  static constexpr int kSmemDS = kSmemOnes + 2 * kAugBytes;
   // dQ staging: per element-wise warp one box of 32 rows x 32 fp32 (4 KB).
   static constexpr int kRedBoxBytes = 32 * 128;
   static constexpr int kSmemRed = kSmemDS + 2 * kTileBytes;
@@ -106,9 +122,10 @@ struct AttnBwd1Cfg {
 };
 
 struct AttnBwdParams {
-  const float* lse2;   // [BH, n_pad]: LSE * log2(e), +inf for rows >= N
-  const float* dd;     // [BH, n_pad]: D = rowsum(dO * O), 0 for rows >= N
-  float* dq_acc;       // one-pass backward: [BH, n_pad, 64] fp32 dQ / scale accumulator
+  const float* lse2;   // two passes: [BH, n_pad]: LSE * log2(e), +inf for rows >= N
+  const float* dd;     // two passes: [BH, n_pad]: D = rowsum(dO * O), 0 for rows >= N
+  uint16_t* aug;       // one pass: [BH, n_pad, 16] bf16 statistics terms, 0 for rows >= N
+  float* dq_acc;       // one pass: [BH, n_pad, 64] fp32 dQ / scale accumulator
   void* dq;            // [BH, N, d] outputs, 16-bit
   void* dk;
   void* dv;
@@ -132,17 +149,20 @@ struct BwdFork {
   cudaEvent_t fork, join;
 };
 
-// Workspace bytes of the tensor-core backward: fp32 LSE * log2(e) and D per padded query
-// row, and at d = 64 the fp32 dQ accumulator (64 floats per padded row) after them.
+// Workspace of the tensor-core backward, per padded query row: at d = 128 fp32
+// LSE * log2(e) and D (8 bytes); at d = 64 the 16 bf16 statistics terms (32 bytes) and
+// then, after those of every row, the fp32 dQ accumulator row (256 bytes).
 inline long long bwd_tc_ws_bytes(long long BH, long long n_pad, int d) {
-  return BH * n_pad * (2 * 4 + (d == 64 ? 64 * 4 : 0));
+  return BH * n_pad * (d == 64 ? 32 + 64 * 4 : 2 * 4);
 }
 
-// tdq_acc: at d = 64 a TMA map of the dQ accumulator ([BH, n_pad, 64] fp32, boxes of
-// 32 x 32, 128-byte swizzle); unused at d = 128.
+// tdq_acc, taug: at d = 64 TMA maps of the dQ accumulator ([BH, n_pad, 64] fp32, boxes of
+// 32 x 32, 128-byte swizzle) and of the statistics terms ([BH, n_pad, 16] bf16, boxes of
+// 128 rows, 32-byte swizzle); unused at d = 128.
 template <int D, bool F16>
 cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const void* o,
+                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc,
+                            const CUtensorMap& taug, const void* o,
                             const void* dout, const float* lse, float* ws, const AttnBwdParams& p,
                             cudaStream_t stream, const BwdFork* fork);
 

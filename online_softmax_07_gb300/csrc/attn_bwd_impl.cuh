@@ -66,6 +66,20 @@ __device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, volatile
   return done != 0 || mbar_wait(bar, parity, abort, status);
 }
 
+// Shared-memory matrix descriptor of a K-major operand with 32-byte swizzle (rows of 16
+// 16-bit elements; 8-row groups 256 bytes apart): swizzle mode 6 at bits 61-63.
+__device__ __forceinline__ uint64_t desc_sw32(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(256 >> 4) << 32) | (1ull << 46) | (6ull << 61);
+}
+
+// x as the sum of two bf16 values (high in bits 0..15, low in 16..31): the high part is x
+// rounded, the low part the rounded remainder, together within about 2^-18 |x|.
+__device__ __forceinline__ uint32_t bf16_hi_lo(float x) {
+  const uint32_t hi = pack_bf16x2(x, 0.f) & 0xFFFFu;
+  return pack_bf16x2(x, x - __uint_as_float(hi << 16));
+}
+
 // Instruction-descriptor bit 15 (kind::f16): the A operand is MN-major in shared memory.
 constexpr uint32_t kIdescAMnMajor = 1u << 15;
 
@@ -144,7 +158,9 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __re
                                                             const float* __restrict__ lse,
                                                             float* __restrict__ lse2,
                                                             float* __restrict__ dd, int BH, int N,
-                                                            int n_pad, float* __restrict__ dq_acc) {
+                                                            int n_pad, float* __restrict__ dq_acc,
+                                                            uint16_t* __restrict__ aug,
+                                                            float inv_scale) {
   constexpr int kPer = D / 32;  // 16-bit elements per lane and row: 2 or 4
   const long long total = static_cast<long long>(BH) * n_pad;
   const long long row0 =
@@ -208,8 +224,19 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __re
     if (row < total) {
       const long long bh = row / n_pad;
       const int q = static_cast<int>(row - bh * n_pad);
-      dd[row] = q < N ? mine : 0.f;
-      lse2[row] = q < N ? lse[bh * N + q] * 1.4426950408889634f : INFINITY;
+      if (aug != nullptr) {
+        // One pass: the row's statistics terms [-LSE/scale high, low, -D high, low, 0 ...]
+        // (all 0 for rows >= N: those queries have zero dO and dP rows, so whatever P
+        // they get adds nothing).
+        const float c = q < N ? -lse[bh * N + q] * inv_scale : 0.f;
+        const float nd = q < N ? -mine : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(aug + row * 16);
+        dst[0] = make_uint4(bf16_hi_lo(c), bf16_hi_lo(nd), 0u, 0u);
+        dst[1] = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        dd[row] = q < N ? mine : 0.f;
+        lse2[row] = q < N ? lse[bh * N + q] * 1.4426950408889634f : INFINITY;
+      }
     }
   }
 }
@@ -235,7 +262,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do,
-                         const __grid_constant__ CUtensorMap tm_dqacc, const AttnBwdParams p) {
+                         const __grid_constant__ CUtensorMap tm_dqacc,
+                         const __grid_constant__ CUtensorMap tm_aug, const AttnBwdParams p) {
   static_assert(!Fused || D == 64, "the one-pass backward is for d = 64");
   using Cfg = std::conditional_t<Fused, AttnBwd1Cfg, AttnBwdCfg<D>>;
   extern __shared__ uint8_t smem_raw[];
@@ -271,6 +299,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(smem_u32(&bars->tmem_base), Cfg::kTmemCols);
     tmem_relinquish();
   }
+  if constexpr (Fused) {
+    // The two constant A tiles of the statistics step (2 x 256 16-byte chunks): in every
+    // row [1, 1, 0, ...] (bf16) then [0, 0, 1, 1, 0, ...], repeated in both halves.
+    constexpr uint32_t kOne2 = 0x3F803F80u;  // two bf16 ones
+    uint4* ones = reinterpret_cast<uint4*>(smem + Cfg::kSmemOnes);
+    for (int c = threadIdx.x; c < 2 * Cfg::kAugBytes / 16; c += kBwdThreads)
+      ones[c] = c < Cfg::kAugBytes / 16 ? make_uint4(kOne2, 0u, 0u, 0u) : make_uint4(0u, kOne2, 0u, 0u);
+    fence_proxy_async_smem();  // read by the tensor pipe
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -303,15 +340,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t full = smem_u32(&bars->stage_full[s]);
         const int i = i0 + it;
         const uint32_t dst = stage_addr(s);
-        mbar_arrive_expect_tx(full, 2 * Cfg::kTileBytes + 1024);
+        mbar_arrive_expect_tx(full, Cfg::kStageBytes);
 #pragma unroll
         for (int b = 0; b < Cfg::kBoxes; ++b) {
           tma_load_3d(dst + b * kBoxBytes, &tm_q, full, b * kBoxCols, i * kBlockM, bh);
           tma_load_3d(dst + Cfg::kTileBytes + b * kBoxBytes, &tm_do, full, b * kBoxCols, i * kBlockM, bh);
         }
-        const long long srow = static_cast<long long>(bh) * p.n_pad + i * kBlockM;
-        bulk_load_1d(dst + 2 * Cfg::kTileBytes, p.lse2 + srow, 512, full);
-        bulk_load_1d(dst + 2 * Cfg::kTileBytes + 512, p.dd + srow, 512, full);
+        if constexpr (Fused) {
+          tma_load_3d(dst + 2 * Cfg::kTileBytes, &tm_aug, full, 0, i * kBlockM, bh);
+        } else {
+          const long long srow = static_cast<long long>(bh) * p.n_pad + i * kBlockM;
+          bulk_load_1d(dst + 2 * Cfg::kTileBytes, p.lse2 + srow, 512, full);
+          bulk_load_1d(dst + 2 * Cfg::kTileBytes + 512, p.dd + srow, 512, full);
+        }
         issued = it + 1;
       }
       // Every issued copy must land before the block's shared memory goes away.
@@ -382,7 +423,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t kIdescDQ = idesc_f16kind(kBlockM, D, true, F16) | kIdescAMnMajor;
       const uint64_t dDS = desc_sw128(sbase + Cfg::kSmemDS, kBoxBytes, 1024);
       const uint64_t dKmn = desc_sw128(sbase + Cfg::kSmemFixed0, kBoxBytes, 1024);
-      auto group_t = [&](uint32_t tD, uint64_t dA, uint64_t dB) {  // S^T or dP^T, K = 64
+      // S^T (or dP^T), K = 64, then the statistics step: the constant ones tile `dOnes`
+      // (A) times the query tile's terms (B, in stage `st`) adds -LSE/scale (or -D) to
+      // every column; a bf16 product, whatever the element type of the others.
+      constexpr uint32_t kIdescAug = idesc_f16kind(kBlockM, kBlockM, false, false);
+      const uint64_t dOnesS = desc_sw32(sbase + Cfg::kSmemOnes);
+      const uint64_t dOnesD = desc_sw32(sbase + Cfg::kSmemOnes + Cfg::kAugBytes);
+      auto group_t = [&](uint32_t tD, uint64_t dA, uint64_t dB, uint64_t dOnes, int st) {
         uint64_t a[4], b[4];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -390,6 +437,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           b[kk] = dB + 2 * kk;
         }
         mma_ss4_elect(tD, a, b, kIdescS, 0u);
+        mma_bf16_ss_elect(tD, dOnes, desc_sw32(stage_addr(st % Cfg::kStages) + 2 * Cfg::kTileBytes),
+                          kIdescAug, 1u);
       };
       // dV or dK: A = 16 queries (8 packed columns) per step, the 64-query halves `half`
       // columns apart.
@@ -405,9 +454,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       const uint32_t tP = tbase + Cfg::kColP, tDQ = tbase + Cfg::kColDQ;
       if (ok) {
-        group_t(tS, dK, desc_k(0, 0));
+        group_t(tS, dK, desc_k(0, 0), dOnesS, 0);
         mma_commit_elect(smem_u32(&bars->s_full));
-        group_t(tDP, dV, desc_k(0, 1));
+        group_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
         mma_commit_elect(smem_u32(&bars->dp_full));
       }
       for (int it = 0; ok && it < nq; ++it) {
@@ -417,7 +466,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                               ((it + 1) / Cfg::kStages) & 1) &&
                      wait_bar(&bars->s_free, it & 1)))
             break;
-          group_t(tS, dK, desc_k(it + 1, 0));
+          group_t(tS, dK, desc_k(it + 1, 0), dOnesS, it + 1);
           mma_commit_elect(smem_u32(&bars->s_full));
         }
         if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
@@ -435,7 +484,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss8_elect(tDQ, a, b, kIdescDQ, 0u);
         }
         if (more) {
-          group_t(tDP, dV, desc_k(it + 1, 1));
+          group_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
           mma_commit_elect(smem_u32(&bars->dp_full));
         }
       }
@@ -552,23 +601,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     };
-    // The statistics of query tile it come in by TMA with its stage; the warps wait on the
-    // stage's own barrier to see them, for tile it+1 at the end of tile it (off the path
-    // from S^T to P^T; the stage is refilled only after these warps are done with it).
-    ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->stage_full[0]), 0, abort, p.status));
     if constexpr (Fused) {
-      // One pass (d = 64), per query tile it: S^T into registers, "S^T free" (the next S^T
-      // may overwrite it), P; then, once dP^T(it) is in (which also reports dV, dK and dQ
-      // of tile it - 1 complete), P^T into its own columns, p_done, the dQ partial of tile
-      // it - 1 drained, dS^T over dP^T and dS into the shared-memory staging, ds_ready.
+      // One pass (d = 64), per query tile it: S^T - LSE/scale into registers, "S^T free"
+      // (the next S^T may overwrite it), P; then, once dP^T(it) - D is in (which also
+      // reports dV, dK and dQ of tile it - 1 complete), P^T into its own columns, p_done,
+      // the dQ partial of tile it - 1 drained, dS^T over dP^T and dS into the shared-memory
+      // staging, ds_ready.  The statistics came in through the tensor core, so these warps
+      // read nothing from the stages.
       const uint32_t tP = tbase + lane_off + Cfg::kColP;
+      // P^T of 32 queries from S^T - LSE/scale: exp2(scale log2 e (S^T - LSE/scale)).
+      auto p_chunk1 = [&](const uint32_t* sr, int c0, bool diag, uint64_t* pv, uint32_t* pk) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float x0, x1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2),
+                    x0, x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (diag) {
+            if (c0 + c < r) p0 = 0.f;
+            if (c0 + c + 1 < r) p1 = 0.f;
+          }
+          pv[c >> 1] = f2_pack(p0, p1);
+          pk[c >> 1] = pack_elem2<F16>(p0, p1);
+        }
+      };
+      // dS^T = P^T * (dP^T - D) of 32 queries, packed to 16 bits.
+      auto ds_chunk1 = [&](const uint32_t* dr, const uint64_t* pv, uint32_t* pd) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float d0, d1;
+          f2_unpack(f2_mul(pv[c >> 1], f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1]))),
+                    d0, d1);
+          pd[c >> 1] = pack_elem2<F16>(d0, d1);
+        }
+      };
       for (int it = 0; ok && it < nq; ++it) {
         ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
         if (!ok) break;
         tc_fence_after();
-        const float* lse2s = reinterpret_cast<const float*>(
-            smem + Cfg::kSmemStages + (it % Cfg::kStages) * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
-        const float* dds = lse2s + 128;
         const bool diag = p.causal && i0 + it == j;
         uint64_t pv[32];
         uint32_t pk[32];
@@ -581,7 +651,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
           }
-          p_chunk(sr, lse2s, 64 * h + 32 * ch, diag, pv + 16 * ch, pk + 16 * ch);
+          p_chunk1(sr, 64 * h + 32 * ch, diag, pv + 16 * ch, pk + 16 * ch);
         }
         ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
         if (!ok) break;
@@ -599,7 +669,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int c0 = 64 * h + 32 * ch;
           uint32_t dr[32], pd[16];
           tmem_ld32_wait(tDP + c0, dr);
-          ds_chunk(dr, dds, c0, pv + 16 * ch, pd);
+          ds_chunk1(dr, pv + 16 * ch, pd);
           tmem_st16(tDP + 64 * h + 16 * ch, pd);
           // Row r (this key) of box h: queries 64h + 32ch .. +31 are its 16-byte chunks
           // 4ch .. 4ch+3, each at its 128-byte-swizzle position (chunk ^ (r % 8)).
@@ -614,12 +684,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
-        if (it + 1 < nq)
-          ok = __all_sync(0xffffffffu,
-                          bwd_wait(smem_u32(&bars->stage_full[(it + 1) % Cfg::kStages]),
-                                    ((it + 1) / Cfg::kStages) & 1, abort, p.status));
       }
     } else {
+    // The statistics of query tile it come in by TMA with its stage; the warps wait on the
+    // stage's own barrier to see them, for tile it+1 at the end of tile it (off the path
+    // from S^T to P^T; the stage is refilled only after these warps are done with it).
+    ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->stage_full[0]), 0, abort, p.status));
     for (int it = 0; ok && it < nq; ++it) {
       ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
       if (!ok) break;
@@ -1002,23 +1072,26 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_finalize_kernel(const float* 
 
 template <int D, bool F16>
 cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const void* o,
-                            const void* dout, const float* lse, float* ws,
-                            const AttnBwdParams& p0, cudaStream_t stream, const BwdFork* fork) {
+                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc,
+                            const CUtensorMap& taug, const void* o, const void* dout,
+                            const float* lse, float* ws, const AttnBwdParams& p0,
+                            cudaStream_t stream, const BwdFork* fork) {
   static_assert(D == 64 || D == 128, "head dimension");
   static_assert(sizeof(AttnBwdBarriers) <= 512, "barrier block");
   constexpr bool kFused = (D == 64);
   AttnBwdParams p = p0;
   const long long rows = static_cast<long long>(p.BH) * p.n_pad;
-  float* lse2 = ws;
-  float* dd = ws + rows;
-  p.lse2 = lse2;
-  p.dd = dd;
-  p.dq_acc = kFused ? ws + 2 * rows : nullptr;
+  // Workspace: d = 128 LSE * log2(e) and D per row; d = 64 the statistics terms (16 bf16
+  // per row) and then the dQ accumulator (64 fp32 per row).
+  p.lse2 = kFused ? nullptr : ws;
+  p.dd = kFused ? nullptr : ws + rows;
+  p.aug = kFused ? reinterpret_cast<uint16_t*>(ws) : nullptr;
+  p.dq_acc = kFused ? ws + 8 * rows : nullptr;
   attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((rows + 8 * kPrepRows - 1) / (8 * kPrepRows)),
                                  256, 0, stream>>>(
-      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dd, p.BH,
-      p.N, p.n_pad, p.dq_acc);
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
+      const_cast<float*>(p.lse2), const_cast<float*>(p.dd), p.BH, p.N, p.n_pad, p.dq_acc, p.aug,
+      1.0f / p.scale);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.BH) * p.nblk);
@@ -1031,7 +1104,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
         cudaSuccess)
       return e;
     attn_bwd_dkdv_kernel<D, F16, true><<<grid, kBwdThreads, C1::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, tdq_acc, p);
+        tq, tk, tv, tdo, tdq_acc, taug, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long long out_rows = static_cast<long long>(p.BH) * p.N;
     const long long fin_blocks = std::min<long long>((out_rows * 8 + 255) / 256, 1LL << 20);
@@ -1054,7 +1127,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
     // The fork point is the prep's completion, recorded before the key-outer launch.
     if (fork != nullptr && (e = cudaEventRecord(fork->fork, stream)) != cudaSuccess) return e;
     attn_bwd_dkdv_kernel<D, F16, false><<<grid, kBwdThreads, Cfg::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, tdq_acc, p);
+        tq, tk, tv, tdo, tdq_acc, taug, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (fork == nullptr) {
       attn_bwd_dq_kernel<D, F16><<<grid, kBwdThreads, Cfg::kDqSmemBytes, stream>>>(tq, tk, tv,

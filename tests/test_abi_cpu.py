@@ -210,13 +210,13 @@ def test_splitkv_rejects_f32(lib):
 
 
 def test_bwd_workspace_size(lib):
-    # Per (head, query row), rows padded to a multiple of 128: 2 fp32 statistics, and for
-    # bf16/fp16 at d = 64 a 64-float dQ accumulator row.
+    # Per (head, query row), rows padded to a multiple of 128: 2 fp32 statistics, or for
+    # bf16/fp16 at d = 64 16 bf16 statistics terms and a 64-float dQ accumulator row.
     dt = abi.fa_bwd_workspace_bytes_dt
     assert dt(2, 3, 300, 128, abi.FA_BF16) == 2 * 6 * 384 * 4
     assert dt(2, 3, 300, 128, abi.FA_F16) == 2 * 6 * 384 * 4
-    assert dt(2, 3, 300, 64, abi.FA_BF16) == (2 + 64) * 6 * 384 * 4
-    assert dt(1, 1, 128, 64, abi.FA_F16) == (2 + 64) * 128 * 4
+    assert dt(2, 3, 300, 64, abi.FA_BF16) == (16 * 2 + 64 * 4) * 6 * 384
+    assert dt(1, 1, 128, 64, abi.FA_F16) == (16 * 2 + 64 * 4) * 128
     assert dt(1, 1, 128, 64, abi.FA_F32) == 2 * 128 * 4
     assert dt(1, 1, 100, 17, abi.FA_F32) == 2 * 128 * 4
     assert dt(1, 1, 100, 96, abi.FA_BF16) == 0       # unsupported d
@@ -225,8 +225,8 @@ def test_bwd_workspace_size(lib):
     assert dt(-1, 1, 100, 64, abi.FA_BF16) == 0
     assert dt(0, 4, 100, 64, abi.FA_BF16) == 0
     # The dtype-free size serves every case: the d = 64 one.
-    assert abi.fa_bwd_workspace_bytes(2, 3, 300) == (2 + 64) * 6 * 384 * 4
-    assert abi.fa_bwd_workspace_bytes(1, 1, 128) == (2 + 64) * 128 * 4
+    assert abi.fa_bwd_workspace_bytes(2, 3, 300) == (16 * 2 + 64 * 4) * 6 * 384
+    assert abi.fa_bwd_workspace_bytes(1, 1, 128) == (16 * 2 + 64 * 4) * 128
     assert abi.fa_bwd_workspace_bytes(0, 4, 100) == 0
     assert abi.fa_bwd_workspace_bytes(-1, 4, 100) == 0
 
