@@ -269,7 +269,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 /* Workspace fa_bwd needs for this head dimension and dtype, in bytes, with
  * n_pad = ceil(N / 128) * 128: bf16/fp16 at d = 64: 288 * B * H * n_pad (16 bf16 row
  * statistics terms and a 64-float dQ accumulator row per padded query row); bf16/fp16 at
- * d = 128 and fp32 (1 <= d <= 128): 8 * B * H * n_pad.  0 for negative sizes, for a d or
+ * d = 128: 40 * B * H * n_pad (two fp32 statistics and the 16 bf16 terms per row); fp32
+ * (1 <= d <= 128): 8 * B * H * n_pad.  0 for negative sizes, for a d or
  * dtype fa_bwd does not support, and for problems of more than INT_MAX 128-row tiles. */
 size_t fa_bwd_workspace_bytes_dt(int B, int H, int N, int d, fa_dtype dtype);
 

@@ -160,13 +160,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
       !encode_bhnd(enc, &tdo, dout, bh, N, d, f16, kBlockM))
     return FA_ERR_CUDA;
   const int n_pad = static_cast<int>(nblk * kBlockM);
-  // d = 64: the workspace holds the statistics terms (32 bytes per row), then the dQ
-  // accumulator (256 bytes per row).
-  if (d == 64 && (!encode_aug(enc, &taug, workspace, bh, n_pad) ||
-                  !encode_dq_acc(enc, &tacc, static_cast<const float*>(workspace) + 8 * BH * n_pad,
-                                 bh, n_pad)))
+  // The workspace holds the statistics terms (32 bytes per row): at d = 64 first, followed
+  // by the dQ accumulator (256 bytes per row); at d = 128 after LSE * log2(e) and D.
+  const float* ws_f = static_cast<const float*>(workspace);
+  if (!encode_aug(enc, &taug, d == 64 ? ws_f : ws_f + 2 * BH * n_pad, bh, n_pad))
     return FA_ERR_CUDA;
-  if (d != 64) tacc = taug = tq;  // not read at d = 128
+  if (d == 64 && !encode_dq_acc(enc, &tacc, ws_f + 8 * BH * n_pad, bh, n_pad)) return FA_ERR_CUDA;
+  if (d != 64) tacc = tq;  // not read at d = 128
   AttnBwdParams p;
   p.lse2 = nullptr;  // set by the launcher from the workspace
   p.dd = nullptr;

@@ -45,13 +45,15 @@ struct AttnBwdCfg {
   static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D, 16-bit
   static constexpr int kStages = 2;                       // streamed tile pairs in flight
-  // A stage holds two streamed tiles and, for the key-outer pass, 128 LSE*log2(e)
-  // and 128 D values of the query tile (1 KB).
-  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  // A key-outer stage holds Q_i, dO_i and the query tile's statistics terms (128 rows x
+  // 16 bf16, 32-byte swizzle), as in the one-pass kernel (AttnBwd1Cfg).
+  static constexpr int kAugBytes = 128 * 32;
+  static constexpr int kStageBytes = 2 * kTileBytes + kAugBytes;
   static constexpr int kSmemFixed0 = 0;           // resident tile 0 (K_j or Q_i)
   static constexpr int kSmemFixed1 = kTileBytes;  // resident tile 1 (V_j or dO_i)
   static constexpr int kSmemStages = 2 * kTileBytes;
-  static constexpr int kSmemBars = kSmemStages + kStages * kStageBytes;
+  static constexpr int kSmemOnes = kSmemStages + kStages * kStageBytes;  // 2 x 4 KB
+  static constexpr int kSmemBars = kSmemOnes + 2 * kAugBytes;
   static constexpr int kSmemBytes = kSmemBars + 512 + 1024;  // + barriers + alignment slack
   // TMEM columns: S (or S^T), dP (or dP^T), then one or two fp32 accumulators: all 512.
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
@@ -122,9 +124,9 @@ struct AttnBwd1Cfg {
 };
 
 struct AttnBwdParams {
-  const float* lse2;   // two passes: [BH, n_pad]: LSE * log2(e), +inf for rows >= N
-  const float* dd;     // two passes: [BH, n_pad]: D = rowsum(dO * O), 0 for rows >= N
-  uint16_t* aug;       // one pass: [BH, n_pad, 16] bf16 statistics terms, 0 for rows >= N
+  const float* lse2;   // query-outer pass: [BH, n_pad]: LSE * log2(e), +inf for rows >= N
+  const float* dd;     // query-outer pass: [BH, n_pad]: D = rowsum(dO * O), 0 for rows >= N
+  uint16_t* aug;       // key-outer passes: [BH, n_pad, 16] bf16 statistics terms, 0 for rows >= N
   float* dq_acc;       // one pass: [BH, n_pad, 64] fp32 dQ / scale accumulator
   void* dq;            // [BH, N, d] outputs, 16-bit
   void* dk;
@@ -150,15 +152,16 @@ struct BwdFork {
 };
 
 // Workspace of the tensor-core backward, per padded query row: at d = 128 fp32
-// LSE * log2(e) and D (8 bytes); at d = 64 the 16 bf16 statistics terms (32 bytes) and
-// then, after those of every row, the fp32 dQ accumulator row (256 bytes).
+// LSE * log2(e) and D (8 bytes, for the query-outer pass) and then the 16 bf16 statistics
+// terms (32 bytes, for the key-outer pass); at d = 64 the terms (32 bytes) and then the
+// fp32 dQ accumulator row (256 bytes).  Each part covers all rows before the next.
 inline long long bwd_tc_ws_bytes(long long BH, long long n_pad, int d) {
-  return BH * n_pad * (d == 64 ? 32 + 64 * 4 : 2 * 4);
+  return BH * n_pad * (d == 64 ? 32 + 64 * 4 : 2 * 4 + 32);
 }
 
-// tdq_acc, taug: at d = 64 TMA maps of the dQ accumulator ([BH, n_pad, 64] fp32, boxes of
-// 32 x 32, 128-byte swizzle) and of the statistics terms ([BH, n_pad, 16] bf16, boxes of
-// 128 rows, 32-byte swizzle); unused at d = 128.
+// tdq_acc: at d = 64 a TMA map of the dQ accumulator ([BH, n_pad, 64] fp32, boxes of
+// 32 x 32, 128-byte swizzle; unused at d = 128); taug: a TMA map of the statistics terms
+// ([BH, n_pad, 16] bf16, boxes of 128 rows, 32-byte swizzle).
 template <int D, bool F16>
 cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq_acc,

@@ -29,16 +29,6 @@ struct AttnBwdBarriers {
   int abort;
 };
 
-// 1-D bulk copy global -> shared memory, completion counted on `bar` (both addresses
-// 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
-                                             uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // Element-wise add of a shared-memory box into the global tensor of `tmap` (fp32 adds,
 // done at L2); completion tracked like a TMA store, by bulk groups.
 __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int x, int y,
@@ -224,16 +214,15 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __re
     if (row < total) {
       const long long bh = row / n_pad;
       const int q = static_cast<int>(row - bh * n_pad);
-      if (aug != nullptr) {
-        // One pass: the row's statistics terms [-LSE/scale high, low, -D high, low, 0 ...]
-        // (all 0 for rows >= N: those queries have zero dO and dP rows, so whatever P
-        // they get adds nothing).
-        const float c = q < N ? -lse[bh * N + q] * inv_scale : 0.f;
-        const float nd = q < N ? -mine : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(aug + row * 16);
-        dst[0] = make_uint4(bf16_hi_lo(c), bf16_hi_lo(nd), 0u, 0u);
-        dst[1] = make_uint4(0u, 0u, 0u, 0u);
-      } else {
+      // The key-outer kernels' statistics terms [-LSE/scale high, low, -D high, low, 0 ...]
+      // (all 0 for rows >= N: those queries have zero dO and dP rows, so whatever P they
+      // get adds nothing), and for the query-outer pass LSE * log2(e) and D.
+      const float c = q < N ? -lse[bh * N + q] * inv_scale : 0.f;
+      const float nd = q < N ? -mine : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(aug + row * 16);
+      dst[0] = make_uint4(bf16_hi_lo(c), bf16_hi_lo(nd), 0u, 0u);
+      dst[1] = make_uint4(0u, 0u, 0u, 0u);
+      if (lse2 != nullptr) {
         dd[row] = q < N ? mine : 0.f;
         lse2[row] = q < N ? lse[bh * N + q] * 1.4426950408889634f : INFINITY;
       }
@@ -299,7 +288,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(smem_u32(&bars->tmem_base), Cfg::kTmemCols);
     tmem_relinquish();
   }
-  if constexpr (Fused) {
+  {
     // The two constant A tiles of the statistics step (2 x 256 16-byte chunks): in every
     // row [1, 1, 0, ...] (bf16) then [0, 0, 1, 1, 0, ...], repeated in both halves.
     constexpr uint32_t kOne2 = 0x3F803F80u;  // two bf16 ones
@@ -346,13 +335,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(dst + b * kBoxBytes, &tm_q, full, b * kBoxCols, i * kBlockM, bh);
           tma_load_3d(dst + Cfg::kTileBytes + b * kBoxBytes, &tm_do, full, b * kBoxCols, i * kBlockM, bh);
         }
-        if constexpr (Fused) {
-          tma_load_3d(dst + 2 * Cfg::kTileBytes, &tm_aug, full, 0, i * kBlockM, bh);
-        } else {
-          const long long srow = static_cast<long long>(bh) * p.n_pad + i * kBlockM;
-          bulk_load_1d(dst + 2 * Cfg::kTileBytes, p.lse2 + srow, 512, full);
-          bulk_load_1d(dst + 2 * Cfg::kTileBytes + 512, p.dd + srow, 512, full);
-        }
+        tma_load_3d(dst + 2 * Cfg::kTileBytes, &tm_aug, full, 0, i * kBlockM, bh);
         issued = it + 1;
       }
       // Every issued copy must land before the block's shared memory goes away.
@@ -381,14 +364,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto desc_mn = [&](int it, int tile) {  // MN-major view of a streamed tile
       return desc_sw128(stage_addr(it % Cfg::kStages) + tile * Cfg::kTileBytes, kBoxBytes, 1024);
     };
-    // S^T = K_j Q_i^T into tS, or dP^T = V_j dO_i^T into tDP: keys on lanes, queries on
-    // columns; the streamed tile is the K-major B operand.
-    auto issue_t = [&](uint32_t tD, uint64_t dA, uint64_t dB) {
+    // The statistics step: the constant ones tile `dOnes` (A) times the query tile's terms
+    // (B, in stage st) adds -LSE/scale (dOnesS) or -D (dOnesD) to every column; a bf16
+    // product, whatever the element type of the others.
+    constexpr uint32_t kIdescAug = idesc_f16kind(kBlockM, kBlockM, false, false);
+    const uint64_t dOnesS = desc_sw32(sbase + Cfg::kSmemOnes);
+    const uint64_t dOnesD = desc_sw32(sbase + Cfg::kSmemOnes + Cfg::kAugBytes);
+    auto issue_aug = [&](uint32_t tD, uint64_t dOnes, int st) {
+      mma_bf16_ss_elect(tD, dOnes, desc_sw32(stage_addr(st % Cfg::kStages) + 2 * Cfg::kTileBytes),
+                        kIdescAug, 1u);
+    };
+    // S^T - LSE/scale = K_j Q_i^T + (stats) into tS, or dP^T - D = V_j dO_i^T + (stats) into
+    // tDP: keys on lanes, queries on columns; the streamed tile is the K-major B operand.
+    auto issue_t = [&](uint32_t tD, uint64_t dA, uint64_t dB, uint64_t dOnes, int st) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
         mma_bf16_ss_elect(tD, dA + off16, dB + off16, kIdescS, kk > 0 ? 1u : 0u);
       }
+      issue_aug(tD, dOnes, st);
     };
     // tAcc += A^T-part from TMEM (16 queries = 8 packed columns per step; column half h
     // of the tile was packed into columns 64h .. 64h+31) times a streamed MN-major tile.
@@ -423,12 +417,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t kIdescDQ = idesc_f16kind(kBlockM, D, true, F16) | kIdescAMnMajor;
       const uint64_t dDS = desc_sw128(sbase + Cfg::kSmemDS, kBoxBytes, 1024);
       const uint64_t dKmn = desc_sw128(sbase + Cfg::kSmemFixed0, kBoxBytes, 1024);
-      // S^T (or dP^T), K = 64, then the statistics step: the constant ones tile `dOnes`
-      // (A) times the query tile's terms (B, in stage `st`) adds -LSE/scale (or -D) to
-      // every column; a bf16 product, whatever the element type of the others.
-      constexpr uint32_t kIdescAug = idesc_f16kind(kBlockM, kBlockM, false, false);
-      const uint64_t dOnesS = desc_sw32(sbase + Cfg::kSmemOnes);
-      const uint64_t dOnesD = desc_sw32(sbase + Cfg::kSmemOnes + Cfg::kAugBytes);
+      // S^T (or dP^T), K = 64 under one elect, then the statistics step.
       auto group_t = [&](uint32_t tD, uint64_t dA, uint64_t dB, uint64_t dOnes, int st) {
         uint64_t a[4], b[4];
 #pragma unroll
@@ -437,8 +426,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           b[kk] = dB + 2 * kk;
         }
         mma_ss4_elect(tD, a, b, kIdescS, 0u);
-        mma_bf16_ss_elect(tD, dOnes, desc_sw32(stage_addr(st % Cfg::kStages) + 2 * Cfg::kTileBytes),
-                          kIdescAug, 1u);
+        issue_aug(tD, dOnes, st);
       };
       // dV or dK: A = 16 queries (8 packed columns) per step, the 64-query halves `half`
       // columns apart.
@@ -490,9 +478,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     } else {
     if (ok) {
-      issue_t(tS, dK, desc_k(0, 0));
+      issue_t(tS, dK, desc_k(0, 0), dOnesS, 0);
       mma_commit_elect(smem_u32(&bars->s_full));
-      issue_t(tDP, dV, desc_k(0, 1));
+      issue_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
       mma_commit_elect(smem_u32(&bars->dp_full));
     }
     for (int it = 0; ok && it < nq; ++it) {
@@ -503,14 +491,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
                             ((it + 1) / Cfg::kStages) & 1)))
           break;
-        issue_t(tS, dK, desc_k(it + 1, 0));
+        issue_t(tS, dK, desc_k(it + 1, 0), dOnesS, it + 1);
         mma_commit_elect(smem_u32(&bars->s_full));
       }
       if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
       issue_acc(tDK, tDP, desc_mn(it, 0), it > 0);
       mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
       if (more) {
-        issue_t(tDP, dV, desc_k(it + 1, 1));
+        issue_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
         mma_commit_elect(smem_u32(&bars->dp_full));
       }
     }
@@ -530,51 +518,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    // P^T of 32 queries (columns c0 .. c0+31 of this key's row) from S^T:
-    // exp2(S^T * scale * log2 e - LSE * log2 e), kept in fp32 pairs (pv, for dS^T) and
-    // packed to 16 bits (pk, the A operand of dV); causal diagonal tile: query q sees key r
-    // iff r <= q.
-    auto p_chunk = [&](const uint32_t* sr, const float* lse2s, int c0, bool diag, uint64_t* pv,
-                       uint32_t* pk) {
-      const float4* l4 = reinterpret_cast<const float4*>(lse2s + c0);
+    // P^T of 32 queries (columns c0 .. c0+31 of this key's row) from S^T - LSE/scale:
+    // exp2(scale log2 e (S^T - LSE/scale)), kept in fp32 pairs (pv, for dS^T) and packed
+    // to 16 bits (pk, the A operand of dV); causal diagonal tile: query q sees key r iff
+    // r <= q.
+    auto p_chunk = [&](const uint32_t* sr, int c0, bool diag, uint64_t* pv, uint32_t* pk) {
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 l = l4[c4];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 4 * c4 + 2 * e;
-          const uint64_t negl = e ? f2_pack(-l.z, -l.w) : f2_pack(-l.x, -l.y);
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
-                           negl),
-                    x0, x1);
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if (diag) {
-            if (c0 + c < r) p0 = 0.f;
-            if (c0 + c + 1 < r) p1 = 0.f;
-          }
-          pv[c >> 1] = f2_pack(p0, p1);
-          pk[c >> 1] = pack_elem2<F16>(p0, p1);
+      for (int c = 0; c < 32; c += 2) {
+        float x0, x1;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2),
+                  x0, x1);
+        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        if (diag) {
+          if (c0 + c < r) p0 = 0.f;
+          if (c0 + c + 1 < r) p1 = 0.f;
         }
+        pv[c >> 1] = f2_pack(p0, p1);
+        pk[c >> 1] = pack_elem2<F16>(p0, p1);
       }
     };
-    // dS^T = P^T * (dP^T - D) of 32 queries, packed to 16 bits.
-    auto ds_chunk = [&](const uint32_t* dr, const float* dds, int c0, const uint64_t* pv,
-                        uint32_t* pd) {
-      const float4* d4 = reinterpret_cast<const float4*>(dds + c0);
+    // dS^T = P^T * (dP^T - D) of 32 queries from dP^T - D, packed to 16 bits.
+    auto ds_chunk = [&](const uint32_t* dr, const uint64_t* pv, uint32_t* pd) {
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 dq4 = d4[c4];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 4 * c4 + 2 * e;
-          const uint64_t negd = e ? f2_pack(-dq4.z, -dq4.w) : f2_pack(-dq4.x, -dq4.y);
-          const uint64_t ds = f2_mul(
-              pv[c >> 1], f2_add(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), negd));
-          float d0, d1;
-          f2_unpack(ds, d0, d1);
-          pd[c >> 1] = pack_elem2<F16>(d0, d1);
-        }
+      for (int c = 0; c < 32; c += 2) {
+        float d0, d1;
+        f2_unpack(f2_mul(pv[c >> 1], f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1]))),
+                  d0, d1);
+        pd[c >> 1] = pack_elem2<F16>(d0, d1);
       }
     };
     // One-pass: the dQ partial of query tile t (TMEM lanes 32 wq .. +31 = its queries,
@@ -609,32 +579,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // staging, ds_ready.  The statistics came in through the tensor core, so these warps
       // read nothing from the stages.
       const uint32_t tP = tbase + lane_off + Cfg::kColP;
-      // P^T of 32 queries from S^T - LSE/scale: exp2(scale log2 e (S^T - LSE/scale)).
-      auto p_chunk1 = [&](const uint32_t* sr, int c0, bool diag, uint64_t* pv, uint32_t* pk) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float x0, x1;
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2),
-                    x0, x1);
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if (diag) {
-            if (c0 + c < r) p0 = 0.f;
-            if (c0 + c + 1 < r) p1 = 0.f;
-          }
-          pv[c >> 1] = f2_pack(p0, p1);
-          pk[c >> 1] = pack_elem2<F16>(p0, p1);
-        }
-      };
-      // dS^T = P^T * (dP^T - D) of 32 queries, packed to 16 bits.
-      auto ds_chunk1 = [&](const uint32_t* dr, const uint64_t* pv, uint32_t* pd) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float d0, d1;
-          f2_unpack(f2_mul(pv[c >> 1], f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1]))),
-                    d0, d1);
-          pd[c >> 1] = pack_elem2<F16>(d0, d1);
-        }
-      };
       for (int it = 0; ok && it < nq; ++it) {
         ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
         if (!ok) break;
@@ -651,7 +595,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
           }
-          p_chunk1(sr, 64 * h + 32 * ch, diag, pv + 16 * ch, pk + 16 * ch);
+          p_chunk(sr, 64 * h + 32 * ch, diag, pv + 16 * ch, pk + 16 * ch);
         }
         ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
         if (!ok) break;
@@ -669,7 +613,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int c0 = 64 * h + 32 * ch;
           uint32_t dr[32], pd[16];
           tmem_ld32_wait(tDP + c0, dr);
-          ds_chunk1(dr, pv + 16 * ch, pd);
+          ds_chunk(dr, pv + 16 * ch, pd);
           tmem_st16(tDP + 64 * h + 16 * ch, pd);
           // Row r (this key) of box h: queries 64h + 32ch .. +31 are its 16-byte chunks
           // 4ch .. 4ch+3, each at its 128-byte-swizzle position (chunk ^ (r % 8)).
@@ -686,18 +630,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
       }
     } else {
-    // The statistics of query tile it come in by TMA with its stage; the warps wait on the
-    // stage's own barrier to see them, for tile it+1 at the end of tile it (off the path
-    // from S^T to P^T; the stage is refilled only after these warps are done with it).
-    ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->stage_full[0]), 0, abort, p.status));
+    // The statistics came in through the tensor core (S^T - LSE/scale, dP^T - D), so these
+    // warps read nothing from the stages.
     for (int it = 0; ok && it < nq; ++it) {
       ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
       const int i = i0 + it;
-      const float* lse2s = reinterpret_cast<const float*>(
-          smem + Cfg::kSmemStages + (it % Cfg::kStages) * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
-      const float* dds = lse2s + 128;
       const bool diag = p.causal && i == j;  // query q sees key r iff r <= q
       // P^T: kept in registers for dS^T and stored (16-bit) over the first half of this
       // warp's S^T columns for dV.
@@ -707,7 +646,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int c0 = 64 * h + 32 * ch;    // first query (column) of this chunk
         uint32_t sr[32], pk[16];
         tmem_ld32_wait(tS + c0, sr);
-        p_chunk(sr, lse2s, c0, diag, pv + 16 * ch, pk);
+        p_chunk(sr, c0, diag, pv + 16 * ch, pk);
         tmem_st16(tS + 64 * h + 16 * ch, pk);
       }
       tmem_wait_st();
@@ -724,17 +663,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int c0 = 64 * h + 32 * ch;
         uint32_t dr[32], pd[16];
         tmem_ld32_wait(tDP + c0, dr);
-        ds_chunk(dr, dds, c0, pv + 16 * ch, pd);
+        ds_chunk(dr, pv + 16 * ch, pd);
         tmem_st16(tDP + 64 * h + 16 * ch, pd);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
-      if (it + 1 < nq)
-        ok = __all_sync(0xffffffffu,
-                        bwd_wait(smem_u32(&bars->stage_full[(it + 1) % Cfg::kStages]),
-                                  ((it + 1) / Cfg::kStages) & 1, abort, p.status));
     }
     }
     if (ok) {
@@ -1081,11 +1016,11 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   constexpr bool kFused = (D == 64);
   AttnBwdParams p = p0;
   const long long rows = static_cast<long long>(p.BH) * p.n_pad;
-  // Workspace: d = 128 LSE * log2(e) and D per row; d = 64 the statistics terms (16 bf16
-  // per row) and then the dQ accumulator (64 fp32 per row).
+  // Workspace: d = 128 LSE * log2(e) and D per row, then the statistics terms (16 bf16
+  // per row); d = 64 the terms and then the dQ accumulator (64 fp32 per row).
   p.lse2 = kFused ? nullptr : ws;
   p.dd = kFused ? nullptr : ws + rows;
-  p.aug = kFused ? reinterpret_cast<uint16_t*>(ws) : nullptr;
+  p.aug = reinterpret_cast<uint16_t*>(kFused ? ws : ws + 2 * rows);
   p.dq_acc = kFused ? ws + 8 * rows : nullptr;
   attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((rows + 8 * kPrepRows - 1) / (8 * kPrepRows)),
                                  256, 0, stream>>>(

@@ -210,11 +210,12 @@ def test_splitkv_rejects_f32(lib):
 
 
 def test_bwd_workspace_size(lib):
-    # Per (head, query row), rows padded to a multiple of 128: 2 fp32 statistics, or for
-    # bf16/fp16 at d = 64 16 bf16 statistics terms and a 64-float dQ accumulator row.
+    # Per (head, query row), rows padded to a multiple of 128: bf16/fp16 at d = 128 2 fp32
+    # statistics and 16 bf16 statistics terms; at d = 64 the terms and a 64-float dQ
+    # accumulator row; fp32 2 fp32 statistics.
     dt = abi.fa_bwd_workspace_bytes_dt
-    assert dt(2, 3, 300, 128, abi.FA_BF16) == 2 * 6 * 384 * 4
-    assert dt(2, 3, 300, 128, abi.FA_F16) == 2 * 6 * 384 * 4
+    assert dt(2, 3, 300, 128, abi.FA_BF16) == (2 * 4 + 16 * 2) * 6 * 384
+    assert dt(2, 3, 300, 128, abi.FA_F16) == (2 * 4 + 16 * 2) * 6 * 384
     assert dt(2, 3, 300, 64, abi.FA_BF16) == (16 * 2 + 64 * 4) * 6 * 384
     assert dt(1, 1, 128, 64, abi.FA_F16) == (16 * 2 + 64 * 4) * 128
     assert dt(1, 1, 128, 64, abi.FA_F32) == 2 * 128 * 4
