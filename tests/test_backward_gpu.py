@@ -114,6 +114,28 @@ def test_backward_large_logits(d):
         _check(name, g, r)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_backward_large_score_offset(d, dtype):
+    """Q and K share a constant 45 in dimension 0, so every score carries +2025: the
+    softmax (and every gradient but the shifted dimension's) is that of the problem
+    without it, while LSE/scale is ~2025.  The key-outer kernels add -LSE/scale through
+    the tensor core as a high and a low bf16 term; the high term alone would be off by up
+    to 4 there (a factor 1.65 in P at scale 1/8), the pair is within about 0.01.
+    Dimension 0 of dQ is 45·scale·(row sum of dS) = 0 exactly, so there only the rounding
+    of dS shows (times 45), and that of dK is 45× the others: both gradients are compared
+    on dimensions 1 .. d-1, dV in full (a wrong P shows in all three)."""
+    q, k, v, do = _inputs(1, 2, 500, d, seed=2600 + d, dtype=dtype)
+    q[..., 0] = 45.0
+    k[..., 0] = 45.0
+    scale = 1.0 / np.sqrt(d)
+    dq, dk, dv = _run_bwd(q, k, v, do, scale, True, dtype=dtype)
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, scale, True)
+    _check("dQ", dq[..., 1:], rq[..., 1:])
+    _check("dK", dk[..., 1:], rk[..., 1:])
+    _check("dV", dv, rv)
+
+
 def _dq_close(got, ref):
     """dQ at d = 64 is summed in fp32 by several blocks in a varying order: two runs may
     differ by the rounding of those sums, at most about one 16-bit ulp per element."""
