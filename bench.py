@@ -913,7 +913,7 @@ def forward_run(args):
 def block_study(args):
     """The block-size study: each attention workload (B4 H16 N4096 d64; B2 H16 N8192 d128
     causal; B1 H8 N32768 d128 causal, Q std 4) through fa_fwd_block with 64-, 128- and (at
-    d = 64) 256-key tiles: median and mean of 20 CUDA-event-timed launches after 3 warm-ups,
+    d = 64) 192- and 256-key tiles: median and mean of 20 CUDA-event-timed launches after 3 warm-ups,
     TFLOP/s, and the O / LSE errors against the fp64 oracle on 34 seeded rows of four
     heads.  One JSON line per (workload, block)."""
     import torch
@@ -935,7 +935,7 @@ def block_study(args):
         o = torch.empty_like(tq)
         lse = torch.empty((B, H, N), device=dev)
         scale = 1.0 / math.sqrt(d)
-        for block_n in ((64, 128, 256) if d == 64 else (64, 128)):
+        for block_n in ((64, 128, 192, 256) if d == 64 else (64, 128)):
             call = lambda: abi.fa_fwd_block(tq, tk, tv, o, lse, B, H, N, d, scale,
                                             int(w["causal"]), abi.FA_BF16, block_n, stream)
             for _ in range(3):

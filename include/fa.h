@@ -100,9 +100,9 @@ fa_status fa_fwd_dt(const void* q, const void* k, const void* v, void* o, float*
  * exists for that study: same operation, arguments and results as fa_fwd_dt.
  *
  * block_n: 0 or 128 = fa_fwd_dt (the kernel the library otherwise runs; any dtype fa_fwd_dt
- *          takes); 64 (d = 64 or 128) or 256 (d = 64): the same tcgen05 kernel built with
- *          64- or 256-key tiles, FA_BF16 only.  Other values: FA_ERR_INVALID; 256 with
- *          d = 128 or a 16-bit type other than bf16: FA_ERR_UNSUPPORTED.
+ *          takes); 64 (d = 64 or 128), 192 or 256 (d = 64): the same tcgen05 kernel built
+ *          with 64-, 192- or 256-key tiles, FA_BF16 only.  Other values: FA_ERR_INVALID;
+ *          192 or 256 with d = 128, or a 16-bit type other than bf16: FA_ERR_UNSUPPORTED.
  * Errors: as fa_fwd_dt.
  */
 fa_status fa_fwd_block(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -195,6 +195,8 @@ fa_status run_tc(const void* q, const void* k, const void* v, void* o, float* ls
   if (block_n == 64)  // block-size study kernels (bf16)
     e = d == 64 ? launch_attn_tc<64, 64, false>(tq, tk, tv, to, p, stream)
                 : launch_attn_tc<128, 64, false>(tq, tk, tv, to, p, stream);
+  else if (block_n == 192)
+    e = launch_attn_tc<64, 192, false>(tq, tk, tv, to, p, stream);
   else if (block_n == 256)
     e = launch_attn_tc<64, 256, false>(tq, tk, tv, to, p, stream);
   else if (d == 64)
@@ -301,10 +303,10 @@ fa_status fa_fwd_block(const void* q, const void* k, const void* v, void* o, flo
                        cudaStream_t stream) {
   if (block_n == 0 || block_n == kDefaultBlockN)
     return fa_fwd_dt(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream);
-  if (block_n != 64 && block_n != 256) return FA_ERR_INVALID;
+  if (block_n != 64 && block_n != 192 && block_n != 256) return FA_ERR_INVALID;
   fa_status st = check_tc_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype);
   if (st != FA_OK) return st;
-  if (dtype != FA_BF16 || (block_n == 256 && d != 64)) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_BF16 || (block_n >= 192 && d != 64)) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H == 0 || N == 0) return FA_OK;
   return run_tc(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, 1, nullptr, nullptr, stream,
                 block_n);

@@ -57,19 +57,22 @@ template <bool F16>
 constexpr float kRescaleLog2 = 8.0f;
 
 // D: head dimension; BN: keys per K/V tile (the "block size" of the tile loop).  BN = 128
-// is the kernel the library runs; BN = 64 (both d) and 256 (d = 64) are built for the
-// block-size study.
+// is the kernel the library runs; BN = 64 (both d) and 192, 256 (d = 64) are built for
+// the block-size study.
 template <int D, int BN>
 struct AttnTcCfg {
   static_assert(D == 64 || D == 128, "head dimension");
-  static_assert(BN == 64 || BN == 128 || (BN == 256 && D == 64), "key block");
+  static_assert(BN == 64 || BN == 128 || ((BN == 192 || BN == 256) && D == 64), "key block");
   static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kQTileBytes = kBoxes * kBoxBytes;  // 128 query rows x D
   static constexpr int kKvBoxBytes = BN * 128;            // BN keys x 64 columns
   static constexpr int kTileBytes = kBoxes * kKvBoxBytes; // one K or V tile: BN keys x D
   // K/V ring depth: the slots that fit next to the two Q tiles in about 224 KB.
-  static constexpr int kSlots = (D == 128) ? (BN == 64 ? 10 : 5) : (BN == 64 ? 16 : BN == 128 ? 8 : 6);
-  static constexpr bool kPairWait = (D == 64);  // one landing barrier per K/V pair
+  static constexpr int kSlots =
+      (D == 128) ? (BN == 64 ? 10 : 5) : (BN == 64 ? 16 : BN == 128 ? 8 : BN == 192 ? 8 : 6);
+  // One landing barrier per K/V pair (d = 64 with three S buffers or one), else one per
+  // slot (the two-buffer issue order of d = 128, also used by 192-key tiles).
+  static constexpr bool kPairWait = (D == 64 && BN != 192);
   static constexpr int kSmemQ0 = 0;
   static constexpr int kSmemQ1 = kQTileBytes;
   static constexpr int kSmemSlots = 2 * kQTileBytes;
@@ -78,9 +81,9 @@ struct AttnTcCfg {
   // TMEM columns: kSBufs S/P buffers of BN columns, then O of tile 0 and 1.  d = 128:
   // two buffers (one per tile).  d = 64: the O accumulators take only 128 columns, which
   // leaves room for a third buffer, so that the next S of a tile can be computed while
-  // its current P is still being formed; at BN = 256 one 256-column buffer is all that
-  // fits, and the two tiles take turns.
-  static constexpr int kSBufs = (D == 128) ? 2 : (BN == 256 ? 1 : 3);
+  // its current P is still being formed; at BN = 192 two buffers fit (as at d = 128), at
+  // BN = 256 one 256-column buffer is all that fits, and the two tiles take turns.
+  static constexpr int kSBufs = (D == 128 || BN == 192) ? 2 : (BN == 256 ? 1 : 3);
   static constexpr uint32_t kColO0 = kSBufs * BN, kColO1 = kColO0 + D;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kColO1 + D <= kTmemCols, "TMEM columns");

@@ -303,6 +303,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if constexpr (BN == 64) mma_ts4_elect(tO, a, b, kIdescPV, acc ? 1u : 0u);
       else if constexpr (BN == 128) mma_ts8_elect(tO, a, b, kIdescPV, acc ? 1u : 0u);
+      else if constexpr (BN == 192) {
+        mma_ts8_elect(tO, a, b, kIdescPV, acc ? 1u : 0u);
+        mma_ts4_elect(tO, a + 8, b + 8, kIdescPV, 1u);
+      }
       else mma_ts16_elect(tO, a, b, kIdescPV, acc ? 1u : 0u);
     };
 
@@ -513,6 +517,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // half, which stays in registers (the upper one is loaded again below).
         const float mx_hi = load_chunk(128, ChunkW{}, sr);
         rowmax = fmaxf(load_chunk(0, ChunkW{}, sr), mx_hi);
+      } else if constexpr (BN == 192) {
+        // The 64 upper columns for their maximum only, then the 128 lower ones, which
+        // stay in registers (the upper ones are loaded again below).
+        const float mx_hi = load_chunk(128, std::integral_constant<int, 64>{}, sr);
+        rowmax = fmaxf(load_chunk(0, ChunkW{}, sr), mx_hi);
       } else {
         rowmax = load_chunk(0, ChunkW{}, sr);
       }
@@ -543,9 +552,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm2 = f2_pack(-m2, -m2);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-      auto exp_chunk = [&](int c0) {  // the kChunk scores in s are keys c0 .. c0 + kChunk - 1
+      // The W scores in s are keys c0 .. c0 + W - 1.
+      auto exp_chunk = [&](int c0, auto width) {
+        constexpr int W = decltype(width)::value;
 #pragma unroll
-        for (int h = 0; h < kChunk / 32; ++h) {
+        for (int h = 0; h < W / 32; ++h) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -560,12 +571,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tmem_st16(tS + c0 / 2 + 16 * h, pk);
         }
       };
-      exp_chunk(0);
+      exp_chunk(0, ChunkW{});
       if constexpr (BN == 256) {
         // The upper half again (its columns are still S: the P of the lower half went to
         // columns 0 .. 63).
         load_chunk(128, ChunkW{}, sr);
-        exp_chunk(128);
+        exp_chunk(128, ChunkW{});
+      } else if constexpr (BN == 192) {
+        // The upper 64 columns again (still S: the P of the lower 128 went to 0 .. 63).
+        load_chunk(128, std::integral_constant<int, 64>{}, sr);
+        exp_chunk(128, std::integral_constant<int, 64>{});
       }
       float a0, a1, a2, a3, a4, a5, a6, a7;
       f2_unpack(acc[0], a0, a1);

@@ -183,7 +183,8 @@ def test_splitkv_static_argument_checks(lib, args, expect):
 
 @pytest.mark.parametrize("block_n,d,dtype,expect", [
     (32, 64, abi.FA_BF16, abi.FA_ERR_INVALID),
-    (192, 64, abi.FA_BF16, abi.FA_ERR_INVALID),
+    (160, 64, abi.FA_BF16, abi.FA_ERR_INVALID),
+    (192, 128, abi.FA_BF16, abi.FA_ERR_UNSUPPORTED),    # 192-key tiles only at d = 64
     (256, 128, abi.FA_BF16, abi.FA_ERR_UNSUPPORTED),    # 256-key tiles only at d = 64
     (64, 64, abi.FA_F16, abi.FA_ERR_UNSUPPORTED),       # study kernels are bf16 only
     (64, 64, abi.FA_F32, abi.FA_ERR_UNSUPPORTED),
@@ -196,7 +197,7 @@ def test_fa_fwd_block_argument_checks(lib, block_n, d, dtype, expect):
 
 def test_fa_fwd_block_empty_and_bad_scale(lib):
     # checked on the host before any CUDA call, whatever the block size
-    for block_n in (64, 256):
+    for block_n in (64, 192, 256):
         assert lib.fa_fwd_block(FAKE, FAKE, FAKE, FAKE, None, 0, 1, 256, 64, 0.1, 1, abi.FA_BF16,
                                 block_n, None) == abi.FA_OK
         assert lib.fa_fwd_block(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 256, 64, -1.0, 1, abi.FA_BF16,

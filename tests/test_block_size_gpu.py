@@ -23,7 +23,7 @@ from gpu_helpers import check_attention, sample_rows, to_device
 
 pytestmark = pytest.mark.gpu
 
-BLOCKS = [(64, 64), (64, 128), (64, 256), (128, 64), (128, 128)]   # (d, keys per tile)
+BLOCKS = [(64, 64), (64, 128), (64, 192), (64, 256), (128, 64), (128, 128)]   # (d, keys per tile)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -98,6 +98,7 @@ def test_default_block_is_fa_fwd_dt():
 
 
 @pytest.mark.parametrize("name,block_n", [("attn_bf16_b4h16n4096d64", 64),
+                                          ("attn_bf16_b4h16n4096d64", 192),
                                           ("attn_bf16_b4h16n4096d64", 256),
                                           ("attn_bf16_b2h16n8191d128_causal", 64),
                                           ("attn_bf16_b1h8n32768d128_causal_qstd4", 64)])
