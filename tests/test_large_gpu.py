@@ -1,6 +1,7 @@
-"""Tensors of more than 2^31 elements: B=1 H=4100 N=4096 d=128 bf16, 4.3 GB per tensor.
-Heads 4096..4099 start at or beyond element 2^31, so every index into Q, K, V, O, LSE,
-dO and the gradients must be 64-bit.  Sampled rows of heads on both sides of that
+"""Tensors of more than 2^31 elements: B=1 N=4096 bf16, H=4100 at d=128 and H=8196 at
+d=64, 4.3 GB per tensor.  The last four heads start at or beyond element 2^31, so every
+index into Q, K, V, O, LSE, dO, the gradients and (d = 64) the backward's dQ accumulator
+and statistics terms must be 64-bit.  Sampled rows of heads on both sides of that
 boundary, forward and backward, against the fp64 oracle."""
 
 import numpy as np
@@ -21,11 +22,14 @@ def _lib():
     abi.load()
 
 
-def test_forward_and_backward_beyond_2_31_elements():
+@pytest.mark.parametrize("d", [128, 64])
+def test_forward_and_backward_beyond_2_31_elements(d):
     import torch
 
-    B, H, N, d = 1, 4100, 4096, 128
-    assert B * H * N * d > 2 ** 31 and 4096 * N * d == 2 ** 31
+    B, N = 1, 4096
+    hb = 2 ** 31 // (N * d)   # the first head at element 2^31
+    H = hb + 4
+    assert B * H * N * d > 2 ** 31 and hb * N * d == 2 ** 31
     scale = 1.0 / np.sqrt(d)
     q, k, v, do = (synth.device_normal((B, H, N, d), seed=5_000_000 + i, dtype=torch.bfloat16)
                    for i in range(4))
@@ -33,7 +37,7 @@ def test_forward_and_backward_beyond_2_31_elements():
     lse = torch.empty((B, H, N), device="cuda")
     abi.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, 1)
     assert abi.fa_last_device_error() == abi.FA_OK
-    nbytes = abi.fa_bwd_workspace_bytes(B, H, N)
+    nbytes = abi.fa_bwd_workspace_bytes_dt(B, H, N, d, abi.FA_BF16)
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     abi.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, 1, ws, nbytes, abi.FA_BF16)
@@ -43,7 +47,7 @@ def test_forward_and_backward_beyond_2_31_elements():
     def head(t, h):
         return t[0, h].float().cpu().numpy()[None, None]
 
-    for h in (0, 4095, 4096, H - 1):
+    for h in (0, hb - 1, hb, H - 1):
         rows = sample_rows(N, 24, seed=h)
         qh, kh, vh, doh = (head(t, h) for t in (q, k, v, do))
         o_ref, lse_ref = oracle.attention_forward(qh, kh, vh, scale, True, rows=rows)
