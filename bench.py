@@ -55,7 +55,7 @@ import numpy as np  # noqa: E402
 ATTN = dict(name="attn_bf16_b2h16n8192d128_causal", B=2, H=16, N=8192, d=128, causal=True)
 ROWS = dict(name="rows_4096x32768", rows=4096, length=32768)
 METRIC = "attn fwd TFLOP/s and % of GB300 bf16 dense peak (1 GPU); row-softmax HBM GB/s"
-FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
 def run_config(world):
@@ -603,10 +603,16 @@ def our_arm(args, rank, world, local_rank):
                          "traffic": recorded_traffic("row_state_block_kernel"),
                          "peak_source": peaks["source"]},
         },
+        # `peak` is the burst figure.  The timed steps run back to back after a load
+        # window, under the board's power cap (see `clocks`), so the fraction of the
+        # sustained figure is given beside it.
         "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": per_gpu_tflops / peaks["bf16_tflops"],
                      "traffic": recorded_traffic("attn_fwd_tc_kernel"),
-                     "peak_source": peaks["source"] + " bf16 burst"},
+                     "peak_source": peaks["source"] + " bf16 burst",
+                     "peak_sustained": peaks["bf16_tflops_sustained"] or None,
+                     "frac_of_sustained": (per_gpu_tflops / peaks["bf16_tflops_sustained"]
+                                           if peaks["bf16_tflops_sustained"] else None)},
         "clocks": clocks,
         "e2e": {"value": flops * world / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
