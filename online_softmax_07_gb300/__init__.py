@@ -116,9 +116,11 @@ def _copy_streams(dev):
 
 # Groups of (batch, head) slabs of the host path: the copies of one group overlap the
 # kernels of its neighbours, so more groups shorten the exposed first copy in and last
-# copy out, until a group's kernel is held up by its longest query block.  Measured on
-# B2 H16 N8192 d128 causal (fa_fwd_host): 2 groups 1.405 ms, 4 1.272, 8 1.281, 16 1.689.
-_HOST_CHUNKS = 4
+# copy out, until a group's kernel is held up by its longest query block and the fixed
+# cost of each copy adds up.  Measured on B2 H16 N8192 d128 causal (attention_forward,
+# median wall time per call, two boxes): 4 groups 1.300 / 1.306 ms, 5 (7, 7, 7, 7 and 4
+# heads) 1.265 / 1.271, 6 1.281 / 1.285, 8 1.315 / 1.319; earlier 2 groups 1.405, 16 1.689.
+_HOST_CHUNKS = 5
 
 
 def _attention_forward_host(q, k, v, scale, causal, with_lse, out, lse_out, dtype, s):

@@ -15,9 +15,9 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("B,H,N,d,causal,pin", [
     (1, 3, 300, 128, True, True),     # 3 chunks of one head
-    (2, 5, 257, 64, False, False),    # 10 heads in 8 uneven chunks, inputs not pinned
+    (2, 5, 257, 64, False, False),    # 10 heads in 5 chunks of 2, inputs not pinned
     (1, 1, 129, 128, True, True),     # a single chunk
-    (4, 16, 1024, 128, True, True),   # 64 heads in 8 chunks of 8
+    (4, 16, 1024, 128, True, True),   # 64 heads: four chunks of 13 and a last one of 12
 ])
 def test_host_path_equals_device_path(B, H, N, d, causal, pin):
     q, k, v = (torch.from_numpy(t).to(torch.bfloat16)
