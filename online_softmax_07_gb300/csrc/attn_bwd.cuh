@@ -108,16 +108,18 @@ struct AttnBwd1Cfg {
   // swizzle cannot move a one onto a term of the other statistic.
   static constexpr int kSmemOnes = kSmemStages + kStages * kStageBytes;
   // dS of the current tile pair, [key][query]: two 64-query boxes of 128 keys x 128 B,
-  // 128-byte swizzle (the MN-major A operand of dS K_j).
+  // 128-byte swizzle: the K-major A operand dS^T of dK += dS^T Q_i and the MN-major A
+  // operand of dQ_i = dS K_j.
   static constexpr int kSmemDS = kSmemOnes + 2 * kAugBytes;
   // dQ staging: per element-wise warp one box of 32 rows x 32 fp32 (4 KB).
   static constexpr int kRedBoxBytes = 32 * 128;
   static constexpr int kSmemRed = kSmemDS + 2 * kTileBytes;
   static constexpr int kSmemBars = kSmemRed + 8 * kRedBoxBytes;
   static constexpr int kSmemBytes = kSmemBars + 512 + 1024;
-  // TMEM: S^T, dP^T (dS^T packed over it), dV, dK, P^T (16-bit, two queries a column:
-  // its own columns, so that the next S^T may overwrite S^T as soon as the element-wise
-  // warps hold it in registers) and the dQ partial.
+  // TMEM: S^T, dP^T, dV, dK, P^T (16-bit, two queries a column: its own columns, so that
+  // the next S^T may overwrite S^T as soon as the element-wise warps hold it in
+  // registers; the next dP^T likewise, since dS goes to shared memory only) and the dQ
+  // partial.
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 320;
   static constexpr uint32_t kColP = 384, kColDQ = 448;
   static constexpr uint32_t kTmemCols = 512;

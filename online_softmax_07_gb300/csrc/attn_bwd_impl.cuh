@@ -25,6 +25,8 @@ struct AttnBwdBarriers {
   uint64_t v_full[4];       // query-outer: the V ring
   uint64_t v_empty[4];
   uint64_t s_free;          // one-pass (d = 64): the element-wise warps hold S^T in registers
+  uint64_t dp_free;         // one-pass: ... and dP^T
+  uint64_t dq_done;         // one-pass: dK and the dQ partial of a tile pair finished
   uint32_t tmem_base;
   int abort;
 };
@@ -281,6 +283,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&bars->stage_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars->s_free), 8);
+    mbar_init(smem_u32(&bars->dp_free), 8);
+    mbar_init(smem_u32(&bars->dq_done), 1);
     bars->abort = 0;
     mbar_init_fence();
   }
@@ -405,17 +409,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // One pass (d = 64), per query tile it:
       //   S^T(it+1) (once the element-wise warps hold S^T(it) in registers)  |
       //   dV(it) = P^T(it) dO_it (P^T in its own columns)  |
-      //   dK(it)  |  dQ(it) = dS(it) K_j  |  dP^T(it+1)
-      // dQ(it): A = dS from shared memory, MN-major (queries contiguous, the two 64-query
-      // boxes 16 KB apart), B = K_j, MN-major, 16 keys (2 KB of each) per step.  Products
-      // complete in issue order (one issuing thread), so the commit of dP^T(it+1) also
-      // reports dV(it), dK(it) and dQ(it) done: the element-wise warps wait for nothing
-      // else before they overwrite P^T and the dS staging or drain the dQ partial, and
-      // dQ(it+1) is issued only after ds_ready(it+1), which they signal after that drain.
-      // The products go out in groups under one elect each: this warp shares its
-      // scheduler with two element-wise warps, and every instruction on its path costs.
+      //   dP^T(it+1) (once they hold dP^T(it) as well)  |
+      //   dK(it) = dS^T(it) Q_it  |  dQ(it) = dS(it) K_j
+      // dS of the tile pair is staged in shared memory once, [key][query] in two 64-query
+      // boxes (128-byte swizzle), and read by both of its products: K-major as the A
+      // operand dS^T of dK, MN-major (the boxes 16 KB apart) as the A operand dS of dQ;
+      // B = Q_it or K_j, MN-major, 16 rows (2 KB) per step.  dS^T is not stored in TMEM,
+      // so dP^T(it+1) need not wait for dK(it) and runs while the element-wise warps form
+      // dS(it).  Products complete in issue order (one issuing thread): the commit of
+      // dP^T(it) also reports dV(it-1) done (P^T may be overwritten), and the commit after
+      // dQ(it) (dq_done) reports dK(it) done too (the staging may be rewritten, the dQ
+      // partial drained); dQ(it+1) is issued only after ds_ready(it+1), which the element-
+      // wise warps signal after that drain.  The products go out in groups under one elect
+      // each: this warp shares its scheduler with two element-wise warps, and every
+      // instruction on its path costs.
       constexpr uint32_t kIdescDQ = idesc_f16kind(kBlockM, D, true, F16) | kIdescAMnMajor;
       const uint64_t dDS = desc_sw128(sbase + Cfg::kSmemDS, kBoxBytes, 1024);
+      const uint64_t dDSt = desc_sw128(sbase + Cfg::kSmemDS, 16, 1024);
       const uint64_t dKmn = desc_sw128(sbase + Cfg::kSmemFixed0, kBoxBytes, 1024);
       // S^T (or dP^T), K = 64 under one elect, then the statistics step.
       auto group_t = [&](uint32_t tD, uint64_t dA, uint64_t dB, uint64_t dOnes, int st) {
@@ -427,18 +437,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mma_ss4_elect(tD, a, b, kIdescS, 0u);
         issue_aug(tD, dOnes, st);
-      };
-      // dV or dK: A = 16 queries (8 packed columns) per step, the 64-query halves `half`
-      // columns apart.
-      auto group_acc = [&](uint32_t tAcc, uint32_t tA, uint32_t half, uint64_t dB, bool acc) {
-        uint32_t a[8];
-        uint64_t b[8];
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          a[kk] = tA + (kk >> 2) * half + (kk & 3) * 8;
-          b[kk] = dB + kk * 128;
-        }
-        mma_ts8_elect(tAcc, a, b, kIdescAcc, acc ? 1u : 0u);
       };
       const uint32_t tP = tbase + Cfg::kColP, tDQ = tbase + Cfg::kColDQ;
       if (ok) {
@@ -458,9 +456,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit_elect(smem_u32(&bars->s_full));
         }
         if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
-        group_acc(tDV, tP, 32, desc_mn(it, 1), it > 0);
+        {
+          // dV += P^T(it) dO_it: A = 16 queries (8 packed columns) per step, the 64-query
+          // halves 32 columns apart.
+          uint32_t a[8];
+          uint64_t b[8];
+          const uint64_t dB = desc_mn(it, 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            a[kk] = tP + (kk >> 2) * 32 + (kk & 3) * 8;
+            b[kk] = dB + kk * 128;
+          }
+          mma_ts8_elect(tDV, a, b, kIdescAcc, it > 0 ? 1u : 0u);
+        }
+        if (more) {
+          if (!(ok = wait_bar(&bars->dp_free, it & 1))) break;
+          group_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
+          mma_commit_elect(smem_u32(&bars->dp_full));
+        }
         if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
-        group_acc(tDK, tDP, 64, desc_mn(it, 0), it > 0);
+        {
+          // dK += dS^T(it) Q_it: A = the staging read K-major, 16 queries (32 bytes of a
+          // 128-byte row) per step, the second 64-query box 16 KB on.
+          uint64_t a[8], b[8];
+          const uint64_t dB = desc_mn(it, 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            a[kk] = dDSt + ((((kk >> 2) * kBoxBytes) + (kk & 3) * 32) >> 4);
+            b[kk] = dB + kk * 128;
+          }
+          mma_ss8_elect(tDK, a, b, kIdescAcc, it > 0 ? 1u : 0u);
+        }
         mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
         {
           uint64_t a[8], b[8];
@@ -471,10 +497,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           mma_ss8_elect(tDQ, a, b, kIdescDQ, 0u);
         }
-        if (more) {
-          group_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
-          mma_commit_elect(smem_u32(&bars->dp_full));
-        }
+        mma_commit_elect(smem_u32(&bars->dq_done));
       }
     } else {
     if (ok) {
@@ -574,10 +597,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if constexpr (Fused) {
       // One pass (d = 64), per query tile it: S^T - LSE/scale into registers, "S^T free"
       // (the next S^T may overwrite it), P; then, once dP^T(it) - D is in (which also
-      // reports dV, dK and dQ of tile it - 1 complete), P^T into its own columns, p_done,
-      // the dQ partial of tile it - 1 drained, dS^T over dP^T and dS into the shared-memory
-      // staging, ds_ready.  The statistics came in through the tensor core, so these warps
-      // read nothing from the stages.
+      // reports dV of tile it - 1 complete), P^T into its own columns, p_done; dP^T into
+      // registers, "dP^T free"; once dK and dQ of tile it - 1 are complete (dq_done), its
+      // dQ partial drained, dS into the shared-memory staging, ds_ready.  The statistics
+      // came in through the tensor core, so these warps read nothing from the stages.
       const uint32_t tP = tbase + lane_off + Cfg::kColP;
       for (int it = 0; ok && it < nq; ++it) {
         ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
@@ -607,23 +630,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
-        if (it > 0) reduce_dq(it - 1);
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          const int c0 = 64 * h + 32 * ch;
-          uint32_t dr[32], pd[16];
-          tmem_ld32_wait(tDP + c0, dr);
-          ds_chunk(dr, pv + 16 * ch, pd);
-          tmem_st16(tDP + 64 * h + 16 * ch, pd);
-          // Row r (this key) of box h: queries 64h + 32ch .. +31 are its 16-byte chunks
-          // 4ch .. 4ch+3, each at its 128-byte-swizzle position (chunk ^ (r % 8)).
-          const uint32_t row = sbase + Cfg::kSmemDS + h * kBoxBytes + r * 128 + ((r & 7) << 4);
-          if (ch == 0)
-            st_shared_swz4<0>(row, pd);
-          else
-            st_shared_swz4<4>(row, pd);
+        // dS^T = P^T * (dP^T - D) of this warp's 64 queries, 16-bit.
+        uint32_t pd[32];
+        {
+          uint32_t dr[32];
+          tmem_ld32_wait(tDP + 64 * h, dr);
+          ds_chunk(dr, pv, pd);
+          tmem_ld32_wait(tDP + 64 * h + 32, dr);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->dp_free));
+          ds_chunk(dr, pv + 16, pd + 16);
         }
-        tmem_wait_st();
+        if (it > 0) {
+          ok = __all_sync(0xffffffffu,
+                          bwd_wait(smem_u32(&bars->dq_done), (it - 1) & 1, abort, p.status));
+          if (!ok) break;
+          tc_fence_after();
+          reduce_dq(it - 1);
+        }
+        // Row r (this key) of box h: queries 64h .. 64h+63 are its 16-byte chunks 0 .. 7,
+        // each at its 128-byte-swizzle position (chunk ^ (r % 8)).
+        const uint32_t row = sbase + Cfg::kSmemDS + h * kBoxBytes + r * 128 + ((r & 7) << 4);
+        st_shared_swz4<0>(row, pd);
+        st_shared_swz4<4>(row, pd + 16);
         fence_proxy_async_smem();  // dS is read by the tensor pipe
         tc_fence_before();
         __syncwarp();
