@@ -33,10 +33,12 @@
 namespace osfa {
 
 // Warps 0-7: element-wise work, warp w on TMEM lanes 32 (w % 4) .. +31 and on the
-// column half w / 4 of each tile; 8: MMA issue; 9: TMA loads; 10-11 idle.
+// column half w / 4 of each tile; 8: MMA issue; 9: TMA loads; 10: in the one-pass kernel
+// a second MMA-issuing warp (dK and dQ), else idle; 11 idle.
 constexpr int kBwdThreads = 384;
 constexpr int kBwdWarpMma = 8;
 constexpr int kBwdWarpLoad = 9;
+constexpr int kBwdWarpMma2 = 10;
 
 // Two-pass backward (d = 128).
 template <int D>
