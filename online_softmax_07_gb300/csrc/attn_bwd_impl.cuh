@@ -20,7 +20,7 @@ struct AttnBwdBarriers {
   uint64_t ds_ready;     // element-wise -> MMA: dS (or dS^T) stored in TMEM
   uint64_t acc_final;    // MMA -> element-wise: the last accumulation finished
   uint64_t mma_drain;    // MMA warp: all of its MMAs finished (before TMEM is freed)
-  uint64_t mma_drain2;   // one-pass: the same for the second MMA warp
+  uint64_t mma_drain2;   // one pass: the same for the second MMA warp
   uint64_t stage_full[4];   // key-outer: Q_i, dO_i stages; query-outer: the K ring
   uint64_t stage_empty[4];
   uint64_t v_full[4];       // query-outer: the V ring
@@ -311,59 +311,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort = &bars->abort;
   auto stage_addr = [&](int s) { return sbase + Cfg::kSmemStages + s * Cfg::kStageBytes; };
 
-  if (Fused && warp == kBwdWarpMma2) {
-    if constexpr (Fused) {
-      // ------------------------------------------------------------ second MMA issuer
-      // One pass: per query tile it, once dS(it) is staged, dK += dS^T(it) Q_it (A = the
-      // staging read K-major, 16 queries = 32 bytes of a 128-byte row per step, the second
-      // 64-query box 16 KB on) and dQ(it) = dS(it) K_j (A = the staging read MN-major, B =
-      // K_j MN-major, 16 keys per step) into the dQ partial.
-      constexpr uint32_t kIdescAcc = idesc_f16kind(kBlockM, D, true, F16);
-      constexpr uint32_t kIdescDQ = kIdescAcc | kIdescAMnMajor;
-      const uint64_t dDS = desc_sw128(sbase + Cfg::kSmemDS, kBoxBytes, 1024);
-      const uint64_t dDSt = desc_sw128(sbase + Cfg::kSmemDS, 16, 1024);
-      const uint64_t dKmn = desc_sw128(sbase + Cfg::kSmemFixed0, kBoxBytes, 1024);
-      const uint32_t tDK = tbase + Cfg::kColAcc1, tDQ = tbase + Cfg::kColDQ;
-      auto wait_bar = [&](uint64_t* bar, int parity) {
-        const bool r = __all_sync(0xffffffffu, bwd_wait(smem_u32(bar), parity, abort, p.status));
-        if (r) tc_fence_after();
-        return r;
-      };
-      bool ok = wait_bar(&bars->fixed_full, 0);
-      for (int it = 0; ok && it < nq; ++it) {
-        const int st = it % Cfg::kStages;
-        if (!(ok = wait_bar(&bars->stage_full[st], (it / Cfg::kStages) & 1) &&
-                   wait_bar(&bars->ds_ready, it & 1)))
-          break;
-        {
-          uint64_t a[8], b[8];
-          const uint64_t dB = desc_sw128(stage_addr(st), kBoxBytes, 1024);  // Q_it, MN-major
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            a[kk] = dDSt + ((((kk >> 2) * kBoxBytes) + (kk & 3) * 32) >> 4);
-            b[kk] = dB + kk * 128;
-          }
-          mma_ss8_elect(tDK, a, b, kIdescAcc, it > 0 ? 1u : 0u);
-        }
-        mma_commit_elect(smem_u32(&bars->stage_empty[st]));
-        {
-          uint64_t a[8], b[8];
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            a[kk] = dDS + kk * 128;
-            b[kk] = dKmn + kk * 128;
-          }
-          mma_ss8_elect(tDQ, a, b, kIdescDQ, 0u);
-        }
-        mma_commit_elect(smem_u32(&bars->dq_done));
-      }
-      if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
-      mma_commit_elect(smem_u32(&bars->mma_drain2));
-      int no_abort = 0;
-      bwd_wait(smem_u32(&bars->mma_drain2), 0, &no_abort, p.status);
-      __syncwarp();
-    }
-  } else if (warp >= 10) {
+  if (warp == 11 || (!Fused && warp == kBwdWarpMma2)) {
     // idle
   } else if (warp == kBwdWarpLoad) {
     // ------------------------------------------------------------ TMA producer
@@ -404,8 +352,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bwd_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]), (it / Cfg::kStages) & 1,
                   &no_abort, p.status);
     }
-  } else if (warp == kBwdWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kBwdWarpMma || (Fused && warp == kBwdWarpMma2)) {
+    // ------------------------------------------------------------ MMA issuers
+    // One pass: two warps issue the products, each on its own SM sub-partition (both
+    // share theirs with two element-wise warps, and every instruction on an issuing
+    // warp's path costs).  The products of one issuing thread complete in issue order; a
+    // stage is released by one commit of each warp, and acc_final takes one of each.
+    const bool second = warp == kBwdWarpMma2;
     constexpr uint32_t kIdescS = idesc_f16kind(kBlockM, kBlockM, false, F16);
     constexpr uint32_t kIdescAcc = idesc_f16kind(kBlockM, D, true, F16);
     const uint64_t dK = desc_sw128(sbase + Cfg::kSmemFixed0, 16, 1024);   // A of S^T
@@ -453,22 +406,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           (acc || kk > 0) ? 1u : 0u);
       }
     };
-    // Software pipeline on the tensor pipe, per query tile it:
-    //   dV += P^T(it) dO_it  |  S^T(it+1)  |  dK += dS^T(it) Q_it  |  dP^T(it+1)
-    // dV needs only P^T, so it and the next S^T run while the element-wise warps form
-    // dS^T; the next element-wise step starts on S^T(it+1) while dK and dP^T(it+1) run.
-    // Each TMEM region is overwritten only after the product that reads it (one issuing
-    // thread: products complete in issue order).
     bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0);
     if constexpr (Fused) {
-      // One pass (d = 64).  Two warps issue the products, each on its own SM sub-
-      // partition (both share theirs with two element-wise warps, and every instruction
-      // on an issuing warp's path costs): this one, per query tile it,
+      // One pass (d = 64).  The first warp issues, per query tile it,
       //   S^T(it+1) (once the element-wise warps hold S^T(it) in registers)  |
       //   dV(it) = P^T(it) dO_it (P^T in its own columns)  |
       //   dP^T(it+1) (once they hold dP^T(it) as well),
-      // and the second (warp kBwdWarpMma2) dK(it) = dS^T(it) Q_it and dQ(it) = dS(it) K_j
-      // once dS(it) is staged.  dS of the tile pair is staged in shared memory once,
+      // and the second dK(it) = dS^T(it) Q_it and dQ(it) = dS(it) K_j once dS(it) is
+      // staged.  dS of the tile pair is staged in shared memory once,
       // [key][query] in two 64-query boxes (128-byte swizzle), and read by both of its
       // products: K-major as the A operand dS^T of dK, MN-major (the boxes 16 KB apart) as
       // the A operand dS of dQ.  dS^T is not stored in TMEM, so dP^T(it+1) need not wait
@@ -477,7 +422,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // dV(it-1) done (P^T may be overwritten), and the second warp's commit after dQ(it)
       // (dq_done) reports dK(it) done too (the staging may be rewritten, the partial
       // drained); dQ(it+1) is issued only after ds_ready(it+1), which the element-wise
-      // warps signal after that drain.  A stage is released by one commit of each warp.
+      // warps signal after that drain.
       // S^T (or dP^T), K = 64 under one elect, then the statistics step.
       auto group_t = [&](uint32_t tD, uint64_t dA, uint64_t dB, uint64_t dOnes, int st) {
         uint64_t a[4], b[4];
@@ -490,6 +435,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         issue_aug(tD, dOnes, st);
       };
       const uint32_t tP = tbase + Cfg::kColP;
+      if (second) {
+        // dK += dS^T(it) Q_it: A = the staging read K-major, 16 queries (32 bytes of a
+        // 128-byte row) per step, the second 64-query box 16 KB on; dQ(it) = dS(it) K_j:
+        // A = the staging read MN-major, B = K_j MN-major, 16 keys per step.
+        constexpr uint32_t kIdescDQ = kIdescAcc | kIdescAMnMajor;
+        const uint64_t dDS = desc_sw128(sbase + Cfg::kSmemDS, kBoxBytes, 1024);
+        const uint64_t dDSt = desc_sw128(sbase + Cfg::kSmemDS, 16, 1024);
+        const uint64_t dKmn = desc_sw128(sbase + Cfg::kSmemFixed0, kBoxBytes, 1024);
+        const uint32_t tDQ = tbase + Cfg::kColDQ;
+        for (int it = 0; ok && it < nq; ++it) {
+          const int st = it % Cfg::kStages;
+          if (!(ok = wait_bar(&bars->stage_full[st], (it / Cfg::kStages) & 1) &&
+                     wait_bar(&bars->ds_ready, it & 1)))
+            break;
+          {
+            uint64_t a[8], b[8];
+            const uint64_t dB = desc_mn(it, 0);  // Q_it
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              a[kk] = dDSt + ((((kk >> 2) * kBoxBytes) + (kk & 3) * 32) >> 4);
+              b[kk] = dB + kk * 128;
+            }
+            mma_ss8_elect(tDK, a, b, kIdescAcc, it > 0 ? 1u : 0u);
+          }
+          mma_commit_elect(smem_u32(&bars->stage_empty[st]));
+          {
+            uint64_t a[8], b[8];
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              a[kk] = dDS + kk * 128;
+              b[kk] = dKmn + kk * 128;
+            }
+            mma_ss8_elect(tDQ, a, b, kIdescDQ, 0u);
+          }
+          mma_commit_elect(smem_u32(&bars->dq_done));
+        }
+      } else {
       if (ok) {
         group_t(tS, dK, desc_k(0, 0), dOnesS, 0);
         mma_commit_elect(smem_u32(&bars->s_full));
@@ -528,37 +510,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit_elect(smem_u32(&bars->dp_full));
         }
       }
-    } else {
-    if (ok) {
-      issue_t(tS, dK, desc_k(0, 0), dOnesS, 0);
-      mma_commit_elect(smem_u32(&bars->s_full));
-      issue_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
-      mma_commit_elect(smem_u32(&bars->dp_full));
-    }
-    for (int it = 0; ok && it < nq; ++it) {
-      const bool more = it + 1 < nq;
-      if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
-      issue_acc(tDV, tS, desc_mn(it, 1), it > 0);
-      if (more) {
-        if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
-                            ((it + 1) / Cfg::kStages) & 1)))
-          break;
-        issue_t(tS, dK, desc_k(it + 1, 0), dOnesS, it + 1);
-        mma_commit_elect(smem_u32(&bars->s_full));
       }
-      if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
-      issue_acc(tDK, tDP, desc_mn(it, 0), it > 0);
-      mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
-      if (more) {
-        issue_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
+    } else {
+      // Two passes (d = 128), one issuing warp; software pipeline on the tensor pipe, per
+      // query tile it:
+      //   dV += P^T(it) dO_it  |  S^T(it+1)  |  dK += dS^T(it) Q_it  |  dP^T(it+1)
+      // dV needs only P^T, so it and the next S^T run while the element-wise warps form
+      // dS^T; the next element-wise step starts on S^T(it+1) while dK and dP^T(it+1) run.
+      // P^T is stored over S^T and dS^T over dP^T: each region is overwritten only after
+      // the product that reads it (issue order).  (Issuing dK and dP^T from a second warp,
+      // as the one-pass kernel does, lets dK overtake the next S^T and was slower here.)
+      if (ok) {
+        issue_t(tS, dK, desc_k(0, 0), dOnesS, 0);
+        mma_commit_elect(smem_u32(&bars->s_full));
+        issue_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
         mma_commit_elect(smem_u32(&bars->dp_full));
       }
-    }
+      for (int it = 0; ok && it < nq; ++it) {
+        const bool more = it + 1 < nq;
+        if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
+        issue_acc(tDV, tS, desc_mn(it, 1), it > 0);
+        if (more) {
+          if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
+                              ((it + 1) / Cfg::kStages) & 1)))
+            break;
+          issue_t(tS, dK, desc_k(it + 1, 0), dOnesS, it + 1);
+          mma_commit_elect(smem_u32(&bars->s_full));
+        }
+        if (!(ok = wait_bar(&bars->ds_ready, it & 1))) break;
+        issue_acc(tDK, tDP, desc_mn(it, 0), it > 0);
+        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
+        if (more) {
+          issue_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
+          mma_commit_elect(smem_u32(&bars->dp_full));
+        }
+      }
     }
     if (ok) mma_commit_elect(smem_u32(&bars->acc_final));
-    mma_commit_elect(smem_u32(&bars->mma_drain));
+    uint64_t* drain = second ? &bars->mma_drain2 : &bars->mma_drain;
+    mma_commit_elect(smem_u32(drain));
     int no_abort = 0;
-    bwd_wait(smem_u32(&bars->mma_drain), 0, &no_abort, p.status);
+    bwd_wait(smem_u32(drain), 0, &no_abort, p.status);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ element-wise warps
