@@ -595,7 +595,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // columns 32 h .. +31) goes through this warp's 32 x 32 fp32 staging box (128-byte
     // swizzle) into the accumulator by a TMA reduce-add.  Called once the partial is
     // known complete (dP^T of tile t + 1 seen, or the final commit).
-    auto reduce_dq = [&](int t) {
+    // One pass: the dQ partial of a query tile (TMEM lanes 32 wq .. +31 = its queries,
+    // columns 32 h .. +31) goes through this warp's 32 x 32 fp32 staging box (128-byte
+    // swizzle) into the accumulator by a TMA reduce-add, in two steps around the caller's
+    // fence.proxy.async: the partial into the box (once the partial is known complete and
+    // the box's previous reduce-add has read it), then the reduce-add of query tile t.
+    auto dq_to_box = [&]() {
       if constexpr (Fused) {
         uint32_t a[32];
         tmem_ld32_wait(tbase + lane_off + Cfg::kColDQ + 32 * h, a);
@@ -606,8 +611,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             sbase + Cfg::kSmemRed + warp * Cfg::kRedBoxBytes + lane * 128 + ((lane & 7) << 4);
         st_shared_swz4<0>(row, a);
         st_shared_swz4<4>(row, a + 16);
-        fence_proxy_async_smem();
-        __syncwarp();
+      }
+    };
+    auto box_to_acc = [&](int t) {
+      if constexpr (Fused) {
         if (lane == 0) {
           tma_reduce_add_3d(&tm_dqacc, sbase + Cfg::kSmemRed + warp * Cfg::kRedBoxBytes, 32 * h,
                             (i0 + t) * kBlockM + wq * 32, bh);
@@ -620,8 +627,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // (the next S^T may overwrite it), P; then, once dP^T(it) - D is in (which also
       // reports dV of tile it - 1 complete), P^T into its own columns, p_done; dP^T into
       // registers, "dP^T free"; once dK and dQ of tile it - 1 are complete (dq_done), its
-      // dQ partial drained, dS into the shared-memory staging, ds_ready.  The statistics
-      // came in through the tensor core, so these warps read nothing from the stages.
+      // dQ partial into the staging box, dS into the shared-memory staging, one proxy
+      // fence for both, the partial's reduce-add, ds_ready.  The statistics came in
+      // through the tensor core, so these warps read nothing from the stages.
       const uint32_t tP = tbase + lane_off + Cfg::kColP;
       for (int it = 0; ok && it < nq; ++it) {
         ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->s_full), it & 1, abort, p.status));
@@ -668,16 +676,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           bwd_wait(smem_u32(&bars->dq_done), (it - 1) & 1, abort, p.status));
           if (!ok) break;
           tc_fence_after();
-          reduce_dq(it - 1);
+          dq_to_box();
         }
         // Row r (this key) of box h: queries 64h .. 64h+63 are its 16-byte chunks 0 .. 7,
         // each at its 128-byte-swizzle position (chunk ^ (r % 8)).
         const uint32_t row = sbase + Cfg::kSmemDS + h * kBoxBytes + r * 128 + ((r & 7) << 4);
         st_shared_swz4<0>(row, pd);
         st_shared_swz4<4>(row, pd + 16);
-        fence_proxy_async_smem();  // dS is read by the tensor pipe
+        fence_proxy_async_smem();  // dS and the dQ box are read by the async proxy
         tc_fence_before();
         __syncwarp();
+        if (it > 0) box_to_acc(it - 1);
         if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
       }
     } else {
@@ -728,7 +737,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (Fused && ok) {
       tc_fence_after();
-      reduce_dq(nq - 1);
+      dq_to_box();
+      fence_proxy_async_smem();
+      __syncwarp();
+      box_to_acc(nq - 1);
     }
     const int kg = j * kBlockM + r;
     if (ok) {
