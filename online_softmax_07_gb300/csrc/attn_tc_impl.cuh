@@ -710,11 +710,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
+// The register hand-off of a 384-thread block (two warpgroups raised to kRegsSoftmax,
+// one lowered to kRegsIssue) draws on the registers the block was launched with: it needs
+// 168 a thread.  A kernel compiled with fewer would leave setmaxnreg.inc waiting for
+// registers that never come, so such a kernel is not launched.  Checked once per kernel.
+template <typename Kernel>
+cudaError_t check_register_split(Kernel kernel) {
+  cudaFuncAttributes a{};
+  cudaError_t e = cudaFuncGetAttributes(&a, kernel);
+  if (e != cudaSuccess) return e;
+  constexpr int kNeeded = 2 * 128 * kRegsSoftmax + 128 * kRegsIssue;
+  static_assert(kNeeded == kAttnThreads * 168, "the split hands over exactly 384 x 168");
+  return a.numRegs * kAttnThreads >= kNeeded ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 template <int D, int BN, bool F16>
 cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, const AttnTcParams& p, cudaStream_t stream) {
   using Cfg = AttnTcCfg<D, BN>;
   static_assert(sizeof(AttnTcBarriers) <= 512, "barrier block");
+  static const cudaError_t split_ok = check_register_split(attn_fwd_tc_kernel<D, BN, F16>);
+  if (split_ok != cudaSuccess) return split_ok;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, BN, F16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
