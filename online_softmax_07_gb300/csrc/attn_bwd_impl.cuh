@@ -977,6 +977,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int c0 = 64 * h + 32 * ch;   // first key (column) of this chunk
         uint32_t sr[32];
         tmem_ld32_wait(tS + c0, sr);
+        if (ch == 1 && it + 1 < nk) {  // S(it) is in registers: the next S may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
+        }
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float x0, x1;
@@ -990,11 +995,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           pv[16 * ch + (c >> 1)] = f2_pack(p0, p1);
         }
-      }
-      if (it + 1 < nk) {  // S(it) is in registers: the next S may overwrite it
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
       }
       // dS = P * (dP - D), stored (16-bit) over the first half of this warp's dP columns.
       ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
