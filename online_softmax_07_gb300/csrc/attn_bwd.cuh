@@ -73,7 +73,8 @@ struct AttnBwdCfg {
 
 // One-pass backward at d = 64 (the key-outer pass also forms dQ): each key-tile CTA
 // computes, per query tile i, the partial dQ_i += dS_ij K_j with a fifth tile product
-// (dS staged in shared memory, queries contiguous) into TMEM, and the element-wise warps
+// (dS staged in shared memory, where dK += dS^T Q_i reads it too) into TMEM, and the
+// element-wise warps
 // add it into an fp32 dQ accumulator in the workspace by TMA reduce-adds (element-wise
 // fp32 adds at L2), each warp its 32 x 32 share, during the next query tile (by then the
 // partial is complete).  A finalize launch
@@ -83,7 +84,7 @@ struct AttnBwdCfg {
 // sums (and at times its last bit after rounding) vary from run to run; dK and dV stay
 // deterministic.  Warp roles as in the two-pass kernels (a block of more than 384
 // threads would be compiled with 128 registers a thread, too few for the element-wise
-// warps).
+// warps), with warp 10 issuing dK and dQ beside the MMA warp.
 //
 // The row statistics enter through the tensor core instead of the element-wise warps:
 // every query row carries bf16 terms of -LSE/scale and of -D (a high and a low part each,

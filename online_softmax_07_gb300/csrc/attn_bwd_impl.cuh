@@ -472,44 +472,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit_elect(smem_u32(&bars->dq_done));
         }
       } else {
-      if (ok) {
-        group_t(tS, dK, desc_k(0, 0), dOnesS, 0);
-        mma_commit_elect(smem_u32(&bars->s_full));
-        group_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
-        mma_commit_elect(smem_u32(&bars->dp_full));
-      }
-      for (int it = 0; ok && it < nq; ++it) {
-        const bool more = it + 1 < nq;
-        if (more) {
-          if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
-                              ((it + 1) / Cfg::kStages) & 1) &&
-                     wait_bar(&bars->s_free, it & 1)))
-            break;
-          group_t(tS, dK, desc_k(it + 1, 0), dOnesS, it + 1);
+        if (ok) {
+          group_t(tS, dK, desc_k(0, 0), dOnesS, 0);
           mma_commit_elect(smem_u32(&bars->s_full));
-        }
-        if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
-        {
-          // dV += P^T(it) dO_it: A = 16 queries (8 packed columns) per step, the 64-query
-          // halves 32 columns apart.
-          uint32_t a[8];
-          uint64_t b[8];
-          const uint64_t dB = desc_mn(it, 1);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            a[kk] = tP + (kk >> 2) * 32 + (kk & 3) * 8;
-            b[kk] = dB + kk * 128;
-          }
-          mma_ts8_elect(tDV, a, b, kIdescAcc, it > 0 ? 1u : 0u);
-        }
-        // This warp's last product reading stage it.
-        mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
-        if (more) {
-          if (!(ok = wait_bar(&bars->dp_free, it & 1))) break;
-          group_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
+          group_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
           mma_commit_elect(smem_u32(&bars->dp_full));
         }
-      }
+        for (int it = 0; ok && it < nq; ++it) {
+          const bool more = it + 1 < nq;
+          if (more) {
+            if (!(ok = wait_bar(&bars->stage_full[(it + 1) % Cfg::kStages],
+                                ((it + 1) / Cfg::kStages) & 1) &&
+                       wait_bar(&bars->s_free, it & 1)))
+              break;
+            group_t(tS, dK, desc_k(it + 1, 0), dOnesS, it + 1);
+            mma_commit_elect(smem_u32(&bars->s_full));
+          }
+          if (!(ok = wait_bar(&bars->p_done, it & 1))) break;
+          {
+            // dV += P^T(it) dO_it: A = 16 queries (8 packed columns) per step, the 64-query
+            // halves 32 columns apart.
+            uint32_t a[8];
+            uint64_t b[8];
+            const uint64_t dB = desc_mn(it, 1);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              a[kk] = tP + (kk >> 2) * 32 + (kk & 3) * 8;
+              b[kk] = dB + kk * 128;
+            }
+            mma_ts8_elect(tDV, a, b, kIdescAcc, it > 0 ? 1u : 0u);
+          }
+          // This warp's last product reading stage it.
+          mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
+          if (more) {
+            if (!(ok = wait_bar(&bars->dp_free, it & 1))) break;
+            group_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
+            mma_commit_elect(smem_u32(&bars->dp_full));
+          }
+        }
       }
     } else {
       // Two passes (d = 128), one issuing warp; software pipeline on the tensor pipe, per
