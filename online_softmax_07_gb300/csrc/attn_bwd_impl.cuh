@@ -59,6 +59,41 @@ __device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, volatile
   return done != 0 || mbar_wait(bar, parity, abort, status);
 }
 
+// Issues the load of 32 lanes x 32 TMEM columns (taddr) into d[], stores the 32 words
+// of v[] as eight 16-byte chunks of a 128-byte-swizzled row (`base` = row address plus
+// the row's swizzle offset, as for st_shared_swz4) while the load is in flight, then
+// waits for the load.  The outputs are early-clobber: the load may land before the
+// stores have read v[].
+__device__ __forceinline__ void tmem_ld32_st_swz8_wait(uint32_t taddr, uint32_t* d, uint32_t base,
+                                                       const uint32_t* v) {
+  asm volatile(
+      "{\n\t.reg .b32 a;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];\n\t"
+      "xor.b32 a, %33, 0;\n\tst.shared.v4.b32 [a], {%34, %35, %36, %37};\n\t"
+      "xor.b32 a, %33, 16;\n\tst.shared.v4.b32 [a], {%38, %39, %40, %41};\n\t"
+      "xor.b32 a, %33, 32;\n\tst.shared.v4.b32 [a], {%42, %43, %44, %45};\n\t"
+      "xor.b32 a, %33, 48;\n\tst.shared.v4.b32 [a], {%46, %47, %48, %49};\n\t"
+      "xor.b32 a, %33, 64;\n\tst.shared.v4.b32 [a], {%50, %51, %52, %53};\n\t"
+      "xor.b32 a, %33, 80;\n\tst.shared.v4.b32 [a], {%54, %55, %56, %57};\n\t"
+      "xor.b32 a, %33, 96;\n\tst.shared.v4.b32 [a], {%58, %59, %60, %61};\n\t"
+      "xor.b32 a, %33, 112;\n\tst.shared.v4.b32 [a], {%62, %63, %64, %65};\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t}"
+      : "=&r"(d[0]), "=&r"(d[1]), "=&r"(d[2]), "=&r"(d[3]), "=&r"(d[4]), "=&r"(d[5]),
+        "=&r"(d[6]), "=&r"(d[7]), "=&r"(d[8]), "=&r"(d[9]), "=&r"(d[10]), "=&r"(d[11]),
+        "=&r"(d[12]), "=&r"(d[13]), "=&r"(d[14]), "=&r"(d[15]), "=&r"(d[16]), "=&r"(d[17]),
+        "=&r"(d[18]), "=&r"(d[19]), "=&r"(d[20]), "=&r"(d[21]), "=&r"(d[22]), "=&r"(d[23]),
+        "=&r"(d[24]), "=&r"(d[25]), "=&r"(d[26]), "=&r"(d[27]), "=&r"(d[28]), "=&r"(d[29]),
+        "=&r"(d[30]), "=&r"(d[31])
+      : "r"(taddr), "r"(base), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]),
+        "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
+        "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]),
+        "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major operand with 32-byte swizzle (rows of 16
 // 16-bit elements; 8-row groups 256 bytes apart): swizzle mode 6 at bits 61-63.
 __device__ __forceinline__ uint64_t desc_sw32(uint32_t saddr) {
@@ -671,18 +706,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (lane == 0) mbar_arrive(smem_u32(&bars->dp_free));
           ds_chunk(dr, pv + 16, pd + 16);
         }
+        // Row r (this key) of box h: queries 64h .. 64h+63 are its 16-byte chunks 0 .. 7,
+        // each at its 128-byte-swizzle position (chunk ^ (r % 8)).
+        const uint32_t row = sbase + Cfg::kSmemDS + h * kBoxBytes + r * 128 + ((r & 7) << 4);
         if (it > 0) {
           ok = __all_sync(0xffffffffu,
                           bwd_wait(smem_u32(&bars->dq_done), (it - 1) & 1, abort, p.status));
           if (!ok) break;
           tc_fence_after();
-          dq_to_box();
+          // The dQ partial of tile it - 1 is loaded while dS goes to the staging, then
+          // goes to this warp's box.
+          uint32_t a[32];
+          tmem_ld32_st_swz8_wait(tbase + lane_off + Cfg::kColDQ + 32 * h, a, row, pd);
+          tc_fence_before();
+          if (lane == 0) bulk_wait_group_read_0();  // the last reduce-add has read the box
+          __syncwarp();
+          const uint32_t rrow =
+              sbase + Cfg::kSmemRed + warp * Cfg::kRedBoxBytes + lane * 128 + ((lane & 7) << 4);
+          st_shared_swz4<0>(rrow, a);
+          st_shared_swz4<4>(rrow, a + 16);
+        } else {
+          st_shared_swz4<0>(row, pd);
+          st_shared_swz4<4>(row, pd + 16);
         }
-        // Row r (this key) of box h: queries 64h .. 64h+63 are its 16-byte chunks 0 .. 7,
-        // each at its 128-byte-swizzle position (chunk ^ (r % 8)).
-        const uint32_t row = sbase + Cfg::kSmemDS + h * kBoxBytes + r * 128 + ((r & 7) << 4);
-        st_shared_swz4<0>(row, pd);
-        st_shared_swz4<4>(row, pd + 16);
         fence_proxy_async_smem();  // dS and the dQ box are read by the async proxy
         tc_fence_before();
         __syncwarp();
