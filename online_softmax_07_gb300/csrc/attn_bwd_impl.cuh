@@ -94,6 +94,133 @@ __device__ __forceinline__ void tmem_ld32_st_swz8_wait(uint32_t taddr, uint32_t*
       : "memory");
 }
 
+// Issues the load of 32 lanes x 32 TMEM columns (taddr) into d[] and, while it is in
+// flight, forms P of the 32 scores in s[] (already loaded): x = s * scale log2(e) on pairs,
+// p = exp2(x), pv[i] = the fp32 pair (p_2i, p_2i+1) and pk[i] the same pair in the
+// kernel's 16-bit type; then waits for the load.  All outputs are early-clobber: the load
+// may land, and pv / pk are written, while s[] is still being read.
+template <bool F16>
+__device__ __forceinline__ void tmem_ld32_exp_chunk(uint32_t taddr, uint32_t* d, const uint32_t* s,
+                                                    uint64_t sl2x2, uint64_t* pv, uint32_t* pk) {
+  if constexpr (F16) {
+#define CVT "cvt.rn.f16x2.f32"
+    asm volatile(
+        "{\n\t.reg .b64 t;\n\t.reg .f32 x0, x1, q0, q1;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+        "mov.b64 t, {%66, %67};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %32, {q0, q1};\n\t" CVT " %48, q1, q0;\n\t"
+        "mov.b64 t, {%68, %69};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %33, {q0, q1};\n\t" CVT " %49, q1, q0;\n\t"
+        "mov.b64 t, {%70, %71};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %34, {q0, q1};\n\t" CVT " %50, q1, q0;\n\t"
+        "mov.b64 t, {%72, %73};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %35, {q0, q1};\n\t" CVT " %51, q1, q0;\n\t"
+        "mov.b64 t, {%74, %75};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %36, {q0, q1};\n\t" CVT " %52, q1, q0;\n\t"
+        "mov.b64 t, {%76, %77};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %37, {q0, q1};\n\t" CVT " %53, q1, q0;\n\t"
+        "mov.b64 t, {%78, %79};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %38, {q0, q1};\n\t" CVT " %54, q1, q0;\n\t"
+        "mov.b64 t, {%80, %81};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %39, {q0, q1};\n\t" CVT " %55, q1, q0;\n\t"
+        "mov.b64 t, {%82, %83};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %40, {q0, q1};\n\t" CVT " %56, q1, q0;\n\t"
+        "mov.b64 t, {%84, %85};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %41, {q0, q1};\n\t" CVT " %57, q1, q0;\n\t"
+        "mov.b64 t, {%86, %87};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %42, {q0, q1};\n\t" CVT " %58, q1, q0;\n\t"
+        "mov.b64 t, {%88, %89};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %43, {q0, q1};\n\t" CVT " %59, q1, q0;\n\t"
+        "mov.b64 t, {%90, %91};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %44, {q0, q1};\n\t" CVT " %60, q1, q0;\n\t"
+        "mov.b64 t, {%92, %93};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %45, {q0, q1};\n\t" CVT " %61, q1, q0;\n\t"
+        "mov.b64 t, {%94, %95};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %46, {q0, q1};\n\t" CVT " %62, q1, q0;\n\t"
+        "mov.b64 t, {%96, %97};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %47, {q0, q1};\n\t" CVT " %63, q1, q0;\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t}"
+        : "=&r"(d[0]), "=&r"(d[1]), "=&r"(d[2]), "=&r"(d[3]), "=&r"(d[4]), "=&r"(d[5]), "=&r"(d[6]), "=&r"(d[7]), "=&r"(d[8]), "=&r"(d[9]), "=&r"(d[10]), "=&r"(d[11]), "=&r"(d[12]), "=&r"(d[13]), "=&r"(d[14]), "=&r"(d[15]), "=&r"(d[16]), "=&r"(d[17]), "=&r"(d[18]), "=&r"(d[19]), "=&r"(d[20]), "=&r"(d[21]), "=&r"(d[22]), "=&r"(d[23]), "=&r"(d[24]), "=&r"(d[25]), "=&r"(d[26]), "=&r"(d[27]), "=&r"(d[28]), "=&r"(d[29]), "=&r"(d[30]), "=&r"(d[31]), "=&l"(pv[0]), "=&l"(pv[1]), "=&l"(pv[2]), "=&l"(pv[3]), "=&l"(pv[4]), "=&l"(pv[5]), "=&l"(pv[6]), "=&l"(pv[7]), "=&l"(pv[8]), "=&l"(pv[9]), "=&l"(pv[10]), "=&l"(pv[11]), "=&l"(pv[12]), "=&l"(pv[13]), "=&l"(pv[14]), "=&l"(pv[15]), "=&r"(pk[0]), "=&r"(pk[1]), "=&r"(pk[2]), "=&r"(pk[3]), "=&r"(pk[4]), "=&r"(pk[5]), "=&r"(pk[6]), "=&r"(pk[7]), "=&r"(pk[8]), "=&r"(pk[9]), "=&r"(pk[10]), "=&r"(pk[11]), "=&r"(pk[12]), "=&r"(pk[13]), "=&r"(pk[14]), "=&r"(pk[15])
+        : "r"(taddr), "l"(sl2x2), "r"(s[0]), "r"(s[1]), "r"(s[2]), "r"(s[3]), "r"(s[4]), "r"(s[5]), "r"(s[6]), "r"(s[7]), "r"(s[8]), "r"(s[9]), "r"(s[10]), "r"(s[11]), "r"(s[12]), "r"(s[13]), "r"(s[14]), "r"(s[15]), "r"(s[16]), "r"(s[17]), "r"(s[18]), "r"(s[19]), "r"(s[20]), "r"(s[21]), "r"(s[22]), "r"(s[23]), "r"(s[24]), "r"(s[25]), "r"(s[26]), "r"(s[27]), "r"(s[28]), "r"(s[29]), "r"(s[30]), "r"(s[31])
+        : "memory");
+#undef CVT
+  } else {
+#define CVT "cvt.rn.bf16x2.f32"
+    asm volatile(
+        "{\n\t.reg .b64 t;\n\t.reg .f32 x0, x1, q0, q1;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+        "mov.b64 t, {%66, %67};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %32, {q0, q1};\n\t" CVT " %48, q1, q0;\n\t"
+        "mov.b64 t, {%68, %69};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %33, {q0, q1};\n\t" CVT " %49, q1, q0;\n\t"
+        "mov.b64 t, {%70, %71};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %34, {q0, q1};\n\t" CVT " %50, q1, q0;\n\t"
+        "mov.b64 t, {%72, %73};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %35, {q0, q1};\n\t" CVT " %51, q1, q0;\n\t"
+        "mov.b64 t, {%74, %75};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %36, {q0, q1};\n\t" CVT " %52, q1, q0;\n\t"
+        "mov.b64 t, {%76, %77};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %37, {q0, q1};\n\t" CVT " %53, q1, q0;\n\t"
+        "mov.b64 t, {%78, %79};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %38, {q0, q1};\n\t" CVT " %54, q1, q0;\n\t"
+        "mov.b64 t, {%80, %81};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %39, {q0, q1};\n\t" CVT " %55, q1, q0;\n\t"
+        "mov.b64 t, {%82, %83};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %40, {q0, q1};\n\t" CVT " %56, q1, q0;\n\t"
+        "mov.b64 t, {%84, %85};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %41, {q0, q1};\n\t" CVT " %57, q1, q0;\n\t"
+        "mov.b64 t, {%86, %87};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %42, {q0, q1};\n\t" CVT " %58, q1, q0;\n\t"
+        "mov.b64 t, {%88, %89};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %43, {q0, q1};\n\t" CVT " %59, q1, q0;\n\t"
+        "mov.b64 t, {%90, %91};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %44, {q0, q1};\n\t" CVT " %60, q1, q0;\n\t"
+        "mov.b64 t, {%92, %93};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %45, {q0, q1};\n\t" CVT " %61, q1, q0;\n\t"
+        "mov.b64 t, {%94, %95};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %46, {q0, q1};\n\t" CVT " %62, q1, q0;\n\t"
+        "mov.b64 t, {%96, %97};\n\tmul.rn.f32x2 t, t, %65;\n\tmov.b64 {x0, x1}, t;\n\t"
+        "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\t"
+        "mov.b64 %47, {q0, q1};\n\t" CVT " %63, q1, q0;\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t}"
+        : "=&r"(d[0]), "=&r"(d[1]), "=&r"(d[2]), "=&r"(d[3]), "=&r"(d[4]), "=&r"(d[5]), "=&r"(d[6]), "=&r"(d[7]), "=&r"(d[8]), "=&r"(d[9]), "=&r"(d[10]), "=&r"(d[11]), "=&r"(d[12]), "=&r"(d[13]), "=&r"(d[14]), "=&r"(d[15]), "=&r"(d[16]), "=&r"(d[17]), "=&r"(d[18]), "=&r"(d[19]), "=&r"(d[20]), "=&r"(d[21]), "=&r"(d[22]), "=&r"(d[23]), "=&r"(d[24]), "=&r"(d[25]), "=&r"(d[26]), "=&r"(d[27]), "=&r"(d[28]), "=&r"(d[29]), "=&r"(d[30]), "=&r"(d[31]), "=&l"(pv[0]), "=&l"(pv[1]), "=&l"(pv[2]), "=&l"(pv[3]), "=&l"(pv[4]), "=&l"(pv[5]), "=&l"(pv[6]), "=&l"(pv[7]), "=&l"(pv[8]), "=&l"(pv[9]), "=&l"(pv[10]), "=&l"(pv[11]), "=&l"(pv[12]), "=&l"(pv[13]), "=&l"(pv[14]), "=&l"(pv[15]), "=&r"(pk[0]), "=&r"(pk[1]), "=&r"(pk[2]), "=&r"(pk[3]), "=&r"(pk[4]), "=&r"(pk[5]), "=&r"(pk[6]), "=&r"(pk[7]), "=&r"(pk[8]), "=&r"(pk[9]), "=&r"(pk[10]), "=&r"(pk[11]), "=&r"(pk[12]), "=&r"(pk[13]), "=&r"(pk[14]), "=&r"(pk[15])
+        : "r"(taddr), "l"(sl2x2), "r"(s[0]), "r"(s[1]), "r"(s[2]), "r"(s[3]), "r"(s[4]), "r"(s[5]), "r"(s[6]), "r"(s[7]), "r"(s[8]), "r"(s[9]), "r"(s[10]), "r"(s[11]), "r"(s[12]), "r"(s[13]), "r"(s[14]), "r"(s[15]), "r"(s[16]), "r"(s[17]), "r"(s[18]), "r"(s[19]), "r"(s[20]), "r"(s[21]), "r"(s[22]), "r"(s[23]), "r"(s[24]), "r"(s[25]), "r"(s[26]), "r"(s[27]), "r"(s[28]), "r"(s[29]), "r"(s[30]), "r"(s[31])
+        : "memory");
+#undef CVT
+  }
+}
+
 // Shared-memory matrix descriptor of a K-major operand with 32-byte swizzle (rows of 16
 // 16-bit elements; 8-row groups 256 bytes apart): swizzle mode 6 at bits 61-63.
 __device__ __forceinline__ uint64_t desc_sw32(uint32_t saddr) {
@@ -673,16 +800,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool diag = p.causal && i0 + it == j;
         uint64_t pv[32];
         uint32_t pk[32];
+        if (!diag) {
+          // The second half of this warp's S^T loads while P of the first half is formed.
+          uint32_t sr0[32], sr1[32];
+          tmem_ld32_wait(tS + 64 * h, sr0);
+          tmem_ld32_exp_chunk<F16>(tS + 64 * h + 32, sr1, sr0, sl2x2, pv, pk);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
+          p_chunk(sr1, 64 * h + 32, false, pv + 16, pk + 16);
+        } else {
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t sr[32];
-          tmem_ld32_wait(tS + 64 * h + 32 * ch, sr);
-          if (ch == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t sr[32];
+            tmem_ld32_wait(tS + 64 * h + 32 * ch, sr);
+            if (ch == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
+            }
+            p_chunk(sr, 64 * h + 32 * ch, true, pv + 16 * ch, pk + 16 * ch);
           }
-          p_chunk(sr, 64 * h + 32 * ch, diag, pv + 16 * ch, pk + 16 * ch);
         }
         ok = __all_sync(0xffffffffu, bwd_wait(smem_u32(&bars->dp_full), it & 1, abort, p.status));
         if (!ok) break;
