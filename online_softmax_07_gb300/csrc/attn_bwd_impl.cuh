@@ -885,13 +885,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P^T: kept in registers for dS^T and stored (16-bit) over the first half of this
       // warp's S^T columns for dV.
       uint64_t pv[32];
+      if (!diag) {
+        // The second half of this warp's S^T loads while P of the first half is formed.
+        uint32_t sr0[32], sr1[32], pk[16];
+        tmem_ld32_wait(tS + 64 * h, sr0);
+        tmem_ld32_exp_chunk<F16>(tS + 64 * h + 32, sr1, sr0, sl2x2, pv, pk);
+        tmem_st16(tS + 64 * h, pk);
+        p_chunk(sr1, 64 * h + 32, false, pv + 16, pk);
+        tmem_st16(tS + 64 * h + 16, pk);
+      } else {
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = 64 * h + 32 * ch;    // first query (column) of this chunk
-        uint32_t sr[32], pk[16];
-        tmem_ld32_wait(tS + c0, sr);
-        p_chunk(sr, c0, diag, pv + 16 * ch, pk);
-        tmem_st16(tS + 64 * h + 16 * ch, pk);
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = 64 * h + 32 * ch;    // first query (column) of this chunk
+          uint32_t sr[32], pk[16];
+          tmem_ld32_wait(tS + c0, sr);
+          p_chunk(sr, c0, true, pv + 16 * ch, pk);
+          tmem_st16(tS + 64 * h + 16 * ch, pk);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
