@@ -221,6 +221,53 @@ __device__ __forceinline__ void tmem_ld32_exp_chunk(uint32_t taddr, uint32_t* d,
   }
 }
 
+// Issues the load of 32 lanes x 32 TMEM columns (taddr) into d[] and, while it is in
+// flight, forms P of the 32 scores in s[] (already loaded) with the row's statistic:
+// pv[i] = exp2(s * scale log2(e) - LSE log2(e)) of the pair, fp32; then waits for the
+// load.  All outputs are early-clobber.
+__device__ __forceinline__ void tmem_ld32_exp_lse_chunk(uint32_t taddr, uint32_t* d, const uint32_t* s,
+                                                        uint64_t sl2x2, uint64_t negl2, uint64_t* pv) {
+  asm volatile(
+      "{\n\t.reg .b64 t;\n\t.reg .f32 x0, x1, q0, q1;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%48];\n\t"
+      "mov.b64 t, {%51, %52};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %32, {q0, q1};\n\t"
+      "mov.b64 t, {%53, %54};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %33, {q0, q1};\n\t"
+      "mov.b64 t, {%55, %56};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %34, {q0, q1};\n\t"
+      "mov.b64 t, {%57, %58};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %35, {q0, q1};\n\t"
+      "mov.b64 t, {%59, %60};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %36, {q0, q1};\n\t"
+      "mov.b64 t, {%61, %62};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %37, {q0, q1};\n\t"
+      "mov.b64 t, {%63, %64};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %38, {q0, q1};\n\t"
+      "mov.b64 t, {%65, %66};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %39, {q0, q1};\n\t"
+      "mov.b64 t, {%67, %68};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %40, {q0, q1};\n\t"
+      "mov.b64 t, {%69, %70};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %41, {q0, q1};\n\t"
+      "mov.b64 t, {%71, %72};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %42, {q0, q1};\n\t"
+      "mov.b64 t, {%73, %74};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %43, {q0, q1};\n\t"
+      "mov.b64 t, {%75, %76};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %44, {q0, q1};\n\t"
+      "mov.b64 t, {%77, %78};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %45, {q0, q1};\n\t"
+      "mov.b64 t, {%79, %80};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %46, {q0, q1};\n\t"
+      "mov.b64 t, {%81, %82};\n\tfma.rn.f32x2 t, t, %49, %50;\n\tmov.b64 {x0, x1}, t;\n\t"
+      "ex2.approx.ftz.f32 q0, x0;\n\tex2.approx.ftz.f32 q1, x1;\n\tmov.b64 %47, {q0, q1};\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t}"
+      : "=&r"(d[0]), "=&r"(d[1]), "=&r"(d[2]), "=&r"(d[3]), "=&r"(d[4]), "=&r"(d[5]), "=&r"(d[6]), "=&r"(d[7]), "=&r"(d[8]), "=&r"(d[9]), "=&r"(d[10]), "=&r"(d[11]), "=&r"(d[12]), "=&r"(d[13]), "=&r"(d[14]), "=&r"(d[15]), "=&r"(d[16]), "=&r"(d[17]), "=&r"(d[18]), "=&r"(d[19]), "=&r"(d[20]), "=&r"(d[21]), "=&r"(d[22]), "=&r"(d[23]), "=&r"(d[24]), "=&r"(d[25]), "=&r"(d[26]), "=&r"(d[27]), "=&r"(d[28]), "=&r"(d[29]), "=&r"(d[30]), "=&r"(d[31]), "=&l"(pv[0]), "=&l"(pv[1]), "=&l"(pv[2]), "=&l"(pv[3]), "=&l"(pv[4]), "=&l"(pv[5]), "=&l"(pv[6]), "=&l"(pv[7]), "=&l"(pv[8]), "=&l"(pv[9]), "=&l"(pv[10]), "=&l"(pv[11]), "=&l"(pv[12]), "=&l"(pv[13]), "=&l"(pv[14]), "=&l"(pv[15])
+      : "r"(taddr), "l"(sl2x2), "l"(negl2), "r"(s[0]), "r"(s[1]), "r"(s[2]), "r"(s[3]), "r"(s[4]), "r"(s[5]), "r"(s[6]), "r"(s[7]), "r"(s[8]), "r"(s[9]), "r"(s[10]), "r"(s[11]), "r"(s[12]), "r"(s[13]), "r"(s[14]), "r"(s[15]), "r"(s[16]), "r"(s[17]), "r"(s[18]), "r"(s[19]), "r"(s[20]), "r"(s[21]), "r"(s[22]), "r"(s[23]), "r"(s[24]), "r"(s[25]), "r"(s[26]), "r"(s[27]), "r"(s[28]), "r"(s[29]), "r"(s[30]), "r"(s[31])
+      : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major operand with 32-byte swizzle (rows of 16
 // 16-bit elements; 8-row groups 256 bytes apart): swizzle mode 6 at bits 61-63.
 __device__ __forceinline__ uint64_t desc_sw32(uint32_t saddr) {
@@ -1166,12 +1213,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (p.causal) lim = min(lim, qg - key0);
       // P = exp2(S * scale * log2 e - LSE * log2 e), in registers.
       uint64_t pv[32];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = 64 * h + 32 * ch;   // first key (column) of this chunk
+      if (!need_mask) {
+        // The second half of this warp's S loads while P of the first half is formed.
+        uint32_t sr0[32];
+        tmem_ld32_wait(tS + 64 * h, sr0);
         uint32_t sr[32];
-        tmem_ld32_wait(tS + c0, sr);
-        if (ch == 1 && it + 1 < nk) {  // S(it) is in registers: the next S may overwrite it
+        tmem_ld32_exp_lse_chunk(tS + 64 * h + 32, sr, sr0, sl2x2, negl2, pv);
+        if (it + 1 < nk) {  // S(it) is in registers: the next S may overwrite it
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
@@ -1182,12 +1230,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
                            negl2),
                     x0, x1);
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if (need_mask) {
-            if (c0 + c > lim) p0 = 0.f;
-            if (c0 + c + 1 > lim) p1 = 0.f;
+          pv[16 + (c >> 1)] = f2_pack(ex2_approx(x0), ex2_approx(x1));
+        }
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = 64 * h + 32 * ch;   // first key (column) of this chunk
+          uint32_t sr[32];
+          tmem_ld32_wait(tS + c0, sr);
+          if (ch == 1 && it + 1 < nk) {  // S(it) is in registers: the next S may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->p_done));
           }
-          pv[16 * ch + (c >> 1)] = f2_pack(p0, p1);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
+                             negl2),
+                      x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (need_mask) {
+              if (c0 + c > lim) p0 = 0.f;
+              if (c0 + c + 1 > lim) p1 = 0.f;
+            }
+            pv[16 * ch + (c >> 1)] = f2_pack(p0, p1);
+          }
         }
       }
       // dS = P * (dP - D), stored (16-bit) over the first half of this warp's dP columns.
