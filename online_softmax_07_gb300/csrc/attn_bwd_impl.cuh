@@ -21,7 +21,9 @@ struct AttnBwdBarriers {
   uint64_t acc_final;    // MMA -> element-wise: the last accumulation finished
   uint64_t mma_drain;    // MMA warp: all of its MMAs finished (before TMEM is freed)
   uint64_t mma_drain2;   // one pass: the same for the second MMA warp
-  uint64_t stage_full[4];   // key-outer: Q_i, dO_i stages; query-outer: the K ring
+  uint64_t stage_full[4];   // key-outer: Q_i and its statistics terms; query-outer: the K ring
+  uint64_t stage_do_full[4];  // key-outer: dO_i of the stage (loaded after Q_i: S^T needs
+                              // only Q_i and the terms, dP^T and dV need dO_i)
   uint64_t stage_empty[4];
   uint64_t v_full[4];       // query-outer: the V ring
   uint64_t v_empty[4];
@@ -492,6 +494,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&bars->mma_drain2), 1);
     for (int s = 0; s < Cfg::kStages; ++s) {
       mbar_init(smem_u32(&bars->stage_full[s]), 1);
+      mbar_init(smem_u32(&bars->stage_do_full[s]), 1);
       mbar_init(smem_u32(&bars->stage_empty[s]), Fused ? 2 : 1);
     }
     mbar_init(smem_u32(&bars->s_free), 8);
@@ -543,23 +546,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        p.status))
           break;
         const uint32_t full = smem_u32(&bars->stage_full[s]);
+        const uint32_t do_full = smem_u32(&bars->stage_do_full[s]);
         const int i = i0 + it;
         const uint32_t dst = stage_addr(s);
-        mbar_arrive_expect_tx(full, Cfg::kStageBytes);
+        // Q_i and the terms first (the next S^T waits for them alone), then dO_i.
+        mbar_arrive_expect_tx(full, Cfg::kTileBytes + Cfg::kAugBytes);
 #pragma unroll
-        for (int b = 0; b < Cfg::kBoxes; ++b) {
+        for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_load_3d(dst + b * kBoxBytes, &tm_q, full, b * kBoxCols, i * kBlockM, bh);
-          tma_load_3d(dst + Cfg::kTileBytes + b * kBoxBytes, &tm_do, full, b * kBoxCols, i * kBlockM, bh);
-        }
         tma_load_3d(dst + 2 * Cfg::kTileBytes, &tm_aug, full, 0, i * kBlockM, bh);
+        mbar_arrive_expect_tx(do_full, Cfg::kTileBytes);
+#pragma unroll
+        for (int b = 0; b < Cfg::kBoxes; ++b)
+          tma_load_3d(dst + Cfg::kTileBytes + b * kBoxBytes, &tm_do, do_full, b * kBoxCols,
+                      i * kBlockM, bh);
         issued = it + 1;
       }
       // Every issued copy must land before the block's shared memory goes away.
       int no_abort = 0;
       bwd_wait(fbar, 0, &no_abort, p.status);
-      for (int it = max(0, issued - Cfg::kStages); it < issued; ++it)
+      for (int it = max(0, issued - Cfg::kStages); it < issued; ++it) {
         bwd_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]), (it / Cfg::kStages) & 1,
                   &no_abort, p.status);
+        bwd_wait(smem_u32(&bars->stage_do_full[it % Cfg::kStages]), (it / Cfg::kStages) & 1,
+                 &no_abort, p.status);
+      }
     }
   } else if (warp == kBwdWarpMma || (Fused && warp == kBwdWarpMma2)) {
     // ------------------------------------------------------------ MMA issuers
@@ -615,7 +626,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           (acc || kk > 0) ? 1u : 0u);
       }
     };
-    bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0);
+    bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0) &&
+              wait_bar(&bars->stage_do_full[0], 0);
+    auto wait_do = [&](int it) {  // dO_it has landed
+      return wait_bar(&bars->stage_do_full[it % Cfg::kStages], (it / Cfg::kStages) & 1);
+    };
     if constexpr (Fused) {
       // One pass (d = 64).  The first warp issues, per query tile it,
       //   S^T(it+1) (once the element-wise warps hold S^T(it) in registers)  |
@@ -714,7 +729,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // This warp's last product reading stage it.
           mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
           if (more) {
-            if (!(ok = wait_bar(&bars->dp_free, it & 1))) break;
+            if (!(ok = wait_bar(&bars->dp_free, it & 1) && wait_do(it + 1))) break;
             group_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
             mma_commit_elect(smem_u32(&bars->dp_full));
           }
@@ -750,6 +765,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         issue_acc(tDK, tDP, desc_mn(it, 0), it > 0);
         mma_commit_elect(smem_u32(&bars->stage_empty[it % Cfg::kStages]));
         if (more) {
+          if (!(ok = wait_do(it + 1))) break;
           issue_t(tDP, dV, desc_k(it + 1, 1), dOnesD, it + 1);
           mma_commit_elect(smem_u32(&bars->dp_full));
         }
