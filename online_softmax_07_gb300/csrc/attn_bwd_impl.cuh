@@ -13,7 +13,9 @@
 namespace osfa {
 
 struct AttnBwdBarriers {
-  uint64_t fixed_full;   // TMA -> all: the two resident tiles are in shared memory
+  uint64_t fixed_full;   // TMA -> all: the first resident tile (K_j, or Q_i) is in shared memory
+  uint64_t fixed1_full;  // ... and the second (V_j, or dO_i), loaded after the first stage's
+                         // first tile, which the first product needs with the first one
   uint64_t s_full;       // MMA -> element-wise: S (or S^T) of a tile pair in TMEM
   uint64_t dp_full;      // MMA -> element-wise: dP (or dP^T) in TMEM
   uint64_t p_done;       // element-wise -> MMA: P^T stored (key-outer) / S read (query-outer)
@@ -484,6 +486,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->fixed_full), 1);
+    mbar_init(smem_u32(&bars->fixed1_full), 1);
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->dp_full), 1);
     mbar_init(smem_u32(&bars->p_done), 8);    // one arrival per element-wise warp
@@ -532,13 +535,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
+      // K_j, then Q_i0 and its terms (all the first S^T needs), then V_j, then dO_i0, ...
       const uint32_t fbar = smem_u32(&bars->fixed_full);
-      mbar_arrive_expect_tx(fbar, 2 * Cfg::kTileBytes);
+      const uint32_t fbar1 = smem_u32(&bars->fixed1_full);
+      mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
 #pragma unroll
-      for (int b = 0; b < Cfg::kBoxes; ++b) {
+      for (int b = 0; b < Cfg::kBoxes; ++b)
         tma_load_3d(sbase + Cfg::kSmemFixed0 + b * kBoxBytes, &tm_k, fbar, b * kBoxCols, j * kBlockM, bh);
-        tma_load_3d(sbase + Cfg::kSmemFixed1 + b * kBoxBytes, &tm_v, fbar, b * kBoxCols, j * kBlockM, bh);
-      }
+      auto load_v = [&]() {
+        mbar_arrive_expect_tx(fbar1, Cfg::kTileBytes);
+#pragma unroll
+        for (int b = 0; b < Cfg::kBoxes; ++b)
+          tma_load_3d(sbase + Cfg::kSmemFixed1 + b * kBoxBytes, &tm_v, fbar1, b * kBoxCols,
+                      j * kBlockM, bh);
+      };
+      bool v_issued = false;
       int issued = 0;
       for (int it = 0; it < nq; ++it) {
         const int s = it % Cfg::kStages;
@@ -555,6 +566,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_load_3d(dst + b * kBoxBytes, &tm_q, full, b * kBoxCols, i * kBlockM, bh);
         tma_load_3d(dst + 2 * Cfg::kTileBytes, &tm_aug, full, 0, i * kBlockM, bh);
+        if (!v_issued) {
+          load_v();
+          v_issued = true;
+        }
         mbar_arrive_expect_tx(do_full, Cfg::kTileBytes);
 #pragma unroll
         for (int b = 0; b < Cfg::kBoxes; ++b)
@@ -565,6 +580,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Every issued copy must land before the block's shared memory goes away.
       int no_abort = 0;
       bwd_wait(fbar, 0, &no_abort, p.status);
+      if (v_issued) bwd_wait(fbar1, 0, &no_abort, p.status);
       for (int it = max(0, issued - Cfg::kStages); it < issued; ++it) {
         bwd_wait(smem_u32(&bars->stage_full[it % Cfg::kStages]), (it / Cfg::kStages) & 1,
                   &no_abort, p.status);
@@ -626,10 +642,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           (acc || kk > 0) ? 1u : 0u);
       }
     };
-    bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0) &&
-              wait_bar(&bars->stage_do_full[0], 0);
+    bool ok = wait_bar(&bars->fixed_full, 0) && wait_bar(&bars->stage_full[0], 0);
     auto wait_do = [&](int it) {  // dO_it has landed
       return wait_bar(&bars->stage_do_full[it % Cfg::kStages], (it / Cfg::kStages) & 1);
+    };
+    auto wait_v_do0 = [&]() {  // V_j and dO of the first query tile have landed
+      return wait_bar(&bars->fixed1_full, 0) && wait_do(0);
     };
     if constexpr (Fused) {
       // One pass (d = 64).  The first warp issues, per query tile it,
@@ -699,8 +717,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) {
           group_t(tS, dK, desc_k(0, 0), dOnesS, 0);
           mma_commit_elect(smem_u32(&bars->s_full));
-          group_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
-          mma_commit_elect(smem_u32(&bars->dp_full));
+          if ((ok = wait_v_do0())) {
+            group_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
+            mma_commit_elect(smem_u32(&bars->dp_full));
+          }
         }
         for (int it = 0; ok && it < nq; ++it) {
           const bool more = it + 1 < nq;
@@ -747,8 +767,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) {
         issue_t(tS, dK, desc_k(0, 0), dOnesS, 0);
         mma_commit_elect(smem_u32(&bars->s_full));
-        issue_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
-        mma_commit_elect(smem_u32(&bars->dp_full));
+        if ((ok = wait_v_do0())) {
+          issue_t(tDP, dV, desc_k(0, 1), dOnesD, 0);
+          mma_commit_elect(smem_u32(&bars->dp_full));
+        }
       }
       for (int it = 0; ok && it < nq; ++it) {
         const bool more = it + 1 < nq;
@@ -1053,6 +1075,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->fixed_full), 1);
+    mbar_init(smem_u32(&bars->fixed1_full), 1);
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->dp_full), 1);
     mbar_init(smem_u32(&bars->p_done), 8);    // one arrival per element-wise warp
@@ -1092,13 +1115,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
+      // Q_i, then K_0 (all the first S needs), then dO_i, then V_0, K_1, V_1, ...
       const uint32_t fbar = smem_u32(&bars->fixed_full);
-      mbar_arrive_expect_tx(fbar, 2 * Cfg::kTileBytes);
+      const uint32_t fbar1 = smem_u32(&bars->fixed1_full);
+      mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
 #pragma unroll
-      for (int b = 0; b < Cfg::kBoxes; ++b) {
+      for (int b = 0; b < Cfg::kBoxes; ++b)
         tma_load_3d(sbase + Cfg::kSmemFixed0 + b * kBoxBytes, &tm_q, fbar, b * kBoxCols, i * kBlockM, bh);
-        tma_load_3d(sbase + Cfg::kSmemFixed1 + b * kBoxBytes, &tm_do, fbar, b * kBoxCols, i * kBlockM, bh);
-      }
+      bool do_issued = false;
       // K_it and V_it in turn (V_it's slot frees before K_it+1's: dP is done before dQ).
       int issued_k = 0, issued_v = 0;
       for (int it = 0; it < nk; ++it) {
@@ -1112,6 +1136,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int b = 0; b < Cfg::kBoxes; ++b)
           tma_load_3d(k_addr(it) + b * kBoxBytes, &tm_k, kfull, b * kBoxCols, it * kBlockM, bh);
         issued_k = it + 1;
+        if (!do_issued) {
+          mbar_arrive_expect_tx(fbar1, Cfg::kTileBytes);
+#pragma unroll
+          for (int b = 0; b < Cfg::kBoxes; ++b)
+            tma_load_3d(sbase + Cfg::kSmemFixed1 + b * kBoxBytes, &tm_do, fbar1, b * kBoxCols,
+                        i * kBlockM, bh);
+          do_issued = true;
+        }
         const int sv = it % Cfg::kDqSlotsV;
         if (!bwd_wait(smem_u32(&bars->v_empty[sv]), ((it / Cfg::kDqSlotsV) & 1) ^ 1, abort,
                       p.status))
@@ -1125,6 +1157,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       int no_abort = 0;
       bwd_wait(fbar, 0, &no_abort, p.status);
+      if (do_issued) bwd_wait(fbar1, 0, &no_abort, p.status);
       for (int it = max(0, issued_k - Cfg::kDqSlotsK); it < issued_k; ++it)
         bwd_wait(smem_u32(&bars->stage_full[it % Cfg::kDqSlotsK]), (it / Cfg::kDqSlotsK) & 1,
                   &no_abort, p.status);
@@ -1165,13 +1198,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //   S(it+1) (once the element-wise warps hold S(it) in registers)  |
     //   dQ += dS(it) K_it (dS stored over dP(it))  |  dP(it+1)
     // so the next S is computed while dS(it) is being formed.
-    bool ok = wait_bar(&bars->fixed_full, 0) && wait_k(0) && wait_v(0);
+    bool ok = wait_bar(&bars->fixed_full, 0) && wait_k(0);
     if (ok) {
       issue_n(tS, dQ, k_desc(0, 16));
       mma_commit_elect(smem_u32(&bars->s_full));
-      issue_n(tDP, dDO, v_desc(0));
-      mma_commit_elect(smem_u32(&bars->dp_full));
-      release_v(0);
+      if ((ok = wait_bar(&bars->fixed1_full, 0) && wait_v(0))) {
+        issue_n(tDP, dDO, v_desc(0));
+        mma_commit_elect(smem_u32(&bars->dp_full));
+        release_v(0);
+      }
     }
     for (int it = 0; ok && it < nk; ++it) {
       const bool more = it + 1 < nk;
