@@ -16,7 +16,8 @@ constexpr int kKvBars = 8;
 constexpr int kKvFullBars = 16;
 
 struct AttnTcBarriers {
-  uint64_t q_full;
+  uint64_t q_full;       // TMA -> MMA: Q tile 0 is in shared memory
+  uint64_t q1_full;      // ... Q tile 1 (loaded after the first K tile, which S_0(0) needs)
   // s_full and p_ready come in pairs per tile, used alternately: S_t(j) completes on
   // s_full[2 t + (j & 1)] and is waited with parity (j >> 1) & 1, P_t(j) likewise on
   // p_ready.  With three S buffers the MMA warp issues S_t(j+1) before it needs P_t(j),
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->q_full), 1);
+    mbar_init(smem_u32(&bars->q1_full), 1);
     for (int t = 0; t < 2; ++t) {
       for (int u = 0; u < 2; ++u) {
         mbar_init(smem_u32(&bars->s_full[2 * t + u]), 1);
@@ -184,14 +186,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_o);
+      // Q_0, the first K (and V) tile, then Q_1: the first S product needs only Q_0 and
+      // K_0.
       const uint32_t qbar = smem_u32(&bars->q_full);
-      mbar_arrive_expect_tx(qbar, 2 * Cfg::kQTileBytes);
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
+      const uint32_t q1bar = smem_u32(&bars->q1_full);
+      auto load_q = [&](int t, uint32_t bar) {
+        mbar_arrive_expect_tx(bar, Cfg::kQTileBytes);
 #pragma unroll
         for (int b = 0; b < Cfg::kBoxes; ++b)
-          tma_load_3d(sbase + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0) + b * kBoxBytes, &tm_q, qbar,
+          tma_load_3d(sbase + (t ? Cfg::kSmemQ1 : Cfg::kSmemQ0) + b * kBoxBytes, &tm_q, bar,
                       b * kBoxCols, qb * 2 * kBlockM + t * kBlockM, bh);
+      };
+      load_q(0, qbar);
+      bool q1_issued = false;
       int no_abort = 0;
       if constexpr (Cfg::kPairWait) {
         // Pair j: K_j into ring slot 2j % kSlots and V_j into the next slot, both landing
@@ -216,10 +223,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                           (jlo + j) * BN, bh);
           }
           issued = j + 1;
+          if (!q1_issued) {
+            load_q(1, q1bar);
+            q1_issued = true;
+          }
         }
         // Every issued copy must land before the block's shared memory goes away: the
         // pairs not yet known to be released (the ring holds fewer than kKvBars pairs).
+        if (!q1_issued) load_q(1, q1bar);  // (no pair issued: Q_1 still completes its barrier)
         mbar_wait(qbar, 0, &no_abort, p.status);
+        mbar_wait(q1bar, 0, &no_abort, p.status);
         for (int j = max(0, issued - kKvBars); j < issued; ++j)
           mbar_wait(smem_u32(&bars->kv_full[j % kKvBars]), (j / kKvBars) & 1, &no_abort, p.status);
       } else {
@@ -240,10 +253,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tma_load_3d(dst + b * Cfg::kKvBoxBytes, tm, full, b * kBoxCols, (jlo + (it >> 1)) * BN,
                         bh);
           issued = it + 1;
+          if (!q1_issued) {
+            load_q(1, q1bar);
+            q1_issued = true;
+          }
         }
         // Every issued copy must land before the block's shared memory goes away: the
         // last load issued into each slot.
+        if (!q1_issued) load_q(1, q1bar);  // (no load issued: Q_1 still completes its barrier)
         mbar_wait(qbar, 0, &no_abort, p.status);
+        mbar_wait(q1bar, 0, &no_abort, p.status);
         for (int it = max(0, issued - Cfg::kSlots); it < issued; ++it)
           mbar_wait(smem_u32(&bars->kv_full[it % Cfg::kSlots]), (it / Cfg::kSlots) & 1, &no_abort,
                     p.status);
@@ -313,6 +332,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->q_full), 0, abort, p.status));
     if constexpr (Cfg::kPairWait) ok = ok && wait_kv(0);
     else ok = ok && wait_full(0);
+    // Q_1 lands after Q_0 and the first K/V tile: waited for once, before the first S_1.
+    bool q1_ready = false;
+    auto wait_q1 = [&]() {
+      if (!q1_ready) {
+        q1_ready = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->q1_full), 0, abort, p.status));
+        if (q1_ready) tc_fence_after();
+      }
+      return q1_ready;
+    };
     if constexpr (NS == 1) {
       // One S/P buffer (BN = 256 at d = 64): the tiles take turns.  The S at position q
       // of the sequence S_0(0), S_1(0), S_0(1), ... (S_1(j) at min(j+1, n0) + j once tile 0
@@ -324,8 +352,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (ok) {
         tc_fence_after();
         const int t0 = pos_tile(0);
-        issue_s(tbase, t0 ? dQ1 : dQ0, 0);
-        mma_commit_elect(smem_u32(&bars->s_full[2 * t0]));
+        if (t0 == 0 || (ok = wait_q1())) {
+          issue_s(tbase, t0 ? dQ1 : dQ0, 0);
+          mma_commit_elect(smem_u32(&bars->s_full[2 * t0]));
+        }
       }
       for (int q = 0; ok && q < npos; ++q) {
         const int t = pos_tile(q), j = pos_j(q);
@@ -343,6 +373,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!(ok = wait_kv(jn))) break;
             tc_fence_after();
           }
+          if (tn == 1 && !(ok = wait_q1())) break;
           issue_s(tbase, tn ? dQ1 : dQ0, 2 * jn);
           mma_commit_elect(smem_u32(&bars->s_full[2 * tn + (jn & 1)]));
         }
@@ -366,8 +397,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           issue_s(colS(0), dQ0, 0);
           mma_commit_elect(smem_u32(&bars->s_full[0]));
         }
-        issue_s(colS(n0 > 0 ? 1 : 0), dQ1, 0);
-        mma_commit_elect(smem_u32(&bars->s_full[2]));
+        if ((ok = wait_q1())) {
+          issue_s(colS(n0 > 0 ? 1 : 0), dQ1, 0);
+          mma_commit_elect(smem_u32(&bars->s_full[2]));
+        }
       }
       for (int j = 0; ok && j < n1; ++j) {
         const int itV = 2 * j + 1, itK = 2 * j + 2;
@@ -405,9 +438,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           issue_s(tS0, dQ0, 0);
           mma_commit_elect(smem_u32(&bars->s_full[0]));
         }
-        issue_s(tS1, dQ1, 0);
-        mma_commit_elect(smem_u32(&bars->s_full[2]));
-        mma_commit_elect(smem_u32(&bars->slot_empty[0]));
+        if ((ok = wait_q1())) {
+          issue_s(tS1, dQ1, 0);
+          mma_commit_elect(smem_u32(&bars->s_full[2]));
+          mma_commit_elect(smem_u32(&bars->slot_empty[0]));
+        }
       }
       for (int j = 0; ok && j < n1; ++j) {
         const int itV = 2 * j + 1, itK = 2 * j + 2;
