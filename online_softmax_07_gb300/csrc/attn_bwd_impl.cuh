@@ -354,9 +354,11 @@ __device__ __forceinline__ void bwd_work(const AttnBwdParams& p, bool low_first,
 }
 
 // D_i = sum_c dO_ic O_ic and LSE_i * log2(e); rows N .. n_pad-1 of each head get D = 0 and
-// +inf.  A warp takes kPrepRows query rows and issues all their loads before reducing any,
-// so that enough bytes are in flight to stream O and dO at HBM speed.
-constexpr int kPrepRows = 4;
+// +inf.  A warp takes kPrepRows<D> query rows and issues all their loads before reducing
+// any, so that enough bytes are in flight to stream O and dO at HBM speed (eight rows at
+// d = 64, whose rows are half as long; four at d = 128, where eight measured slower).
+template <int D>
+constexpr int kPrepRows = D == 64 ? 8 : 4;
 
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __restrict__ o,
@@ -370,22 +372,22 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __re
   constexpr int kPer = D / 32;  // 16-bit elements per lane and row: 2 or 4
   const long long total = static_cast<long long>(BH) * n_pad;
   const long long row0 =
-      (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kPrepRows;
+      (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kPrepRows<D>;
   const int lane = threadIdx.x & 31;
   if (dq_acc != nullptr) {
     // One-pass backward (d = 64): the fp32 dQ accumulator rows of these query rows start
     // at zero (64 floats = 16 float4 per row).
 #pragma unroll
-    for (int r = 0; r < kPrepRows; ++r) {
+    for (int r = 0; r < kPrepRows<D>; ++r) {
       const long long row = row0 + r;
       if (row < total && lane < 16)
         reinterpret_cast<float4*>(dq_acc + row * 64)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  uint32_t av[kPrepRows][kPer / 2], bv[kPrepRows][kPer / 2];
-  bool real[kPrepRows];
+  uint32_t av[kPrepRows<D>][kPer / 2], bv[kPrepRows<D>][kPer / 2];
+  bool real[kPrepRows<D>];
 #pragma unroll
-  for (int r = 0; r < kPrepRows; ++r) {
+  for (int r = 0; r < kPrepRows<D>; ++r) {
     const long long row = row0 + r;
     const long long bh = row / n_pad;
     const int q = static_cast<int>(row - bh * n_pad);
@@ -405,9 +407,9 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __re
       }
     }
   }
-  float acc[kPrepRows];
+  float acc[kPrepRows<D>];
 #pragma unroll
-  for (int r = 0; r < kPrepRows; ++r) {
+  for (int r = 0; r < kPrepRows<D>; ++r) {
     acc[r] = 0.f;
 #pragma unroll
     for (int i = 0; i < kPer / 2; ++i) {
@@ -421,11 +423,11 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __re
 #pragma unroll
   for (int sh = 16; sh > 0; sh >>= 1)
 #pragma unroll
-    for (int r = 0; r < kPrepRows; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], sh);
-  if (lane < kPrepRows) {
+    for (int r = 0; r < kPrepRows<D>; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], sh);
+  if (lane < kPrepRows<D>) {
     float mine = acc[0];
 #pragma unroll
-    for (int r = 1; r < kPrepRows; ++r) mine = (lane == r) ? acc[r] : mine;
+    for (int r = 1; r < kPrepRows<D>; ++r) mine = (lane == r) ? acc[r] : mine;
     const long long row = row0 + lane;
     if (row < total) {
       const long long bh = row / n_pad;
@@ -1398,7 +1400,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   p.dd = kFused ? nullptr : ws + rows;
   p.aug = reinterpret_cast<uint16_t*>(kFused ? ws : ws + 2 * rows);
   p.dq_acc = kFused ? ws + 8 * rows : nullptr;
-  attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((rows + 8 * kPrepRows - 1) / (8 * kPrepRows)),
+  attn_bwd_prep_kernel<D, F16><<<static_cast<unsigned>((rows + 8 * kPrepRows<D> - 1) / (8 * kPrepRows<D>)),
                                  256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
       const_cast<float*>(p.lse2), const_cast<float*>(p.dd), p.BH, p.N, p.n_pad, p.dq_acc, p.aug,
