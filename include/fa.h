@@ -21,15 +21,18 @@
  *    (Same page, §四, §4.1 and §4.2.)
  *
  * Conventions common to every call:
- *  - Every pointer passed to a compute call is a DEVICE pointer owned by the caller.
- *    The library allocates no device memory: it keeps one status word per device in
- *    static device memory.
+ *  - Every pointer passed to a compute call is a DEVICE pointer owned by the caller
+ *    (fa_fwd_host takes its tensors in host memory and a device workspace). The
+ *    library allocates no device memory: its device state is one status word per
+ *    device and the 64 MiB scratch array of fa_fwd_splitkv_static, both in static
+ *    device memory.
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream). The return
  *    value reports argument errors (checked on the host, nothing is launched) and
  *    launch errors only. Errors the kernels detect while running (a bounded wait that
  *    ran out) are reported by fa_last_device_error().
  *  - Concurrent calls on different streams are allowed; the library keeps no
- *    per-call host state.
+ *    per-call host state. The exception is fa_fwd_splitkv_static, whose calls share
+ *    one scratch array (see there).
  */
 #ifndef ONLINE_SOFTMAX_07_GB300_FA_H
 #define ONLINE_SOFTMAX_07_GB300_FA_H
