@@ -45,6 +45,10 @@ def test_host_path_into_given_buffers_and_without_lse():
     assert torch.equal(o1, o2)
     o_d, _ = osf.attention_forward(q.cuda(), k.cuda(), v.cuda(), scale=0.2)
     assert torch.equal(o1, o_d.cpu())
+    # Device tensors without LSE (the kernels skip the LSE writes): the same O.
+    o_d2, l_d2 = osf.attention_forward(q.cuda(), k.cuda(), v.cuda(), scale=0.2, with_lse=False)
+    assert l_d2 is None
+    assert torch.equal(o1, o_d2.cpu())
 
 
 @pytest.mark.parametrize("B,H,N,d,causal", [
