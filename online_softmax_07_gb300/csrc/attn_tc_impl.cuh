@@ -588,15 +588,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint64_t negm2 = f2_pack(-m2, -m2);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
       // The W scores in s are keys c0 .. c0 + W - 1.
+      // 64 keys (32 packed columns) per TMEM store; 32 keys with 256-key tiles, where the
+      // larger packed block would not fit beside the 128 scores held (it spilled).
+      constexpr int kStoreKeys = BN == 256 ? 32 : 64;
       auto exp_chunk = [&](int c0, auto width) {
         constexpr int W = decltype(width)::value;
-        // 64 keys (32 packed columns) per TMEM store.
 #pragma unroll
-        for (int h = 0; h < W / 64; ++h) {
-          uint32_t pk[32];
+        for (int h = 0; h < W / kStoreKeys; ++h) {
+          uint32_t pk[kStoreKeys / 2];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = 64 * h + 2 * i;
+          for (int i = 0; i < kStoreKeys / 2; ++i) {
+            const int c = kStoreKeys * h + 2 * i;
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negm2), x0, x1);
             const float p0 = ex2_approx(x0);
@@ -604,7 +606,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
             pk[i] = pack_elem2<F16>(p0, p1);
           }
-          tmem_st32(tS + c0 / 2 + 32 * h, pk);
+          if constexpr (kStoreKeys == 64) tmem_st32(tS + c0 / 2 + 32 * h, pk);
+          else tmem_st16(tS + c0 / 2 + 16 * h, pk);
         }
       };
       exp_chunk(0, ChunkW{});
